@@ -1,0 +1,249 @@
+// common.cuh -- sm_103a building blocks shared by the LoRA delta kernels:
+// mbarrier waits with a time limit, TMA tile copies, tcgen05 MMA / TMEM
+// access, shared-memory matrix descriptors, and the fixed summation tree.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lora {
+
+// ----------------------------------------------------------------- limits
+// A wait on an mbarrier gives up after this long (ns of %globaltimer). The
+// kernels finish in micro- to milliseconds; reaching the limit means the
+// pipeline is broken, and the kernel reports it instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s, for teardown waits
+
+// Status word codes (first word of the caller's workspace).
+constexpr uint32_t kDevTimeout = 1u;
+
+// ------------------------------------------------------------ small utils
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+__device__ __forceinline__ uint32_t warp_id() {
+  return __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
+}
+
+// --------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0u;
+}
+
+// Per-CTA abort state: a flag in shared memory and the caller's status word.
+struct Abort {
+  volatile uint32_t* flag;   // shared memory
+  uint32_t* status;          // global (may be null)
+};
+
+// Slow path of a bounded wait. Returns false when the CTA is aborting: either
+// this wait ran past its limit (then it raises the abort flag and records
+// `site` in the status word) or another thread of the CTA already did.
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Abort ab, uint32_t site,
+                                       uint64_t limit_ns, bool honour_abort) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (honour_abort && *ab.flag) return false;
+      if (global_ns() - t0 > limit_ns) {
+        *ab.flag = 1u;
+        if (ab.status) *reinterpret_cast<volatile uint32_t*>(ab.status) = (site << 8) | kDevTimeout;
+        return false;
+      }
+    }
+  }
+}
+
+// Wait for the phase of `bar` with the given parity to complete, for at most
+// kWaitLimitNs. False means "abort": skip the work, keep the control flow.
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_slow(bar, parity, ab, site, kWaitLimitNs, true);
+}
+// Teardown variant: ignores the abort flag, shorter limit.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_slow(bar, parity, ab, site, kDrainLimitNs, false);
+}
+
+// Pipeline ring position: stage index and the phase parity of that stage.
+struct Ring {
+  uint32_t idx = 0, phase = 0;
+  template <int N>
+  __device__ __forceinline__ void next() {
+    if (++idx == N) { idx = 0; phase ^= 1u; }
+  }
+};
+
+// ------------------------------------------------------------------- TMA
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 2-D tiled load into shared memory; completes `bar`'s transaction count.
+// x (innermost coordinate) must be a multiple of 16 bytes / element size.
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+// 2-D tiled store from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store(const CUtensorMap* m, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA / tensor core) reads of the same bytes.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, BF16 inputs, FP32 accumulate. Issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// Load 8 consecutive 32-bit TMEM columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Make later uses of loaded registers depend on the preceding tcgen05.wait::ld.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (16-byte units), descriptor version 1, layout type.
+constexpr uint32_t kLayoutNone = 0, kLayoutSW128 = 2, kLayoutSW64 = 4, kLayoutSW32 = 6;
+__host__ __device__ constexpr uint32_t layout_for_span(int span_bytes) {
+  return span_bytes == 128 ? kLayoutSW128 : (span_bytes == 64 ? kLayoutSW64 : kLayoutSW32);
+}
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(layout) << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: BF16 A and B, FP32 D, dense; a_mn / b_mn
+// select MN-major (1) or K-major (0) operands.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------ arithmetic
+// dV = bf16_rn(fp32(dY) * alpha) on 8 packed BF16 values (one 16-byte chunk).
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float alpha) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16);
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    const __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(lo, alpha), __fmul_rn(hi, alpha));
+    w[i] = *reinterpret_cast<const uint32_t*>(&p);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The fixed summation tree. Leaves are 16-term tensor-core dot products
+// (fresh accumulator each), combined by the canonical pairwise tree over the
+// leaf index: level l adds node i and node i + 2^l when i is a multiple of
+// 2^(l+1) (a node with no partner passes up unchanged). Group of 4 leaves:
+__device__ __forceinline__ float tree4(float l0, float l1, float l2, float l3) {
+  return __fadd_rn(__fadd_rn(l0, l1), __fadd_rn(l2, l3));
+}
+
+}  // namespace lora

@@ -1,0 +1,304 @@
+// down.cu -- the reductions over the long dimension:
+//   U  partials: U[m][r]  = sum_k x[m][k] * a[r][k]      (forward "U = X @ A^T")
+//   dU partials: dU[m][r] = sum_n dv[m][n] * b[n][r],   dv = bf16(dy * alpha)
+// (page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA + Triton, both
+// batch-invariant", section "Summary"; dV is formed in shared memory and never
+// stored, rounding point "D4").
+//
+// Work unit = (128-row tile, slice of the reduction dimension). A persistent
+// CTA streams the unit's 128 x 64 BF16 input tiles through a TMA/mbarrier
+// ring (128-byte swizzle, 16-byte chunks, one pass over the input), issues
+// four tcgen05 MMAs (M=128, N=RP, K=16) per tile, each into its own fresh TMEM
+// accumulator (a "leaf" = one 16-term dot product), and eight epilogue warps
+// add the leaves with the canonical pairwise tree in FP32 (round to nearest).
+// The unit's result is one FP32 partial per (row, r); a separate combine
+// launch finishes the same tree across slices and rounds to BF16.
+//
+// Warp roles: 0 = TMA producer, 1 = MMA issuer (and TMEM owner),
+// 2..9 = epilogue (two warps per TMEM lane quarter, half of the columns each),
+// 10..13 = dV transform (dU only).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+template <int RP, bool DV>
+struct DownCfg {
+  static constexpr int kBM = 128, kBK = 64;
+  static constexpr int kInBytes = kBM * kBK * 2;     // 16 KB input tile
+  static constexpr int kWBytes = RP * kBK * 2;       // RP x 64 weight tile
+  static constexpr int kStageBytes = kInBytes + kWBytes;
+  static constexpr int kStages = RP == 64 ? 8 : (RP == 32 ? 9 : 10);
+  static constexpr int kLeaves = kBK / 16;
+  static constexpr int kGroupCols = kLeaves * RP;
+  static constexpr int kGroups = 512 / kGroupCols;
+  static constexpr int kSlice = down_slice(RP);
+  static constexpr int kGS = kSlice / kBK;            // leaf groups per slice (power of two)
+  static constexpr int kLevels = kGS == 16 ? 4 : (kGS == 8 ? 3 : (kGS == 4 ? 2 : (kGS == 2 ? 1 : 0)));
+  static constexpr int kEpiWarps = 8, kXfWarps = DV ? 4 : 0;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kXfWarps);
+  static constexpr int kCPT = RP / 2;                 // columns per epilogue thread
+  static constexpr int kCH = kCPT < 16 ? kCPT : 16;   // columns per TMEM load batch
+  static constexpr int kWSpan = DV ? RP * 2 : 128;    // swizzle span of the weight tile
+  static constexpr int kNumBars = 3 * kStages + 2 * kGroups + 1;
+  static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
+  static_assert((1 << kLevels) == kGS, "slice must hold a power-of-two number of tiles");
+  static_assert(kGroups >= 2, "TMEM ring too shallow");
+};
+
+template <int RP, bool DV>
+__global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
+    down_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_w,
+                float* __restrict__ part, int M, int Kred, int n_mt, int n_sl, float alpha, uint32_t* status) {
+  using C = DownCfg<RP, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;                      // 1024-byte aligned tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (base - raw) + size_t(C::kStages) * C::kStageBytes);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto ready = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * C::kStages + s); };
+  auto tfull = [&](int g) { return bar0 + 8u * (3 * C::kStages + g); };
+  auto tempty = [&](int g) { return bar0 + 8u * (3 * C::kStages + C::kGroups + g); };
+  const uint32_t drain = bar0 + 8u * (3 * C::kStages + 2 * C::kGroups);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(ready(s), C::kXfWarps > 0 ? C::kXfWarps : 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int g = 0; g < C::kGroups; ++g) {
+      mbar_init(tfull(g), 1);
+      mbar_init(tempty(g), C::kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    mbar_fence_init();
+    prefetch_map(&tm_in);
+    prefetch_map(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, status};
+  const int total = n_mt * n_sl;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+      Ring r;
+      uint32_t issued = 0, parities = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const int mt = u % n_mt, sl = u / n_mt;
+        const int k0 = sl * C::kSlice;
+        const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (wait(empty(r.idx), r.phase ^ 1u, ab, 1)) {
+            const uint32_t st = base + r.idx * C::kStageBytes;
+            const int k = k0 + kb * C::kBK;
+            mbar_expect_tx(full(r.idx), C::kStageBytes);
+            tma_load(st, &tm_in, full(r.idx), k, mt * C::kBM, pol_stream);
+            if (DV) tma_load(st + C::kInBytes, &tm_w, full(r.idx), 0, k, pol_keep);   // b[n][r], n = k..k+63
+            else tma_load(st + C::kInBytes, &tm_w, full(r.idx), k, 0, pol_keep);      // a[r][k..k+63]
+            issued |= 1u << r.idx;
+            parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
+          }
+          r.next<C::kStages>();
+        }
+      }
+      // never leave with a copy in flight into this CTA's shared memory
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued & (1u << s)) wait_drain(full(s), (parities >> s) & 1u, ab, 2);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, RP, 0, DV ? 1 : 0);
+      constexpr uint32_t w_layout = layout_for_span(C::kWSpan);
+      Ring r, g;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const int sl = u / n_mt;
+        const int k0 = sl * C::kSlice;
+        const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 3);
+          ok = ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 4);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t st = base + r.idx * C::kStageBytes;
+            const uint32_t d = tmem + g.idx * C::kGroupCols;
+#pragma unroll
+            for (int j = 0; j < C::kLeaves; ++j) {
+              // input tile: K-major, 128-byte swizzle; K step j = +32 bytes inside the swizzle atom
+              const uint64_t adesc = smem_desc(st + 32u * j, 16u, 1024u, kLayoutSW128);
+              uint64_t wdesc;
+              if (DV)   // b tile [64 n][RP]: MN-major (r contiguous), 8-row groups of one swizzle span
+                wdesc = smem_desc(st + C::kInBytes + j * 16u * C::kWSpan, 8u * C::kWSpan, 8u * C::kWSpan, w_layout);
+              else      // a tile [RP][64 k]: K-major, 128-byte swizzle
+                wdesc = smem_desc(st + C::kInBytes + 32u * j, 16u, 1024u, kLayoutSW128);
+              mma_bf16(d + j * RP, adesc, wdesc, idesc, 0u);   // fresh accumulator: one leaf
+            }
+            mma_commit(empty(r.idx));
+            mma_commit(tfull(g.idx));
+          }
+          r.next<C::kStages>();
+          g.next<C::kGroups>();
+        }
+      }
+      mma_commit(drain);                 // all MMAs issued above have completed ...
+      wait_drain(drain, 0u, ab, 5);      // ... before TMEM is released
+    }
+  } else if (warp < 2 + C::kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                            // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;                     // column half
+    const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + h * C::kCPT;
+    Ring g;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int mt = u % n_mt, sl = u / n_mt;
+      const int k0 = sl * C::kSlice;
+      const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+      float stack[C::kLevels > 0 ? C::kLevels : 1][C::kCPT];
+      float node[C::kCPT];
+      bool ok_all = true;
+#pragma unroll
+      for (int i = 0; i < C::kGS; ++i) {
+        if (i < nkb) {
+          const bool ok = __all_sync(0xffffffffu, wait(tfull(g.idx), g.phase, ab, 6));   // warp-uniform: tcgen05.ld is .aligned
+          ok_all = ok_all && ok;
+          tc_fence_after();
+#pragma unroll
+          for (int ch = 0; ch < C::kCPT / C::kCH; ++ch) {
+            uint32_t v[C::kLeaves][C::kCH / 8][8];
+            if (ok) {
+#pragma unroll
+              for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+                for (int b8 = 0; b8 < C::kCH / 8; ++b8)
+                  tmem_ld8(tbase + g.idx * C::kGroupCols + j * RP + ch * C::kCH + b8 * 8, v[j][b8]);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+                for (int b8 = 0; b8 < C::kCH / 8; ++b8)
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) v[j][b8][e] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+              for (int b8 = 0; b8 < C::kCH / 8; ++b8) reg_fence(v[j][b8]);
+#pragma unroll
+            for (int c = 0; c < C::kCH; ++c)
+              node[ch * C::kCH + c] = tree4(__uint_as_float(v[0][c / 8][c % 8]), __uint_as_float(v[1][c / 8][c % 8]),
+                                            __uint_as_float(v[2][c / 8][c % 8]), __uint_as_float(v[3][c / 8][c % 8]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (ok && lane == 0) mbar_arrive(tempty(g.idx));
+          g.next<C::kGroups>();
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::kCPT; ++c) node[c] = 0.0f;   // zero leaves: neutral in the tree
+        }
+        // canonical pairwise tree over the slice's groups: merge once per trailing one of i
+#pragma unroll
+        for (int l = 0; l < C::kLevels; ++l) {
+          if (((i >> l) & 1) == 0) {
+#pragma unroll
+            for (int c = 0; c < C::kCPT; ++c) stack[l][c] = node[c];
+            break;
+          }
+#pragma unroll
+          for (int c = 0; c < C::kCPT; ++c) node[c] = __fadd_rn(stack[l][c], node[c]);
+        }
+      }
+      // after the last group (i = kGS - 1, all ones) `node` holds the slice sum
+      const int row = mt * C::kBM + q * 32 + lane;
+      if (ok_all && row < M) {
+        float4* dst = reinterpret_cast<float4*>(part + (size_t(sl) * M + row) * RP + h * C::kCPT);
+#pragma unroll
+        for (int c = 0; c < C::kCPT; c += 4) dst[c / 4] = make_float4(node[c], node[c + 1], node[c + 2], node[c + 3]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- dV = bf16(dY*alpha)
+    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);   // 0..127
+    Ring r;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int sl = u / n_mt;
+      const int k0 = sl * C::kSlice;
+      const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (wait(full(r.idx), r.phase, ab, 7)) {
+          uint4* tile = reinterpret_cast<uint4*>(smem_raw + (base - raw) + size_t(r.idx) * C::kStageBytes);
+#pragma unroll
+          for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = scale_bf16x8(tile[t + 128 * e], alpha);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ready(r.idx));
+        }
+        r.next<C::kStages>();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int RP, bool DV>
+static cudaError_t launch_one(const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred, float alpha,
+                              uint32_t* status, int grid, cudaStream_t st) {
+  using C = DownCfg<RP, DV>;
+  const int n_mt = int(ceil_div(M, C::kBM)), n_sl = int(ceil_div(Kred, C::kSlice));
+  down_kernel<RP, DV><<<grid, C::kThreads, C::kSmem, st>>>(in, w, part, M, Kred, n_mt, n_sl, alpha, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
+                        float alpha, uint32_t* status, int grid, cudaStream_t st) {
+  switch (RP * 2 + (dv ? 1 : 0)) {
+    case 32: return launch_one<16, false>(in, w, part, M, Kred, alpha, status, grid, st);
+    case 33: return launch_one<16, true>(in, w, part, M, Kred, alpha, status, grid, st);
+    case 64: return launch_one<32, false>(in, w, part, M, Kred, alpha, status, grid, st);
+    case 65: return launch_one<32, true>(in, w, part, M, Kred, alpha, status, grid, st);
+    case 128: return launch_one<64, false>(in, w, part, M, Kred, alpha, status, grid, st);
+    case 129: return launch_one<64, true>(in, w, part, M, Kred, alpha, status, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int RP, bool DV>
+static cudaError_t prep_one() {
+  return cudaFuncSetAttribute(down_kernel<RP, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(DownCfg<RP, DV>::kSmem));
+}
+
+cudaError_t prepare_down() {
+  cudaError_t e;
+  if ((e = prep_one<16, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<16, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<64, false>()) != cudaSuccess) return e;
+  return prep_one<64, true>();
+}
+
+}  // namespace lora

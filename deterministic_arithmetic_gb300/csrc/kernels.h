@@ -1,0 +1,60 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units. Not installed; the public interface is include/lora_delta.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lora {
+
+// Rank R is padded to RP in {16, 32, 64} inside the kernels (tcgen05 needs N
+// and K to be multiples of 16); padded rows/columns are TMA zero fill.
+constexpr int padded_rank(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
+
+// Down-projection (U, dU): the reduction over K (or N) is cut into slices of
+// this many elements; each slice is one work unit and leaves one FP32 partial.
+// Slices hold a power-of-two number of 16-element leaves, so the canonical
+// tree over all leaves does not depend on the slice length.
+constexpr int down_slice(int RP) { return RP == 64 ? 256 : 1024; }
+// Weight gradients (dA, dB): rows of the batch are cut into fixed chunks.
+constexpr int kWgradChunk = 256;
+// Up-projection tile width (N direction) per padded rank.
+constexpr int up_bn(int RP) { return 256 / (RP / 16); }
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Work-unit counts (all launches use persistent CTAs over units).
+inline int64_t down_units(int64_t M, int64_t Kred, int RP) { return ceil_div(M, 128) * ceil_div(Kred, down_slice(RP)); }
+inline int64_t up_units(int64_t M, int64_t Nout, int RP) { return ceil_div(M, 128) * ceil_div(Nout, up_bn(RP)); }
+inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil_div(M, kWgradChunk) * ceil_div(C, 128); }
+
+// Launchers (return the launch error, if any). `status` is the device status
+// word; `grid` the number of persistent CTAs.
+cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
+                        float alpha, uint32_t* status, int grid, cudaStream_t st);
+cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int M,
+                      int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st);
+cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int C,
+                         float alpha, uint32_t* status, int grid, cudaStream_t st);
+
+// Combine jobs: canonical tree over S partials.
+struct CombineJob {
+  const float* part;   // partials
+  void* out;           // output
+  int S;               // number of partials
+  int rows, cols;      // output is rows x cols (cols = R for U/dU and dB; K for dA)
+  int RP;              // padded rank (partials' rank dimension)
+  int mode;            // 0: part[S][rows][RP] -> bf16 out[rows][R=cols]
+                       // 1: part[S][RP][rows] -> fp32 out[rows][R=cols]   (dB: rows = N)
+                       // 2: part[S][RP][cols] -> fp32 out[rows=R][cols]   (dA: cols = K)
+};
+cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st);
+
+// Raise the dynamic shared-memory limit of every kernel instance in a
+// translation unit (once per device, with that device current).
+cudaError_t prepare_down();
+cudaError_t prepare_up();
+cudaError_t prepare_wgrad();
+
+}  // namespace lora

@@ -1,0 +1,263 @@
+// up.cu -- the rank-R expansions (write-bound):
+//   dY_lora[m][n] = fp32(sum_r u[m][r] * b[n][r]) * alpha   (forward "(U @ B^T) * alpha")
+//   dX[m][k]      = fp32(sum_r du[m][r] * a[r][k])          (backward "dX = dU @ A")
+// (page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA + Triton, both
+// batch-invariant", section "Summary"; the alpha scale is fused into the
+// epilogue, as that page's "Benchmark" section proposes.)
+//
+// Work unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16). The
+// operands (U or dU tile, B or A tile) are a few KB from L2; the unit is one
+// tcgen05 MMA per 16-wide slice of R (M=128, N=BN, K=16), each into its own
+// TMEM accumulator, summed by the canonical pairwise tree. Eight epilogue
+// warps read TMEM, finish the tree (and the alpha multiply), stage 128 x 32
+// FP32 boxes in 128-byte-swizzled shared memory and write them with TMA
+// stores, so every output byte is written exactly once, in full lines.
+//
+// Warp roles: 0 = TMA producer, 1 = MMA issuer (TMEM owner), 2..9 = epilogue.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+template <int RP, bool DX>
+struct UpCfg {
+  static constexpr int kBM = 128;
+  static constexpr int kLeaves = RP / 16;
+  static constexpr int kBN = up_bn(RP);
+  static constexpr int kSpan = RP * 2;                 // bytes of one operand row (r contiguous)
+  static constexpr int kABytes = kBM * RP * 2;         // U / dU tile [128][RP]
+  static constexpr int kBBytes = kBN * RP * 2;         // B tile [BN][RP] or A tile [RP][BN]
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 2;
+  static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
+  static constexpr int kBufs = 512 / kBufCols;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kHalfCols = kBN / 2;
+  static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
+  static constexpr int kChunks = kHalfCols / kChunk;
+  static constexpr int kStg = 3;                       // staging buffers per column half
+  static constexpr int kStgBytes = kBM * kChunk * 4;   // 16 KB
+  static constexpr int kNumBars = 2 * kStages + 2 * kBufs;
+  static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * kStg * kStgBytes + 1024 + kNumBars * 8 + 16;
+  static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
+  static_assert(kBufs == 2, "double-buffered accumulators");
+};
+
+template <int RP, bool DX>
+__global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
+    up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const __grid_constant__ CUtensorMap tm_out, int M, int Nout, int n_mt, int n_nt, float alpha,
+              uint32_t* status) {
+  using C = UpCfg<RP, DX>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t stg0 = base + C::kStages * C::kStageBytes;        // staging buffers [2 halves][kStg]
+  uint8_t* stg_ptr = gbase + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_ptr + 2 * C::kStg * C::kStgBytes);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kBufs + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < C::kBufs; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), C::kEpiWarps);
+    }
+    *abort_flag = 0u;
+    mbar_fence_init();
+    prefetch_map(&tm_a);
+    prefetch_map(&tm_b);
+    prefetch_map(&tm_out);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, status};
+  const int total = n_mt * n_nt;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      Ring r;
+      uint32_t issued = 0, parities = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const int mt = u / n_nt, nt = u % n_nt;
+        if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
+          const uint32_t st = base + r.idx * C::kStageBytes;
+          mbar_expect_tx(full(r.idx), C::kStageBytes);
+          tma_load(st, &tm_a, full(r.idx), 0, mt * C::kBM, pol);                    // u/du rows
+          if (DX) {
+#pragma unroll
+            for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
+              tma_load(st + C::kABytes + i * (RP * 128), &tm_b, full(r.idx), nt * C::kBN + 64 * i, 0, pol);
+          } else {
+            tma_load(st + C::kABytes, &tm_b, full(r.idx), 0, nt * C::kBN, pol);    // b rows n..n+BN
+          }
+          issued |= 1u << r.idx;
+          parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
+        }
+        r.next<C::kStages>();
+      }
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued & (1u << s)) wait_drain(full(s), (parities >> s) & 1u, ab, 12);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, C::kBN, 0, DX ? 1 : 0);
+      constexpr uint32_t lay = layout_for_span(C::kSpan);
+      Ring r, b;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        bool ok = wait(full(r.idx), r.phase, ab, 13);
+        ok = ok && wait(tempty(b.idx), b.phase ^ 1u, ab, 14);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t st = base + r.idx * C::kStageBytes;
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j) {
+            // u/du tile: K-major, rows of RP*2 bytes, swizzle span = row; K step j = +32 bytes
+            const uint64_t adesc = smem_desc(st + 32u * j, 16u, 8u * C::kSpan, lay);
+            uint64_t bdesc;
+            if (DX)   // a tile: 64-column blocks [RP rows][64 k], MN-major, 128-byte swizzle; K step = 16 rows
+              bdesc = smem_desc(st + C::kABytes + j * 2048u, RP * 128u, 1024u, kLayoutSW128);
+            else      // b tile [BN rows][RP]: K-major like the u tile
+              bdesc = smem_desc(st + C::kABytes + 32u * j, 16u, 8u * C::kSpan, lay);
+            mma_bf16(tmem + b.idx * C::kBufCols + j * C::kBN, adesc, bdesc, idesc, 0u);
+          }
+          mma_commit(empty(r.idx));
+          mma_commit(tfull(b.idx));
+        }
+        r.next<C::kStages>();
+        b.next<C::kBufs>();
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
+    const int rl = q * 32 + lane;                                   // row within the tile
+    const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+    const uint32_t my_stg = stg0 + h * C::kStg * C::kStgBytes;
+    uint8_t* my_stg_ptr = stg_ptr + h * C::kStg * C::kStgBytes;
+    int sidx = 0;
+    Ring b;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int mt = u / n_nt, nt = u % n_nt;
+      const bool ok = __all_sync(0xffffffffu, wait(tfull(b.idx), b.phase, ab, 15));
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        const int col0 = h * C::kHalfCols + c * C::kChunk;
+        const int ncol = nt * C::kBN + col0;
+        if (ncol >= Nout) break;                                     // uniform over the column half
+        uint32_t v[C::kLeaves][4][8];
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+            for (int b8 = 0; b8 < 4; ++b8) tmem_ld8(trow + b.idx * C::kBufCols + j * C::kBN + col0 + b8 * 8, v[j][b8]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+            for (int b8 = 0; b8 < 4; ++b8) reg_fence(v[j][b8]);
+        }
+        float out[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int b8 = e / 8, k = e % 8;
+          float s;
+          if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
+          else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
+          else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
+                         __uint_as_float(v[3][b8][k]));
+          out[e] = DX ? s : __fmul_rn(s, alpha);
+        }
+        if (leader) tma_store_wait_read<C::kStg - 1>();              // the buffer's previous store has read it
+        named_bar(1 + h, 128);
+        uint8_t* buf = my_stg_ptr + sidx * C::kStgBytes + rl * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)                               // 128-byte swizzle: chunk ^ (row % 8)
+          *reinterpret_cast<float4*>(buf + ((cc ^ (rl & 7)) * 16)) =
+              make_float4(out[4 * cc], out[4 * cc + 1], out[4 * cc + 2], out[4 * cc + 3]);
+        fence_proxy_async();
+        named_bar(1 + h, 128);
+        if (leader && ok) {
+          tma_store(&tm_out, my_stg + sidx * C::kStgBytes, ncol, mt * C::kBM);
+          tma_store_commit();
+        }
+        sidx = sidx + 1 == C::kStg ? 0 : sidx + 1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(tempty(b.idx));
+      b.next<C::kBufs>();
+    }
+    if (leader) tma_store_wait_all<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int RP, bool DX>
+static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int M, int Nout,
+                              float alpha, uint32_t* status, int grid, cudaStream_t st) {
+  using C = UpCfg<RP, DX>;
+  const int n_mt = int(ceil_div(M, C::kBM)), n_nt = int(ceil_div(Nout, C::kBN));
+  up_kernel<RP, DX><<<grid, C::kThreads, C::kSmem, st>>>(a, b, out, M, Nout, n_mt, n_nt, alpha, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int M,
+                      int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st) {
+  switch (RP * 2 + (dx ? 1 : 0)) {
+    case 32: return launch_one<16, false>(a, b, out, M, Nout, alpha, status, grid, st);
+    case 33: return launch_one<16, true>(a, b, out, M, Nout, alpha, status, grid, st);
+    case 64: return launch_one<32, false>(a, b, out, M, Nout, alpha, status, grid, st);
+    case 65: return launch_one<32, true>(a, b, out, M, Nout, alpha, status, grid, st);
+    case 128: return launch_one<64, false>(a, b, out, M, Nout, alpha, status, grid, st);
+    case 129: return launch_one<64, true>(a, b, out, M, Nout, alpha, status, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int RP, bool DX>
+static cudaError_t prep_one() {
+  return cudaFuncSetAttribute(up_kernel<RP, DX>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(UpCfg<RP, DX>::kSmem));
+}
+
+cudaError_t prepare_up() {
+  cudaError_t e;
+  if ((e = prep_one<16, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<16, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<64, false>()) != cudaSuccess) return e;
+  return prep_one<64, true>();
+}
+
+}  // namespace lora

@@ -1,0 +1,179 @@
+"""Python binding of the C ABI in ``include/lora_delta.h`` (ctypes).
+
+Argument marshalling only: every step of the operator runs in the CUDA
+kernels of ``liblora_delta.so``. PyTorch provides device memory and streams.
+There is no fallback: if the library is missing or the device is not a
+GB300, the calls raise.
+
+Names follow the C ABI: ``lora_delta_fwd(x, a, b, alpha)`` returns
+``(delta_y, u)``; ``lora_delta_bwd(dy, x, a, b, u, alpha)`` returns
+``(dx, da, db, du)`` (page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA +
+Triton, both batch-invariant", section "Summary").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblora_delta.so")
+
+LORA_OK = 0
+STATUS_NAMES = {0: "LORA_OK", 1: "LORA_ERR_NULL", 2: "LORA_ERR_SHAPE", 3: "LORA_ERR_ALIGN", 4: "LORA_ERR_RANK",
+                5: "LORA_ERR_WORKSPACE", 6: "LORA_ERR_CUDA", 7: "LORA_ERR_DEVICE", 8: "LORA_ERR_TIMEOUT"}
+
+
+class LoraDeltaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_lib().lora_status_str(code).decode()})")
+
+
+_LIB = None
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback implementation)")
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.lora_delta_fwd.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                       ctypes.c_size_t, _vp]
+        lib.lora_delta_fwd.restype = ctypes.c_int
+        lib.lora_delta_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                       _vp, _vp, ctypes.c_size_t, _vp]
+        lib.lora_delta_bwd.restype = ctypes.c_int
+        for fn in (lib.lora_delta_fwd_workspace_size, lib.lora_delta_bwd_workspace_size):
+            fn.argtypes = [_i64, _i64, _i64, _i64]
+            fn.restype = ctypes.c_size_t
+        lib.lora_status_str.argtypes = [ctypes.c_int]
+        lib.lora_status_str.restype = ctypes.c_char_p
+        lib.lora_delta_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
+        lib.lora_delta_device_status.restype = ctypes.c_int
+        lib.lora_delta_set_profile_events.argtypes = [ctypes.POINTER(_vp), ctypes.c_int]
+        lib.lora_delta_set_profile_events.restype = ctypes.c_int
+        lib.lora_delta_describe.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+        lib.lora_delta_describe.restype = ctypes.c_size_t
+        _LIB = lib
+    return _LIB
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``liblora_delta.so`` (raises when it is missing)."""
+    return _lib()
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def lora_delta_fwd_workspace_size(M: int, K: int, N: int, R: int) -> int:
+    return int(_lib().lora_delta_fwd_workspace_size(M, K, N, R))
+
+
+def lora_delta_bwd_workspace_size(M: int, K: int, N: int, R: int) -> int:
+    return int(_lib().lora_delta_bwd_workspace_size(M, K, N, R))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zeroed workspace (its first 256 bytes are the device status block)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def lora_delta_fwd(x, a, b, alpha: float, *, delta_y=None, u=None, workspace=None, stream=None):
+    """Forward: ``u = bf16(x @ a.T)``, ``delta_y = fp32(u @ b.T) * alpha``."""
+    M, K = x.shape
+    R = a.shape[0]
+    N = b.shape[0]
+    _check(x, "x", torch.bfloat16, (M, K)); _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R))
+    if delta_y is None:
+        delta_y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if u is None:
+        u = torch.empty((M, R), dtype=torch.bfloat16, device=x.device)
+    _check(delta_y, "delta_y", torch.float32, (M, N)); _check(u, "u", torch.bfloat16, (M, R))
+    need = lora_delta_fwd_workspace_size(M, K, N, R)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    rc = _lib().lora_delta_fwd(_ptr(x), _ptr(a), _ptr(b), float(alpha), M, K, N, R, _ptr(delta_y), _ptr(u),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_fwd")
+    return delta_y, u
+
+
+def lora_delta_bwd(dy, x, a, b, u, alpha: float, *, dx=None, da=None, db=None, du=None, workspace=None, stream=None):
+    """Backward: returns ``(dx, da, db, du)``; no base-weight gradient."""
+    M, K = x.shape
+    R = a.shape[0]
+    N = b.shape[0]
+    _check(dy, "dy", torch.bfloat16, (M, N)); _check(x, "x", torch.bfloat16, (M, K))
+    _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R)); _check(u, "u", torch.bfloat16, (M, R))
+    dev = x.device
+    dx = torch.empty((M, K), dtype=torch.float32, device=dev) if dx is None else dx
+    da = torch.empty((R, K), dtype=torch.float32, device=dev) if da is None else da
+    db = torch.empty((N, R), dtype=torch.float32, device=dev) if db is None else db
+    du = torch.empty((M, R), dtype=torch.bfloat16, device=dev) if du is None else du
+    _check(dx, "dx", torch.float32, (M, K)); _check(da, "da", torch.float32, (R, K))
+    _check(db, "db", torch.float32, (N, R)); _check(du, "du", torch.bfloat16, (M, R))
+    need = lora_delta_bwd_workspace_size(M, K, N, R)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    rc = _lib().lora_delta_bwd(_ptr(dy), _ptr(x), _ptr(a), _ptr(b), _ptr(u), float(alpha), M, K, N, R, _ptr(dx),
+                               _ptr(da), _ptr(db), _ptr(du), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_bwd")
+    return dx, da, db, du
+
+
+def lora_delta_device_status(workspace: torch.Tensor) -> int:
+    """Device status code of a workspace (0 = no kernel reported a problem)."""
+    code = ctypes.c_int(0)
+    rc = _lib().lora_delta_device_status(_ptr(workspace), ctypes.byref(code))
+    if rc not in (LORA_OK, 8):
+        raise LoraDeltaError(rc, "lora_delta_device_status")
+    return int(code.value)
+
+
+def lora_delta_set_profile_events(events) -> None:
+    """Record ``torch.cuda.Event``s around each internal kernel (None = off)."""
+    if not events:
+        _lib().lora_delta_set_profile_events(None, 0)
+        return
+    for ev in events:
+        if not ev.cuda_event:        # torch creates the CUDA event lazily, at its first record
+            ev.record()
+    arr = (_vp * len(events))(*[ev.cuda_event for ev in events])
+    rc = _lib().lora_delta_set_profile_events(arr, len(events))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_set_profile_events")
+
+
+def lora_delta_describe() -> str:
+    n = _lib().lora_delta_describe(None, 0)
+    buf = ctypes.create_string_buffer(n)
+    _lib().lora_delta_describe(buf, n)
+    return buf.value.decode()
+
+
+def lora_status_str(code: int) -> str:
+    return _lib().lora_status_str(code).decode()

@@ -1,0 +1,135 @@
+/*
+ * lora_delta.h -- C ABI of the batch-invariant shared LoRA delta operator
+ * (GB300 / sm_103a).
+ *
+ * The operator (page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA + Triton,
+ * both batch-invariant", section "Summary"):
+ *
+ *   forward    U        = X @ A^T          FP32 accumulate, rounded to BF16
+ *              delta_y  = (U @ B^T) * alpha FP32 accumulate, FP32 output
+ *   backward   dV = dY * alpha  (rounded to BF16)    dU = dV @ B (rounded to BF16)
+ *              dB = dV^T @ U    dX = dU @ A    dA = dU^T @ X   (FP32)
+ *
+ * No base weight enters either call, so none can be read or given a gradient
+ * (same page, "Acceptance criteria", items 2 and 3).
+ *
+ * Numerics. Every sum is formed from 16-term tensor-core dot products
+ * ("leaves": BF16 products, FP32 accumulation, a fresh accumulator each),
+ * added in FP32 round-to-nearest by the canonical pairwise tree over the leaf
+ * index. The tree depends only on the length of the reduction, never on M,
+ * on the tiling or on the device, and no atomics are used: every row of U,
+ * delta_y, dU and dX is bitwise independent of the other rows in the batch
+ * (batch invariance: same page, "Batch invariance"), and every output is
+ * bitwise identical across reruns.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major, contiguous, in device memory (or memory
+ *     the device can address), 16-byte aligned. BF16 tensors are passed as
+ *     `const void *` (IEEE bfloat16 bit patterns, 2 bytes each).
+ *   - Shapes: M >= 0 (batch rows; M = 0 is a no-op returning LORA_OK),
+ *     K and N positive multiples of 8, R a multiple of 8 in [8, 64];
+ *     M, K, N below 2^31.
+ *   - The caller owns every buffer and the stream; the library never
+ *     allocates, frees or synchronises. Work is enqueued on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) of the current device
+ *     and the call returns without waiting for it.
+ *   - Argument errors are detected on the host before anything is enqueued.
+ *   - `workspace` is scratch owned by the caller, at least the size the
+ *     matching *_workspace_size() query returns, 256-byte aligned. Its first
+ *     256 bytes are a device status block: they must be zero before the first
+ *     call that uses the workspace (for example, allocate it zeroed); a kernel
+ *     that gives up on an internal wait writes a non-zero code there and
+ *     returns (read it with lora_delta_device_status). A workspace must not be
+ *     shared by calls that may run concurrently.
+ */
+#ifndef LORA_DELTA_H
+#define LORA_DELTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lora_status {
+  LORA_OK = 0,
+  LORA_ERR_NULL = 1,       /* a required pointer is NULL */
+  LORA_ERR_SHAPE = 2,      /* M < 0, K or N not a positive multiple of 8, or a size too large */
+  LORA_ERR_ALIGN = 3,      /* a tensor or the workspace is not aligned as required */
+  LORA_ERR_RANK = 4,       /* R not a multiple of 8 in [8, 64] */
+  LORA_ERR_WORKSPACE = 5,  /* workspace smaller than the query returned */
+  LORA_ERR_CUDA = 6,       /* a CUDA runtime or driver call failed (incl. kernel launch) */
+  LORA_ERR_DEVICE = 7,     /* the current device is not an sm_103 (GB300) GPU */
+  LORA_ERR_TIMEOUT = 8     /* a kernel gave up waiting (read from the status block) */
+} lora_status;
+
+/*
+ * Forward pass.
+ *   x        [M][K] bf16   input rows
+ *   a        [R][K] bf16   down projection A (used as A^T)
+ *   b        [N][R] bf16   up projection B (used as B^T)
+ *   alpha                  scale, applied as one FP32 multiply after the FP32 sum
+ *   delta_y  [M][N] fp32   out: (U @ B^T) * alpha
+ *   u        [M][R] bf16   out: U = bf16(X @ A^T), saved for the backward pass
+ *   workspace, workspace_bytes: >= lora_delta_fwd_workspace_size(M, K, N, R)
+ * Kernels: down-projection (U partials), combine (U), up-projection.
+ */
+lora_status lora_delta_fwd(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K, int64_t N,
+                           int64_t R, float *delta_y, void *u, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass (no base-weight gradient).
+ *   dy       [M][N] bf16   upstream gradient of delta_y
+ *   x, a, b               as in the forward pass
+ *   u        [M][R] bf16   the U the forward pass returned
+ *   alpha                  the forward scale
+ *   dx       [M][K] fp32   out: dU @ A
+ *   da       [R][K] fp32   out: dU^T @ X
+ *   db       [N][R] fp32   out: dV^T @ U
+ *   du       [M][R] bf16   out: dU = bf16(dV @ B), dV = bf16(dY * alpha)
+ *   workspace, workspace_bytes: >= lora_delta_bwd_workspace_size(M, K, N, R)
+ * dA and dB reduce over all M rows in fixed 256-row chunks whose partials are
+ * added by the canonical pairwise tree over the chunk index.
+ * Kernels: dU partials, dB partials, combine (dU, dB), dX, dA partials, combine (dA).
+ */
+lora_status lora_delta_bwd(const void *dy, const void *x, const void *a, const void *b, const void *u, float alpha,
+                           int64_t M, int64_t K, int64_t N, int64_t R, float *dx, float *da, float *db, void *du,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes the calls need (0 if the shape is invalid). */
+size_t lora_delta_fwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
+size_t lora_delta_bwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
+
+/* Static description of a status code. */
+const char *lora_status_str(int status);
+
+/*
+ * Reads the device status block at the start of `workspace` (synchronous:
+ * waits for the device). *code receives 0 when no kernel reported a problem,
+ * else (site << 8) | 1 for a wait that timed out at internal site `site`.
+ * Returns LORA_OK, LORA_ERR_NULL or LORA_ERR_CUDA; LORA_ERR_TIMEOUT when
+ * *code is non-zero.
+ */
+lora_status lora_delta_device_status(const void *workspace, int *code);
+
+/*
+ * Profiling hook (process-wide; not thread-safe). When count > 0, later
+ * forward and backward calls record events[0] (cudaEvent_t) before their
+ * first kernel and events[i] after their i-th kernel, up to count - 1
+ * kernels, on the call's stream. count = 0 switches it off. The events stay
+ * owned by the caller.
+ */
+lora_status lora_delta_set_profile_events(void *const *events, int count);
+
+/*
+ * Writes a NUL-terminated JSON description of the numerics and tiling
+ * (provenance) into buf (at most len bytes). Returns the length it needs.
+ */
+size_t lora_delta_describe(char *buf, size_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_DELTA_H */

@@ -234,10 +234,10 @@ int ora_dv(const uint16_t *dy, float alpha, int64_t M, int64_t N, uint16_t *dv)
 
 /*
  * du[m][r] = rnbf(rn32(sum_n dv[m][n] * b[n][r]))  ("dU = dV @ B", rounded to
- * BF16 between the GEMMs, section "Summary").
+ * BF16 between the GEMMs, section "Summary"). f32_du (optional) = the rn32 value.
  */
 int ora_du(const uint16_t *dv, const uint16_t *b, int64_t M, int64_t N, int64_t R,
-           uint16_t *du, double *s_du, int threads)
+           uint16_t *du, float *f32_du, double *s_du, int threads)
 {
     double *sum = alloc_d(M * R);
     if (!sum) return 1;
@@ -247,7 +247,11 @@ int ora_du(const uint16_t *dv, const uint16_t *b, int64_t M, int64_t N, int64_t 
     dot_job j = { dv, N, 1, b, 1, R, M, R, N, sum, s_du, 0, 0 };
 #endif
     dot_all(j, threads);
-    for (int64_t e = 0; e < M * R; ++e) du[e] = rnbf(rn32(sum[e]));
+    for (int64_t e = 0; e < M * R; ++e) {
+        float f = rn32(sum[e]);
+        if (f32_du) f32_du[e] = f;
+        du[e] = rnbf(f);
+    }
     free(sum);
     return 0;
 }

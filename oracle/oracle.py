@@ -70,7 +70,7 @@ class Oracle:
             "ora_u": [_u16p, _u16p, _i64, _i64, _i64, _u16p, _f32p, _f64p, ctypes.c_int],
             "ora_delta_y": [_u16p, _u16p, ctypes.c_float, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
             "ora_dv": [_u16p, ctypes.c_float, _i64, _i64, _u16p],
-            "ora_du": [_u16p, _u16p, _i64, _i64, _i64, _u16p, _f64p, ctypes.c_int],
+            "ora_du": [_u16p, _u16p, _i64, _i64, _i64, _u16p, _f32p, _f64p, ctypes.c_int],
             "ora_db": [_u16p, _u16p, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
             "ora_dx": [_u16p, _u16p, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
             "ora_da": [_u16p, _u16p, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
@@ -99,15 +99,18 @@ class Oracle:
         assert a.dtype == dtype, (a.dtype, dtype)
         return a
 
-    def u(self, x, a, want_s=False):
+    def u(self, x, a, want_s=False, want_f32=False):
+        """U (bf16 bits); with want_s also S = sum|x a|; with want_f32 also the
+        FP32 value before the BF16 rounding."""
         x = self._c(x, np.uint16); a = self._c(a, np.uint16)
         M, K = x.shape; R = a.shape[0]
         assert a.shape == (R, K)
         u = np.empty((M, R), np.uint16)
         s = np.empty((M, R), np.float64) if want_s else None
-        rc = self.lib.ora_u(_p(x, _u16p), _p(a, _u16p), M, K, R, _p(u, _u16p), None, _p(s, _f64p), self.threads)
+        f = np.empty((M, R), np.float32) if want_f32 else None
+        rc = self.lib.ora_u(_p(x, _u16p), _p(a, _u16p), M, K, R, _p(u, _u16p), _p(f, _f32p), _p(s, _f64p), self.threads)
         assert rc == 0
-        return (u, s) if want_s else u
+        return (u,) + ((s,) if want_s else ()) + ((f,) if want_f32 else ()) if (want_s or want_f32) else u
 
     def delta_y(self, u, b, alpha, want_s=False):
         u = self._c(u, np.uint16); b = self._c(b, np.uint16)
@@ -126,14 +129,17 @@ class Oracle:
         assert self.lib.ora_dv(_p(dy, _u16p), float(alpha), M, N, _p(dv, _u16p)) == 0
         return dv
 
-    def du(self, dv, b, want_s=False):
+    def du(self, dv, b, want_s=False, want_f32=False):
+        """dU (bf16 bits); optionally S and the FP32 value before rounding."""
         dv = self._c(dv, np.uint16); b = self._c(b, np.uint16)
         M, N = dv.shape; R = b.shape[1]
         assert b.shape == (N, R)
         du = np.empty((M, R), np.uint16)
         s = np.empty((M, R), np.float64) if want_s else None
-        assert self.lib.ora_du(_p(dv, _u16p), _p(b, _u16p), M, N, R, _p(du, _u16p), _p(s, _f64p), self.threads) == 0
-        return (du, s) if want_s else du
+        f = np.empty((M, R), np.float32) if want_f32 else None
+        assert self.lib.ora_du(_p(dv, _u16p), _p(b, _u16p), M, N, R, _p(du, _u16p), _p(f, _f32p), _p(s, _f64p),
+                               self.threads) == 0
+        return (du,) + ((s,) if want_s else ()) + ((f,) if want_f32 else ()) if (want_s or want_f32) else du
 
     def db(self, dv, u, want_s=False):
         dv = self._c(dv, np.uint16); u = self._c(u, np.uint16)

@@ -1,0 +1,132 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point that include/lora_delta.h declares, and rejects bad arguments on the
+host before touching the device."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lora_delta.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deterministic_arithmetic_gb300 import build_lib
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    build_lib.build()
+    return ld.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(lora_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("lora_delta_fwd", "lora_delta_bwd", "lora_delta_fwd_workspace_size", "lora_delta_bwd_workspace_size",
+              "lora_status_str", "lora_delta_device_status", "lora_delta_set_profile_events", "lora_delta_describe"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/lora_delta.h but not exported"
+
+
+def test_status_strings(lib):
+    lib.lora_status_str.restype = ctypes.c_char_p
+    seen = set()
+    for code in range(9):
+        s = lib.lora_status_str(code).decode()
+        assert s and s != "unknown status"
+        seen.add(s)
+    assert len(seen) == 9
+    assert lib.lora_status_str(99).decode() == "unknown status"
+
+
+def test_workspace_sizes():
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    f = ld.lora_delta_fwd_workspace_size(8192, 4096, 4096, 16)
+    b = ld.lora_delta_bwd_workspace_size(8192, 4096, 4096, 16)
+    # U partials: 4 slices of 1024 x 8192 rows x 16 x fp32, plus the 256-byte status block
+    assert f == 256 + 4 * 8192 * 16 * 4
+    # dU partials (4 slices), dB and dA chunk partials (32 chunks of 256 rows)
+    assert b == 256 + 4 * 8192 * 16 * 4 + 32 * 16 * 4096 * 4 + 32 * 16 * 4096 * 4
+    assert ld.lora_delta_fwd_workspace_size(0, 128, 96, 8) == 256
+    for bad in ((8, 100, 96, 8), (8, 128, 90, 8), (8, 128, 96, 12), (8, 128, 96, 72), (-1, 128, 96, 8), (8, 0, 96, 8)):
+        assert ld.lora_delta_fwd_workspace_size(*bad) == 0
+        assert ld.lora_delta_bwd_workspace_size(*bad) == 0
+    assert ld.lora_delta_fwd_workspace_size(100, 128, 96, 8) <= ld.lora_delta_fwd_workspace_size(200, 128, 96, 8)
+
+
+def _fwd(lib, ptrs, M=64, K=128, N=96, R=8, ws_bytes=1 << 20):
+    f = lib.lora_delta_fwd
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float] + [ctypes.c_int64] * 4 + [ctypes.c_void_p] * 3 + \
+                 [ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    x, a, b, y, u, ws = ptrs
+    return f(x, a, b, 2.0, M, K, N, R, y, u, ws, ws_bytes, None)
+
+
+def _bwd(lib, ptrs, M=64, K=128, N=96, R=8, ws_bytes=1 << 22):
+    f = lib.lora_delta_bwd
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_float] + [ctypes.c_int64] * 4 + [ctypes.c_void_p] * 5 + \
+                 [ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    dy, x, a, b, u, dx, da, db, du, ws = ptrs
+    return f(dy, x, a, b, u, 2.0, M, K, N, R, dx, da, db, du, ws, ws_bytes, None)
+
+
+FAKE = 0x10000   # never dereferenced: every case below fails its host-side checks first
+
+
+def test_argument_errors_are_host_side(lib):
+    ok6 = [FAKE] * 6
+    assert _fwd(lib, ok6, M=0) == 0                                   # M = 0 is a no-op
+    assert _fwd(lib, [None] + ok6[1:]) == 1                           # LORA_ERR_NULL
+    assert _fwd(lib, ok6, K=100) == 2                                 # LORA_ERR_SHAPE
+    assert _fwd(lib, ok6, N=0) == 2
+    assert _fwd(lib, ok6, M=-5) == 2
+    assert _fwd(lib, ok6, R=12) == 4                                  # LORA_ERR_RANK
+    assert _fwd(lib, ok6, R=72) == 4
+    assert _fwd(lib, [FAKE + 2] + ok6[1:]) == 3                       # LORA_ERR_ALIGN
+    assert _fwd(lib, ok6, ws_bytes=16) == 5                           # LORA_ERR_WORKSPACE
+    ok10 = [FAKE] * 10
+    assert _bwd(lib, ok10, M=0) == 0
+    assert _bwd(lib, ok10[:8] + [None, FAKE]) == 1
+    assert _bwd(lib, ok10, R=0) == 4
+    assert _bwd(lib, ok10[:5] + [FAKE + 8] + ok10[6:]) == 3
+    assert _bwd(lib, ok10, ws_bytes=300) == 5
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is for hosts without one")
+    # all arguments valid: the call reaches the device check and must report an error, not compute on the CPU
+    assert _fwd(lib, [FAKE] * 6) in (6, 7)
+
+
+def test_describe(lib):
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    d = json.loads(ld.lora_delta_describe())
+    assert "canonical pairwise" in d["numeric_profile"] and d["arch"] == "sm_103a"
+
+
+def test_python_binding_fails_without_library(tmp_path, monkeypatch):
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    monkeypatch.setattr(ld, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ld, "_LIB", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        ld.library()

@@ -1,0 +1,206 @@
+"""CUDA path (through the C ABI) against the CPU oracle, batch invariance and
+reruns. Every test here needs a GB300 and the built library."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from deterministic_arithmetic_gb300 import synthetic as S  # noqa: E402
+import gpu_util as G  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from deterministic_arithmetic_gb300 import build_lib
+
+    build_lib.build()
+
+
+def _rows_of(out, rows):
+    return {k: (v[rows] if k in ("u", "delta_y", "du", "dx") else v) for k, v in out.items()}
+
+
+# ------------------------------------------------------------------ parity
+def test_tiny_parity(oracle):
+    w = S.tiny()
+    d = w.generate(0)
+    out = G.run(d, w.shape.alpha)
+    G.check_parity(oracle, d, w.shape.alpha, out)
+
+
+@pytest.mark.parametrize("M,K,N,R", [(64, 128, 96, 8), (300, 264, 136, 16), (513, 1024, 520, 32), (129, 200, 72, 64)])
+def test_integer_inputs_are_bitwise_equal_to_the_oracle(oracle, M, K, N, R):
+    """Small-integer inputs keep every partial sum exact, so no summation order
+    can round: the GPU must equal the oracle bit for bit at every boundary."""
+    w = S.integers(M, K, N, R, 2.0, bound=2)
+    d = w.generate(5)
+    out = G.run(d, 2.0)
+    f = oracle.fwd(d["x"], d["a"], d["b"], 2.0)
+    g = oracle.bwd(d["dy"], d["x"], d["a"], d["b"], f["u"], 2.0)
+    for k in ("u", "delta_y"):
+        G.assert_bitwise(k, out[k], f[k])
+    for k in ("du", "db", "dx", "da"):
+        G.assert_bitwise(k, out[k], g[k])
+
+
+EDGE = [  # (M, K, N, R, alpha): ragged M / K / N tails, every padded rank, single rows, one-tile and many-tile cases
+    (1, 64, 64, 8, 2.0), (7, 136, 96, 16, 0.5), (100, 200, 104, 24, 1.0), (129, 512, 264, 32, 2.0),
+    (300, 1032, 520, 40, 0.75), (257, 256, 128, 48, 1.5), (65, 8, 8, 56, 2.0), (600, 2056, 300 - 4, 64, 1.0),
+    (1000, 96, 2048, 16, 3.0), (2, 4096 + 8, 16, 8, 0.25),
+]
+
+
+@pytest.mark.parametrize("M,K,N,R,alpha", EDGE)
+def test_edge_shapes(oracle, M, K, N, R, alpha):
+    w = S.Workload("edge", S.Shape(M, K, N, R, alpha), {"x": 1.0, "a": K ** -0.5, "b": R ** -0.5, "dy": 1.0})
+    d = w.generate(3)
+    out = G.run(d, alpha)
+    G.check_parity(oracle, d, alpha, out)
+
+
+def test_adversarial_same_sign_inputs(oracle):
+    """All products positive and a long reduction: rounding errors cannot
+    cancel, the worst case for the 1e-6 * sum|ab| bound."""
+    M, K, N, R = 256, 17408, 256, 16
+    w = S.Workload("pos", S.Shape(M, K, N, R, 1.0), {"x": 1.0, "a": 1.0, "b": 1.0, "dy": 1.0})
+    d = w.generate(8)
+    for k in d:
+        d[k] = d[k] & np.uint16(0x7FFF)          # clear the sign bit: |value|
+    out = G.run(d, 1.0)
+    worst = G.check_parity(oracle, d, 1.0, out)
+    print("worst |err|/S:", worst)
+
+
+def test_reruns_are_bitwise_identical():
+    w = S.sweep(2048, 1024)
+    d = w.generate(1)
+    a = G.run(d, w.shape.alpha)
+    b = G.run(d, w.shape.alpha)
+    for k in a:
+        G.assert_bitwise(k, a[k], b[k])
+
+
+def test_alpha_scaling_and_zero_weights():
+    w = S.tiny()
+    d = w.generate(2)
+    base = G.run(d, 1.0)
+    two = G.run(d, 2.0)
+    G.assert_bitwise("u", two["u"], base["u"])
+    for k in ("delta_y", "db", "dx", "da"):
+        G.assert_bitwise(k, two[k], (base[k] * np.float32(2.0)).astype(np.float32))
+    zb = dict(d, b=np.zeros_like(d["b"]))
+    out = G.run(zb, 2.0)
+    for k in ("delta_y", "dx", "da"):
+        assert not np.any(out[k]), k
+    assert not np.any(out["du"] & 0x7FFF) and np.any(out["db"])
+    za = dict(d, a=np.zeros_like(d["a"]))
+    out = G.run(za, 2.0)
+    assert not np.any(out["u"] & 0x7FFF) and not np.any(out["delta_y"]) and not np.any(out["db"])
+
+
+# -------------------------------------------------------- batch invariance
+def _check_subbatches(d, alpha, full, sizes):
+    M = d["x"].shape[0]
+    for s in sizes:
+        for rows in (slice(0, s), slice(M - s, M)):
+            sub = G.run(d, alpha, rows=rows)
+            ref = _rows_of(full, rows)
+            for k in ("u", "delta_y", "du", "dx"):
+                G.assert_bitwise(f"{k} rows {rows.start}:{rows.stop}", sub[k], ref[k])
+
+
+def test_tiny_batch_invariance():
+    w = S.tiny()
+    d = w.generate(0)
+    full = G.run(d, w.shape.alpha)
+    _check_subbatches(d, w.shape.alpha, full, (1, 7, 32, 64))
+
+
+@pytest.mark.parametrize("M,KN", S.SWEEP_SHAPES)
+def test_invariance_sweep(oracle, M, KN):
+    """5 seeds x sub-batch sizes {1, 8, 24, 100, M}: every row boundary (U,
+    delta_y, dU, dX) bitwise equal to the full batch's rows; dA/dB by rerun.
+    Parity against the oracle on the first seed."""
+    w = S.sweep(M, KN)
+    for seed in range(5):
+        d = w.generate(seed)
+        full = G.run(d, w.shape.alpha)
+        if seed == 0:
+            G.check_parity(oracle, d, w.shape.alpha, full)
+        sizes = [s for s in S.SWEEP_SUBBATCH if s <= M] + [M]
+        _check_subbatches(d, w.shape.alpha, full, sizes)
+        again = G.run(d, w.shape.alpha)
+        for k in ("da", "db"):
+            G.assert_bitwise(k, again[k], full[k])
+
+
+# ------------------------------------------------------ full-size workloads
+def _sampled_parity(oracle, d, alpha, out, nrows=48, ncols=48, seed=0):
+    rng = np.random.default_rng(seed)
+    M, K = d["x"].shape
+    N = d["b"].shape[0]
+    rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, nrows)]))
+    sub = {"x": d["x"][rows], "dy": d["dy"][rows], "a": d["a"], "b": d["b"]}
+    ref_u, s_u, f_u = oracle.u(sub["x"], d["a"], want_s=True, want_f32=True)
+    G.assert_bf16_close("U rows", out["u"][rows], ref_u, f_u, s_u)
+    y, sy = oracle.delta_y(out["u"][rows], d["b"], alpha, True)
+    G.assert_f32_within("delta_y rows", out["delta_y"][rows], y, sy)
+    dv_rows = oracle.dv(sub["dy"], alpha)
+    ref_du, s_du, f_du = oracle.du(dv_rows, d["b"], want_s=True, want_f32=True)
+    G.assert_bf16_close("dU rows", out["du"][rows], ref_du, f_du, s_du)
+    dx, sdx = oracle.dx(out["du"][rows], d["a"], True)
+    G.assert_f32_within("dX rows", out["dx"][rows], dx, sdx)
+    kc = np.unique(np.concatenate([[0, K - 1], rng.integers(0, K, ncols)]))
+    da, sda = oracle.da(out["du"], np.ascontiguousarray(d["x"][:, kc]), True)
+    G.assert_f32_within("dA cols", out["da"][:, kc], da, sda)
+    nc = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, ncols)]))
+    dv_cols = oracle.dv(np.ascontiguousarray(d["dy"][:, nc]), alpha)
+    db, sdb = oracle.db(dv_cols, out["u"], True)
+    G.assert_f32_within("dB rows", out["db"][nc], db, sdb)
+
+
+def test_training_step_full_size(oracle):
+    """M=8192, K=N=4096, R=16, alpha=2 (the benchmark's workload): sampled
+    rows/columns against the oracle, sub-batch invariance, reruns."""
+    w = S.train()
+    d = w.generate(0)
+    out = G.run(d, w.shape.alpha)
+    _sampled_parity(oracle, d, w.shape.alpha, out)
+    _check_subbatches(d, w.shape.alpha, out, (1, 100, 4097))
+    again = G.run(d, w.shape.alpha)
+    for k in out:
+        G.assert_bitwise(k, again[k], out[k])
+
+
+@pytest.mark.parametrize("site", ["fc1", "fc2"])
+def test_mlp_insertion_points(oracle, site):
+    w = S.mlp_fc1() if site == "fc1" else S.mlp_fc2()
+    d = w.generate(0)
+    out = G.run(d, w.shape.alpha)
+    _sampled_parity(oracle, d, w.shape.alpha, out, nrows=24, ncols=24)
+    _check_subbatches(d, w.shape.alpha, out, (8,))
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_decode_batches(oracle, M):
+    w = S.decode(M)
+    d = w.generate(0)
+    out = G.run(d, w.shape.alpha)
+    ref_u, s_u, f_u = oracle.u(d["x"], d["a"], want_s=True, want_f32=True)
+    G.assert_bf16_close("U", out["u"], ref_u, f_u, s_u)
+    y, sy = oracle.delta_y(out["u"], d["b"], w.shape.alpha, True)
+    G.assert_f32_within("delta_y", out["delta_y"], y, sy)
+    if M == 64:
+        G.check_parity(oracle, d, w.shape.alpha, out)
+    # decode rows are the leading rows of the 64-row batch (same flat streams): same bits
+    if M < 64:
+        w64 = S.decode(64)
+        d64 = w64.generate(0)
+        assert np.array_equal(d64["x"][:M], d["x"]) and np.array_equal(d64["dy"][:M], d["dy"])
+        big = G.run(d64, w64.shape.alpha)
+        for k in ("u", "delta_y", "du", "dx"):
+            G.assert_bitwise(k, out[k], big[k][:M])
