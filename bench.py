@@ -1,0 +1,447 @@
+"""Benchmark of the LoRA delta operator: forward + backward per step.
+
+Workload (the per-GEMM LoRA profile of page "Independent from-scratch
+Qwen-14B step reimplementation ...", section "Finding 2"): M=8192 tokens,
+K=N=4096, R=16, alpha=2, BF16 inputs with FP32 accumulation; X ~ N(0,1),
+A ~ N(0,1/4096), B ~ N(0,1/16), dY ~ N(0,1e-2); seeded synthetic data.
+
+One step = lora_delta_fwd + lora_delta_bwd through the C ABI (9 kernels).
+Metric: algorithmic HBM bytes of the step / step time (GB/s); ms per step and
+the fraction of the measured HBM copy peak are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --impl reference the CPU oracle is timed on the host cores instead (a
+deliberately slow program: the parity reference, not a performance target).
+For N > 1 (launched by torch.distributed.run) every rank runs its own replica
+of the workload (the operator does not shard), and rank 0 prints one line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
+KERNELS = ["down U", "combine U", "up dY_lora", "down dU", "wgrad dB", "combine dU+dB", "up dX", "wgrad dA",
+           "combine dA"]
+N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
+
+
+def algorithmic_bytes(M, K, N, R):
+    """Minimum bytes each step of the operator must move (each streamed operand
+    read once per consuming kernel, each output written once, small operands
+    counted once). Combine kernels add no algorithmic bytes."""
+    bf, f4 = 2, 4
+    return {
+        "down U": M * K * bf + R * K * bf + M * R * bf,             # X, A -> U
+        "combine U": 0,
+        "up dY_lora": M * R * bf + N * R * bf + M * N * f4,         # U, B -> dY_lora
+        "down dU": M * N * bf + N * R * bf + M * R * bf,            # dY, B -> dU
+        "wgrad dB": M * N * bf + M * R * bf + N * R * f4,           # dY, U -> dB
+        "combine dU+dB": 0,
+        "up dX": M * R * bf + R * K * bf + M * K * f4,              # dU, A -> dX
+        "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA
+        "combine dA": 0,
+    }
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by kernel, with the hash of the kernel source
+# the counters were taken on; a kernel changed since then reports null.
+NCU_TRAFFIC = {}
+
+
+def source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "deterministic_arithmetic_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period}"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle
+class OracleSample:
+    """The CPU oracle's fwd+bwd (all 7 steps) on the first ``rows`` rows of the
+    workload, all of K, N and R. Every step of the operator is linear in M, so
+    the time scales to the full batch by M / rows."""
+
+    def __init__(self, shape, rows: int, threads: int = 0):
+        from deterministic_arithmetic_gb300 import synthetic as S
+        from oracle import oracle as oracle_mod
+
+        self.shape, self.rows = shape, rows
+        self.o = oracle_mod.Oracle.load(threads=threads)
+        w = S.Workload("sample", S.Shape(rows, shape.K, shape.N, shape.R, shape.alpha), S.train().std)
+        self.d = w.generate(0)
+
+    def seconds_full(self) -> float:
+        d, a = self.d, self.shape.alpha
+        t0 = time.perf_counter()
+        f = self.o.fwd(d["x"], d["a"], d["b"], a)
+        self.o.bwd(d["dy"], d["x"], d["a"], d["b"], f["u"], a)
+        return (time.perf_counter() - t0) * self.shape.M / self.rows
+
+    @property
+    def threads(self) -> int:
+        return self.o.n_threads
+
+    def describe(self) -> str:
+        sh = self.shape
+        scale = "" if self.rows == sh.M else f"; time x{sh.M / self.rows:g} to the full batch"
+        return (f"oracle fwd+bwd (all 7 steps) on {self.rows} of {sh.M} rows, full K={sh.K}, N={sh.N}, R={sh.R}, "
+                f"{self.threads} threads{scale}")
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores, sized so that the whole
+    --steps/--warmup run stays within about two minutes."""
+    from deterministic_arithmetic_gb300 import synthetic as S
+
+    if rank != 0:
+        return
+    shape = S.train().shape
+    total_bytes = sum(algorithmic_bytes(shape.M, shape.K, shape.N, shape.R).values())
+    probe = OracleSample(shape, 64)
+    per_row = probe.seconds_full() / shape.M
+    rows = int(min(shape.M, max(16, args.reference_budget_s / max(1, args.steps + args.warmup) / per_row)))
+    sample = OracleSample(shape, rows)
+    for _ in range(args.warmup):
+        sample.seconds_full()
+    times = [sample.seconds_full() for _ in range(args.steps)]
+    step_s = statistics.median(times)
+    value = total_bytes / step_s / 1e9
+    desc = sample.describe()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64/Box-Muller)",
+        "config": {"workload": "LoRA training step M=8192 K=N=4096 R=16 alpha=2", "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": sample.threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, world, rank, local):
+    import torch
+
+    from deterministic_arithmetic_gb300 import build_lib
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+    from deterministic_arithmetic_gb300 import synthetic as S
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    if rank == 0 or not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = S.train()
+    sh = w.shape
+    M, K, N, R, alpha = sh.M, sh.K, sh.N, sh.R, sh.alpha
+    d = w.generate(0)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X0, A, B, DY0 = to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"]), to_dev(d["dy"])
+    Xs = [X0] + [X0.clone() for _ in range(N_ROTATE - 1)]
+    DYs = [DY0] + [DY0.clone() for _ in range(N_ROTATE - 1)]
+    Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    DX = torch.empty((M, K), dtype=torch.float32, device=dev)
+    DA = torch.empty((R, K), dtype=torch.float32, device=dev)
+    DB = torch.empty((N, R), dtype=torch.float32, device=dev)
+    DU = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+    wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
+        ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
+        ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # per-kernel events on a sample of the timed steps (fwd: 4 marks, bwd: 7 marks)
+    n_prof = min(args.steps, 64)
+    prof_steps = set(np.linspace(0, args.steps - 1, n_prof).astype(int).tolist())
+    fev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in prof_steps}
+    bev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(7)] for i in prof_steps}
+    for evs in list(fev.values()) + list(bev.values()):
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else int(
+            os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
+            if i in prof_steps:
+                ld.lora_delta_set_profile_events(fev[i])
+            ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
+            if i in prof_steps:
+                ld.lora_delta_set_profile_events(bev[i])
+            ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
+            if i in prof_steps:
+                ld.lora_delta_set_profile_events(None)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    ms_step = elapsed_ms / args.steps
+
+    # per-kernel average durations over the sampled steps
+    ktimes = {k: [] for k in KERNELS}
+    for i in prof_steps:
+        f, b = fev[i], bev[i]
+        for j, name in enumerate(KERNELS[:3]):
+            ktimes[name].append(f[j].elapsed_time(f[j + 1]))
+        for j, name in enumerate(KERNELS[3:]):
+            ktimes[name].append(b[j].elapsed_time(b[j + 1]))
+    kavg = {k: statistics.mean(v) for k, v in ktimes.items()}
+    status = (ld.lora_delta_device_status(wf), ld.lora_delta_device_status(wb))
+    if status != (0, 0):
+        raise SystemExit(f"device status block reports {status}")
+
+    alg = algorithmic_bytes(M, K, N, R)
+    total_bytes = sum(alg.values())
+    peak, peak_kind = measured_peaks()
+    value = total_bytes * world / (ms_step * 1e-3) / 1e9
+    dominant = max(kavg, key=lambda k: kavg[k])
+    achieved = alg[dominant] / (kavg[dominant] * 1e-3) / 1e9
+    src = {"down": "down.cu", "up": "up.cu", "wgrad": "wgrad.cu", "combine": "combine.cu"}[dominant.split()[0]]
+    tr = NCU_TRAFFIC.get(dominant)
+    traffic = tr["bytes"] if tr and tr.get("src_hash") == source_hash(src) else None
+
+    # ----------------------------------------------------------- end to end
+    e2e = None
+    if not args.no_e2e:
+        pin = dict(x=torch.from_numpy(d["x"].view(np.int16)).pin_memory(),
+                   dy=torch.from_numpy(d["dy"].view(np.int16)).pin_memory(),
+                   a=torch.from_numpy(d["a"].view(np.int16)).pin_memory(),
+                   b=torch.from_numpy(d["b"].view(np.int16)).pin_memory())
+        outs = dict(y=torch.empty((M, N), dtype=torch.float32).pin_memory(),
+                    u=torch.empty((M, R), dtype=torch.int16).pin_memory(),
+                    dx=torch.empty((M, K), dtype=torch.float32).pin_memory(),
+                    da=torch.empty((R, K), dtype=torch.float32).pin_memory(),
+                    db=torch.empty((N, R), dtype=torch.float32).pin_memory(),
+                    du=torch.empty((M, R), dtype=torch.int16).pin_memory())
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        xi, dyi = Xs[0], DYs[0]
+
+        def e2e_step():
+            xi.view(torch.int16).copy_(pin["x"], non_blocking=True)
+            DYs[0].view(torch.int16).copy_(pin["dy"], non_blocking=True)
+            A.view(torch.int16).copy_(pin["a"], non_blocking=True)
+            B.view(torch.int16).copy_(pin["b"], non_blocking=True)
+            ld.lora_delta_fwd(xi, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
+            ld.lora_delta_bwd(dyi, xi, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
+            outs["y"].copy_(Y, non_blocking=True)
+            outs["u"].copy_(U.view(torch.int16), non_blocking=True)
+            outs["dx"].copy_(DX, non_blocking=True)
+            outs["da"].copy_(DA, non_blocking=True)
+            outs["db"].copy_(DB, non_blocking=True)
+            outs["du"].copy_(DU.view(torch.int16), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.e2e_steps
+        e2e = {"value": round(total_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps}
+
+    # ---------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(sh, min(M, args.oracle_rows))
+        t_full = sample.seconds_full()
+        cpu = {"value": round(total_bytes / t_full / 1e9, 4), "unit": "GB/s", "cores": sample.threads,
+               "kind": "oracle", "sample": sample.describe(), "ms_per_step": round(t_full * 1e3, 1)}
+
+    if rank == 0:
+        clk = clocks.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, BF16)",
+            "config": {"workload": "LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, 9 kernels)",
+                       "M": M, "K": K, "N": N, "R": R, "alpha": alpha, "accumulate": "fp32",
+                       "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
+                             "output stream per step, all larger than the 129 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "steps_per_s": round(1e3 / ms_step, 1),
+            "roofline_step": {"bound": "hbm", "achieved": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
+                              "peak": peak, "unit": "GB/s", "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
+                              "peak_kind": peak_kind, "algorithmic_bytes": total_bytes},
+            "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes": alg[dominant], "peak_kind": peak_kind},
+            "kernels": {k: {"ms": round(kavg[k], 5), "algorithmic_bytes": alg[k],
+                            "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
+                            "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None}
+                        for k in KERNELS},
+            "gpu_launches": 9 * args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "provenance": json.loads(ld.lora_delta_describe()),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--oracle-rows", type=int, default=8192, help="rows of the CPU-baseline oracle sample")
+    p.add_argument("--reference-budget-s", type=float, default=120.0,
+                   help="CPU seconds the --impl reference run may spend in total")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
