@@ -128,6 +128,30 @@ lora_status lora_delta_set_profile_events(void *const *events, int count);
  */
 size_t lora_delta_describe(char *buf, size_t len);
 
+/*
+ * Forward pass for callers that cannot allocate device memory -- code that
+ * must not go around an allocator it does not own (a framework's caching
+ * allocator, a server that plans every device byte in advance) or a host
+ * program with no allocator of its own where the call is made. The pages have
+ * no counterpart to this call: it exists only for such callers.
+ *
+ * Same arguments, outputs and numerics as lora_delta_fwd, without the
+ * workspace: the scratch (status block and FP32 partial sums of U) comes from
+ * one fixed 16 MiB array in the library's device image, which every device
+ * that loads the library holds until the process exits. Shapes whose
+ * lora_delta_fwd_workspace_size exceeds 16 MiB are rejected with
+ * LORA_ERR_WORKSPACE before anything is enqueued. The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call clears the status block on `stream` and then shares the
+ * same array: calls whose work may overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller.
+ */
+lora_status lora_delta_fwd_noalloc(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K,
+                                   int64_t N, int64_t R, float *delta_y, void *u, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
