@@ -183,7 +183,7 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
   CUtensorMap m_x, m_a, m_u, m_b, m_y;
-  if (!make_map(&m_x, x, false, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!make_map(&m_x, x, false, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_u, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
       !make_map(&m_b, b, false, N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
@@ -228,7 +228,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
   CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_du_rows, m_a, m_dx, m_x_chunk, m_du_chunk;
-  if (!make_map(&m_dy_rows, dy, false, M, N, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!make_map(&m_dy_rows, dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_b_rows, b, false, N, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_dy_chunk, dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_u_chunk, u, false, M, R, RP, 64, swizzle_for_span(span)) ||

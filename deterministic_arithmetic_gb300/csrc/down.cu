@@ -7,7 +7,10 @@
 //
 // Work unit = (128-row tile, slice of the reduction dimension). A persistent
 // CTA streams the unit's 128 x 64 BF16 input tiles through a TMA/mbarrier
-// ring (128-byte swizzle, 16-byte chunks, one pass over the input), issues
+// ring (one pass over the input; each tile lands as two 128 x 32 K-slabs with
+// a 64-byte swizzle: measured on GB300, the tensor core reads this layout far
+// faster than a 128-byte-swizzled 128 x 64 tile, whose MMA operand fetch
+// otherwise adds ~40 cycles per MMA to the streaming time), issues
 // four tcgen05 MMAs (M=128, N=RP, K=16) per tile, each into its own fresh TMEM
 // accumulator (a "leaf" = one 16-term dot product), and eight epilogue warps
 // add the leaves with the canonical pairwise tree in FP32 (round to nearest).
@@ -25,7 +28,8 @@ namespace lora {
 template <int RP, bool DV>
 struct DownCfg {
   static constexpr int kBM = 128, kBK = 64;
-  static constexpr int kInBytes = kBM * kBK * 2;     // 16 KB input tile
+  static constexpr int kInBytes = kBM * kBK * 2;     // 16 KB input tile: two [128][32] K-slabs
+  static constexpr int kSlabBytes = kInBytes / 2;
   static constexpr int kWBytes = RP * kBK * 2;       // RP x 64 weight tile
   static constexpr int kStageBytes = kInBytes + kWBytes;
   static constexpr int kStages = RP == 64 ? 8 : (RP == 32 ? 9 : 10);
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
             const uint32_t st = base + r.idx * C::kStageBytes;
             const int k = k0 + kb * C::kBK;
             mbar_expect_tx(full(r.idx), C::kStageBytes);
-            tma_load(st, &tm_in, full(r.idx), k, mt * C::kBM, pol_stream);
+            tma_load(st, &tm_in, full(r.idx), k, mt * C::kBM, pol_stream);                     // k .. k+31
+            tma_load(st + C::kSlabBytes, &tm_in, full(r.idx), k + 32, mt * C::kBM, pol_stream);  // k+32 .. k+63
             if (DV) tma_load(st + C::kInBytes, &tm_w, full(r.idx), 0, k, pol_keep);   // b[n][r], n = k..k+63
             else tma_load(st + C::kInBytes, &tm_w, full(r.idx), k, 0, pol_keep);      // a[r][k..k+63]
             issued |= 1u << r.idx;
@@ -140,8 +145,9 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
             const uint32_t d = tmem + g.idx * C::kGroupCols;
 #pragma unroll
             for (int j = 0; j < C::kLeaves; ++j) {
-              // input tile: K-major, 128-byte swizzle; K step j = +32 bytes inside the swizzle atom
-              const uint64_t adesc = smem_desc(st + 32u * j, 16u, 1024u, kLayoutSW128);
+              // input slab j/2: K-major, rows of 64 bytes, 64-byte swizzle, 8-row groups 512 bytes
+              // apart; K step j = +32 bytes inside the slab's swizzle atom
+              const uint64_t adesc = smem_desc(st + (j >> 1) * C::kSlabBytes + 32u * (j & 1), 16u, 512u, kLayoutSW64);
               uint64_t wdesc;
               if (DV)   // b tile [64 n][RP]: MN-major (r contiguous), 8-row groups of one swizzle span
                 wdesc = smem_desc(st + C::kInBytes + j * 16u * C::kWSpan, 8u * C::kWSpan, 8u * C::kWSpan, w_layout);
