@@ -5,7 +5,7 @@ Qwen-14B step reimplementation ...", section "Finding 2"): M=8192 tokens,
 K=N=4096, R=16, alpha=2, BF16 inputs with FP32 accumulation; X ~ N(0,1),
 A ~ N(0,1/4096), B ~ N(0,1/16), dY ~ N(0,1e-2); seeded synthetic data.
 
-One step = lora_delta_fwd + lora_delta_bwd through the C ABI (9 kernels).
+One step = lora_delta_fwd + lora_delta_bwd through the C ABI (7 kernels).
 Metric: algorithmic HBM bytes of the step / step time (GB/s); ms per step and
 the fraction of the measured HBM copy peak are reported beside it.
 
@@ -35,26 +35,25 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
-KERNELS = ["down U", "combine U", "up dY_lora", "down dU", "wgrad dB", "combine dU+dB", "up dX", "wgrad dA",
-           "combine dA"]
+KERNELS = ["down U", "up dY_lora", "down dU", "wgrad dB", "up dX", "wgrad dA", "combine dA+dB"]
+N_FWD = 2      # forward kernels; the rest are the backward's
 N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
 
 
 def algorithmic_bytes(M, K, N, R):
     """Minimum bytes each step of the operator must move (each streamed operand
     read once per consuming kernel, each output written once, small operands
-    counted once). Combine kernels add no algorithmic bytes."""
+    counted once). The U and dU combines run inside the up kernels; the final
+    combine of the dA/dB chunk partials adds no algorithmic bytes."""
     bf, f4 = 2, 4
     return {
         "down U": M * K * bf + R * K * bf + M * R * bf,             # X, A -> U
-        "combine U": 0,
         "up dY_lora": M * R * bf + N * R * bf + M * N * f4,         # U, B -> dY_lora
         "down dU": M * N * bf + N * R * bf + M * R * bf,            # dY, B -> dU
         "wgrad dB": M * N * bf + M * R * bf + N * R * f4,           # dY, U -> dB
-        "combine dU+dB": 0,
         "up dX": M * R * bf + R * K * bf + M * K * f4,              # dU, A -> dX
         "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA
-        "combine dA": 0,
+        "combine dA+dB": 0,
     }
 
 
@@ -274,11 +273,12 @@ def run_ours(args, world, rank, local):
         step(i)
     torch.cuda.synchronize()
 
-    # per-kernel events on a sample of the timed steps (fwd: 4 marks, bwd: 7 marks)
+    # per-kernel events on a sample of the timed steps (a mark before the first kernel and after each)
     n_prof = min(args.steps, 64)
     prof_steps = set(np.linspace(0, args.steps - 1, n_prof).astype(int).tolist())
-    fev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in prof_steps}
-    bev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(7)] for i in prof_steps}
+    n_bwd = len(KERNELS) - N_FWD
+    fev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(N_FWD + 1)] for i in prof_steps}
+    bev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(n_bwd + 1)] for i in prof_steps}
     for evs in list(fev.values()) + list(bev.values()):
         for e in evs:
             e.record(stream)
@@ -312,9 +312,9 @@ def run_ours(args, world, rank, local):
     ktimes = {k: [] for k in KERNELS}
     for i in prof_steps:
         f, b = fev[i], bev[i]
-        for j, name in enumerate(KERNELS[:3]):
+        for j, name in enumerate(KERNELS[:N_FWD]):
             ktimes[name].append(f[j].elapsed_time(f[j + 1]))
-        for j, name in enumerate(KERNELS[3:]):
+        for j, name in enumerate(KERNELS[N_FWD:]):
             ktimes[name].append(b[j].elapsed_time(b[j + 1]))
     kavg = {k: statistics.mean(v) for k, v in ktimes.items()}
     status = (ld.lora_delta_device_status(wf), ld.lora_delta_device_status(wb))
@@ -392,7 +392,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, BF16)",
-            "config": {"workload": "LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, 9 kernels)",
+            "config": {"workload": f"LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, {len(KERNELS)} kernels)",
                        "M": M, "K": K, "N": N, "R": R, "alpha": alpha, "accumulate": "fp32",
                        "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
                              "output stream per step, all larger than the 129 MB L2",
@@ -408,7 +408,7 @@ def run_ours(args, world, rank, local):
                             "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
                             "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None}
                         for k in KERNELS},
-            "gpu_launches": 9 * args.steps,
+            "gpu_launches": len(KERNELS) * args.steps,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,

@@ -182,10 +182,9 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
 
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
-  CUtensorMap m_x, m_a, m_u, m_b, m_y;
+  CUtensorMap m_x, m_a, m_b, m_y;
   if (!make_map(&m_x, x, false, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_u, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
       !make_map(&m_b, b, false, N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
       !make_map(&m_y, delta_y, true, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return LORA_ERR_CUDA;
@@ -200,11 +199,9 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
       cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
-  CombineJob ju{upart, u, int(ceil_div(K, down_slice(RP))), int(M), int(R), RP, 0};
-  if (launch_combine(&ju, 1, st) != cudaSuccess) return LORA_ERR_CUDA;
-  rec.mark();
-  if (launch_up(RP, false, m_u, m_b, m_y, int(M), int(N), alpha, status, grid_for(up_units(M, N, RP), nsm), st) !=
-      cudaSuccess)
+  // U = bf16(tree over the K-slice partials), built inside the up-projection, which also writes u
+  if (launch_up(RP, false, m_b, m_y, upart, int(ceil_div(K, down_slice(RP))), u, int(R), int(M), int(N), alpha, status,
+                grid_for(up_units(M, N, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
   return LORA_OK;
@@ -227,12 +224,11 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
 
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
-  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_du_rows, m_a, m_dx, m_x_chunk, m_du_chunk;
+  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_a, m_dx, m_x_chunk, m_du_chunk;
   if (!make_map(&m_dy_rows, dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_b_rows, b, false, N, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_dy_chunk, dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_u_chunk, u, false, M, R, RP, 64, swizzle_for_span(span)) ||
-      !make_map(&m_du_rows, du, false, M, R, RP, 128, swizzle_for_span(span)) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_dx, dx, true, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_x_chunk, x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -259,19 +255,18 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
                    grid_for(wgrad_units(M, N, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
-  CombineJob j2[2] = {{dupart, du, S, int(M), int(R), RP, 0}, {dbpart, db, C, int(N), int(R), RP, 1}};
-  if (launch_combine(j2, 2, st) != cudaSuccess) return LORA_ERR_CUDA;
-  rec.mark();
-  if (launch_up(RP, true, m_du_rows, m_a, m_dx, int(M), int(K), 1.0f, status, grid_for(up_units(M, K, RP), nsm), st) !=
-      cudaSuccess)
+  // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
+  if (launch_up(RP, true, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
+                grid_for(up_units(M, K, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
   if (launch_wgrad(RP, false, m_x_chunk, m_du_chunk, dapart, int(M), int(K), 1.0f, status,
                    grid_for(wgrad_units(M, K, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
-  CombineJob ja{dapart, da, C, int(R), int(K), RP, 2};
-  if (launch_combine(&ja, 1, st) != cudaSuccess) return LORA_ERR_CUDA;
+  // dA and dB: canonical tree over the chunk partials
+  CombineJob jobs[2] = {{dapart, da, C, int(K), int(R), RP, 0}, {dbpart, db, C, int(N), int(R), RP, 1}};
+  if (launch_combine(jobs, 2, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   return LORA_OK;
 }

@@ -1,67 +1,104 @@
-// combine.cu -- finishes the fixed summation tree across work-unit partials.
+// combine.cu -- finishes the fixed summation tree of the weight gradients.
 //
 // Every reduction of the operator is defined as: 16-term tensor-core leaves,
-// added by the canonical pairwise tree over the leaf index. The down and
-// weight-gradient kernels leave one FP32 partial per slice / row chunk (each a
+// added by the canonical pairwise tree over the leaf index. The weight-gradient
+// kernels leave one FP32 partial per 256-row chunk of the batch (each a
 // complete subtree over a power-of-two block of leaves); this kernel adds the
-// S partials of each output element with the same canonical tree, in FP32,
-// round to nearest, and writes the output: U and dU rounded to BF16 (the
-// rounding points "round to BF16" / "D4" of page "[DSv4][P5-3]
-// shared_grouped_lora_delta: CUDA + Triton, both batch-invariant", section
-// "Summary"), dA and dB in FP32. No atomics: one thread owns one output.
-#include <cuda_bf16.h>
-
+// C chunk partials of each element of dA and dB with the canonical tree over
+// the chunk index, in FP32, round to nearest ("dB = dV^T @ U", "dA = dU^T @ X"
+// of page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA + Triton, both
+// batch-invariant", section "Summary"). No atomics: one block owns 128 outputs.
+//
+// A block = 8 warps x 32 lanes: lanes run along the contiguous output index,
+// four outputs each (coalesced 16-byte reads of the [C][RP][cols] partials);
+// warp w adds a contiguous power-of-two block of P chunks with all its loads
+// in flight at once, and the eight warp results are added by a depth-3 tree.
+// The whole is the canonical tree over the chunks (zero padding on the right
+// changes no non-zero sum).
 #include <algorithm>
 
 #include "kernels.h"
 
 namespace lora {
 
-// Canonical pairwise tree over p[0], p[stride], ..., p[(S-1)*stride]: after
-// leaf i, merge once per trailing one bit of i; finally fold the remaining
-// stack from the right. Equals the level-by-level tree where node i pairs
-// with node i + 2^l whenever i is a multiple of 2^(l+1).
-__device__ __forceinline__ float canonical_sum(const float* __restrict__ p, size_t stride, int S) {
-  float stk[32];
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+// canonical tree over n <= 8 float4 values p[0], p[stride], ... (zero padded to 8)
+__device__ __forceinline__ float4 tree8_strided4(const float* __restrict__ p, size_t stride, int n) {
+  float4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    v[i] = i < n ? __ldcg(reinterpret_cast<const float4*>(p + size_t(i) * stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 1; w < 8; w <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; i += 2 * w) v[i] = add4(v[i], v[i + w]);
+  return v[0];
+}
+
+// canonical tree over n float4 values (any n >= 1): blocks of 8, then the canonical tree over blocks
+__device__ __forceinline__ float4 canonical_strided4(const float* __restrict__ p, size_t stride, int n) {
+  if (n <= 8) return tree8_strided4(p, stride, n);
+  float4 stk[32];
   int top = 0;
-  for (int i = 0; i < S; ++i) {
-    float v = p[size_t(i) * stride];
-    for (int t = i; t & 1; t >>= 1) v = __fadd_rn(stk[--top], v);
-    stk[top++] = v;
+  for (int b = 0; b * 8 < n; ++b) {
+    float4 x = tree8_strided4(p + size_t(b) * 8 * stride, stride, min(8, n - 8 * b));
+    for (int t = b; t & 1; t >>= 1) x = add4(stk[--top], x);
+    stk[top++] = x;
   }
-  if (top == 0) return 0.0f;
-  float r = stk[--top];
-  while (top > 0) r = __fadd_rn(stk[--top], r);
+  float4 r = stk[--top];
+  while (top > 0) r = add4(stk[--top], r);
   return r;
 }
 
-__global__ void __launch_bounds__(256) combine_kernel(CombineJob j0, CombineJob j1) {
-  const CombineJob& j = blockIdx.y == 0 ? j0 : j1;
-  const size_t n = size_t(j.rows) * j.cols;
-  for (size_t e = size_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += size_t(gridDim.x) * blockDim.x) {
-    if (j.mode == 0) {            // part[S][rows][RP] -> bf16 out[rows][R]
-      const size_t m = e / j.cols, r = e % j.cols;
-      const float s = canonical_sum(j.part + m * j.RP + r, size_t(j.rows) * j.RP, j.S);
-      reinterpret_cast<__nv_bfloat16*>(j.out)[e] = __float2bfloat16_rn(s);
-    } else if (j.mode == 1) {     // part[S][RP][rows] -> fp32 out[rows][R]; threads run along rows
-      const size_t r = e / j.rows, nidx = e % j.rows;
-      const float s = canonical_sum(j.part + r * j.rows + nidx, size_t(j.RP) * j.rows, j.S);
-      reinterpret_cast<float*>(j.out)[nidx * j.cols + r] = s;
-    } else {                      // part[S][RP][cols] -> fp32 out[R][cols]
-      const size_t r = e / j.cols, k = e % j.cols;
-      const float s = canonical_sum(j.part + r * j.cols + k, size_t(j.RP) * j.cols, j.S);
-      reinterpret_cast<float*>(j.out)[e] = s;
+__global__ void __launch_bounds__(256) combine_kernel(CombineJob j0, CombineJob j1, int P) {
+  const CombineJob& j = blockIdx.z == 0 ? j0 : j1;
+  const int r = blockIdx.y;
+  const int col0 = blockIdx.x * 128;
+  if (r >= j.R || col0 >= j.cols) return;                // uniform over the block
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = col0 + 4 * lane;                       // cols is a multiple of 8: all four in or all out
+  __shared__ float4 wsum[8][32];
+  const int c0 = warp * P;
+  const int n = max(0, min(P, j.C - c0));
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < j.cols && n > 0) {
+    const size_t stride = size_t(j.RP) * j.cols;
+    s = canonical_strided4(j.part + size_t(c0) * stride + size_t(r) * j.cols + col, stride, n);
+  }
+  wsum[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && col < j.cols) {
+    const float4 a = add4(add4(wsum[0][lane], wsum[1][lane]), add4(wsum[2][lane], wsum[3][lane]));
+    const float4 b = add4(add4(wsum[4][lane], wsum[5][lane]), add4(wsum[6][lane], wsum[7][lane]));
+    const float4 t = add4(a, b);
+    if (j.transpose) {
+      j.out[size_t(col) * j.R + r] = t.x;
+      j.out[size_t(col + 1) * j.R + r] = t.y;
+      j.out[size_t(col + 2) * j.R + r] = t.z;
+      j.out[size_t(col + 3) * j.R + r] = t.w;
+    } else {
+      *reinterpret_cast<float4*>(j.out + size_t(r) * j.cols + col) = t;
     }
   }
 }
 
 cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st) {
   if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
-  size_t most = 0;
-  for (int i = 0; i < njobs; ++i) most = std::max(most, size_t(jobs[i].rows) * jobs[i].cols);
-  if (most == 0) return cudaSuccess;
-  const unsigned bx = unsigned(std::min<size_t>((most + 255) / 256, 4096));
-  combine_kernel<<<dim3(bx, njobs), 256, 0, st>>>(jobs[0], njobs > 1 ? jobs[1] : jobs[0]);
+  int cmax = 0, colmax = 0, rmax = 0;
+  for (int i = 0; i < njobs; ++i) {
+    cmax = std::max(cmax, jobs[i].C);
+    colmax = std::max(colmax, jobs[i].cols);
+    rmax = std::max(rmax, jobs[i].R);
+  }
+  if (cmax == 0 || colmax == 0) return cudaSuccess;
+  // chunks per warp: the smallest power of two with 8 * P >= C (warp blocks stay power-of-two aligned)
+  int P = 1;
+  while (8 * P < cmax) P *= 2;
+  const dim3 grid(unsigned((colmax + 127) / 128), unsigned(rmax), unsigned(njobs));
+  combine_kernel<<<grid, 256, 0, st>>>(jobs[0], njobs > 1 ? jobs[1] : jobs[0], P);
   return cudaGetLastError();
 }
 

@@ -246,4 +246,83 @@ __device__ __forceinline__ float tree4(float l0, float l1, float l2, float l3) {
   return __fadd_rn(__fadd_rn(l0, l1), __fadd_rn(l2, l3));
 }
 
+// ------------------------------------------------ slice partials -> BF16 tile
+// Canonical pairwise tree over the first n (<= NB, NB a power of two) of NB
+// slices, for G groups of 8 consecutive FP32 values: group g of slice i is
+// p[i * stride + 8 g .. 8 g + 7] (16-byte aligned). Slices past n are zero,
+// which leaves every non-zero sum unchanged. All loads are issued before the
+// first add (the partials were just written by the previous kernel: L2).
+template <int NB, int G>
+__device__ __forceinline__ void block_slices(const float* p, size_t stride, int n, float (&o)[G][8]) {
+  float v[NB][G][8];
+#pragma unroll
+  for (int i = 0; i < NB; ++i)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (i < n) {
+        const float4* q = reinterpret_cast<const float4*>(p + size_t(i) * stride + 8 * g);
+        a = __ldcg(q);
+        b = __ldcg(q + 1);
+      }
+      v[i][g][0] = a.x; v[i][g][1] = a.y; v[i][g][2] = a.z; v[i][g][3] = a.w;
+      v[i][g][4] = b.x; v[i][g][5] = b.y; v[i][g][6] = b.z; v[i][g][7] = b.w;
+    }
+#pragma unroll
+  for (int w = 1; w < NB; w <<= 1)
+#pragma unroll
+    for (int i = 0; i < NB; i += 2 * w)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[i][g][c] = __fadd_rn(v[i][g][c], v[i + w][g][c]);
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) o[g][c] = v[0][g][c];
+}
+
+// Canonical pairwise tree over S slices (any S >= 1) of one group of 8 FP32
+// values: blocks of 8 slices (above), then the canonical tree over the blocks.
+__device__ __forceinline__ void sum_slices8(const float* p, size_t stride, int S, float (&o)[8]) {
+  float (&o1)[1][8] = reinterpret_cast<float (&)[1][8]>(o);
+  if (S <= 8) {
+    block_slices<8, 1>(p, stride, S, o1);
+    return;
+  }
+  float stk[24][8];
+  int top = 0;
+  for (int b = 0; b * 8 < S; ++b) {
+    float x[1][8];
+    block_slices<8, 1>(p + size_t(b) * 8 * stride, stride, min(8, S - 8 * b), x);
+    for (int t = b; t & 1; t >>= 1) {
+      --top;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) x[0][c] = __fadd_rn(stk[top][c], x[0][c]);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) stk[top][c] = x[0][c];
+    ++top;
+  }
+  --top;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) o[c] = stk[top][c];
+  while (top > 0) {
+    --top;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) o[c] = __fadd_rn(stk[top][c], o[c]);
+  }
+}
+
+// Round 8 FP32 values to BF16 (nearest even) and pack them into 16 bytes.
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&p2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 }  // namespace lora

@@ -33,21 +33,21 @@ inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil
 // word; `grid` the number of persistent CTAs.
 cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
                         float alpha, uint32_t* status, int grid, cudaStream_t st);
-cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int M,
-                      int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st);
+cudaError_t launch_up(int RP, bool dx, const CUtensorMap& b, const CUtensorMap& out, const float* part, int S,
+                      void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
+                      cudaStream_t st);
 cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int C,
                          float alpha, uint32_t* status, int grid, cudaStream_t st);
 
-// Combine jobs: canonical tree over S partials.
+// Final combine of the weight-gradient chunk partials: canonical tree over
+// the C chunks, FP32 out. part is [C][RP][cols] (cols = K for dA, N for dB).
 struct CombineJob {
-  const float* part;   // partials
-  void* out;           // output
-  int S;               // number of partials
-  int rows, cols;      // output is rows x cols (cols = R for U/dU and dB; K for dA)
-  int RP;              // padded rank (partials' rank dimension)
-  int mode;            // 0: part[S][rows][RP] -> bf16 out[rows][R=cols]
-                       // 1: part[S][RP][rows] -> fp32 out[rows][R=cols]   (dB: rows = N)
-                       // 2: part[S][RP][cols] -> fp32 out[rows=R][cols]   (dA: cols = K)
+  const float* part;
+  float* out;
+  int C;               // number of chunk partials
+  int cols;            // K (dA) or N (dB); a multiple of 8
+  int R, RP;           // rank and padded rank
+  int transpose;       // 0: out[R][cols] (dA); 1: out[cols][R] (dB)
 };
 cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st);
 

@@ -1,19 +1,28 @@
-// up.cu -- the rank-R expansions (write-bound):
-//   dY_lora[m][n] = fp32(sum_r u[m][r] * b[n][r]) * alpha   (forward "(U @ B^T) * alpha")
-//   dX[m][k]      = fp32(sum_r du[m][r] * a[r][k])          (backward "dX = dU @ A")
+// up.cu -- the rank-R expansions (write-bound), each with the combine of its
+// BF16 operand folded in:
+//   forward : U = bf16(tree over K-slices of the U partials)          (written to u)
+//             dY_lora[m][n] = fp32(sum_r u[m][r] * b[n][r]) * alpha    ("(U @ B^T) * alpha")
+//   backward: dU = bf16(tree over N-slices of the dU partials)         (written to du)
+//             dX[m][k] = fp32(sum_r du[m][r] * a[r][k])                ("dX = dU @ A")
 // (page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA + Triton, both
 // batch-invariant", section "Summary"; the alpha scale is fused into the
 // epilogue, as that page's "Benchmark" section proposes.)
 //
-// Work unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16). The
-// operands (U or dU tile, B or A tile) are a few KB from L2; the unit is one
-// tcgen05 MMA per 16-wide slice of R (M=128, N=BN, K=16), each into its own
-// TMEM accumulator, summed by the canonical pairwise tree. Eight epilogue
-// warps read TMEM, finish the tree (and the alpha multiply), stage 128 x 32
-// FP32 boxes in 128-byte-swizzled shared memory and write them with TMA
-// stores, so every output byte is written exactly once, in full lines.
+// Work unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16). Each CTA
+// takes a contiguous range of units (row-tile major), so it rebuilds each
+// 128 x RP BF16 operand tile once: four "prep" warps add the slice partials
+// left by the down kernel with the canonical pairwise tree (FP32, round to
+// nearest), round to BF16, write the tile into shared memory with the same
+// swizzle a TMA load would apply, and the unit with column tile 0 also stores
+// it to u / du in global memory. The unit is one tcgen05 MMA per 16-wide
+// slice of R (M=128, N=BN, K=16), each into its own TMEM accumulator, summed
+// by the canonical tree. Eight epilogue warps read TMEM, finish the tree (and
+// the alpha multiply), stage 128 x 32 FP32 boxes in 128-byte-swizzled shared
+// memory and write them with TMA stores, so every output byte is written
+// exactly once, in full lines.
 //
-// Warp roles: 0 = TMA producer, 1 = MMA issuer (TMEM owner), 2..9 = epilogue.
+// Warp roles: 0 = TMA producer (B / A weight tile), 1 = MMA issuer (TMEM
+// owner), 2..9 = epilogue, 10..13 = prep (operand tile from the partials).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,53 +40,59 @@ struct UpCfg {
   static constexpr int kStages = 2;
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kEpiWarps = 8, kPrepWarps = 4;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kPrepWarps);
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
+  static constexpr int kSub = kLeaves == 4 ? 2 : 1;    // TMEM loads per chunk in parts (register budget)
   static constexpr int kStg = 3;                       // staging buffers per column half
   static constexpr int kStgBytes = kBM * kChunk * 4;   // 16 KB
-  static constexpr int kNumBars = 2 * kStages + 2 * kBufs;
-  static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * kStg * kStgBytes + 1024 + kNumBars * 8 + 16;
-  static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
+  static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
+  static constexpr size_t kCacheOff = kStgOff + 2 * kStg * kStgBytes;   // operand tile cache
+  static constexpr size_t kBarOff = kCacheOff + kABytes;
+  static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1;
+  static constexpr size_t kSmem = kBarOff + 1024 + kNumBars * 8 + 16;
+  static_assert(kStageBytes % 1024 == 0 && kCacheOff % 1024 == 0, "tiles must stay 1024-byte aligned");
   static_assert(kBufs == 2, "double-buffered accumulators");
 };
 
 template <int RP, bool DX>
 __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
-    up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-              const __grid_constant__ CUtensorMap tm_out, int M, int Nout, int n_mt, int n_nt, float alpha,
-              uint32_t* status) {
+    up_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
+              const float* __restrict__ part, int S, __nv_bfloat16* __restrict__ out_bf16, int R, int M, int Nout,
+              int n_mt, int n_nt, float alpha, uint32_t* status) {
   using C = UpCfg<RP, DX>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t stg0 = base + C::kStages * C::kStageBytes;        // staging buffers [2 halves][kStg]
-  uint8_t* stg_ptr = gbase + C::kStages * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_ptr + 2 * C::kStg * C::kStgBytes);
+  const uint32_t stg0 = base + uint32_t(C::kStgOff);               // staging buffers [2 halves][kStg]
+  uint8_t* stg_ptr = gbase + C::kStgOff;
+  uint8_t* tile_cache = gbase + C::kCacheOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (C::kStages + s); };
   auto tfull = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
   auto tempty = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kBufs + b); };
+  const uint32_t drain = bar0 + 8u * (2 * C::kStages + 2 * C::kBufs);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full(s), 1);
+      mbar_init(full(s), 1 + C::kPrepWarps);   // producer (with the weight tile's bytes) + one per prep warp
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < C::kBufs; ++b) {
       mbar_init(tfull(b), 1);
       mbar_init(tempty(b), C::kEpiWarps);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0u;
     mbar_fence_init();
-    prefetch_map(&tm_a);
     prefetch_map(&tm_b);
     prefetch_map(&tm_out);
   }
@@ -91,6 +106,8 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, status};
   const int total = n_mt * n_nt;
+  const int u0 = int(int64_t(total) * blockIdx.x / gridDim.x);
+  const int u1 = int(int64_t(total) * (blockIdx.x + 1) / gridDim.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -98,12 +115,11 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       const uint64_t pol = policy_evict_last();
       Ring r;
       uint32_t issued = 0, parities = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int mt = u / n_nt, nt = u % n_nt;
+      for (int u = u0; u < u1; ++u) {
+        const int nt = u % n_nt;
         if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
           const uint32_t st = base + r.idx * C::kStageBytes;
-          mbar_expect_tx(full(r.idx), C::kStageBytes);
-          tma_load(st, &tm_a, full(r.idx), 0, mt * C::kBM, pol);                    // u/du rows
+          mbar_expect_tx(full(r.idx), C::kBBytes);
           if (DX) {
 #pragma unroll
             for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
@@ -125,7 +141,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(128, C::kBN, 0, DX ? 1 : 0);
       constexpr uint32_t lay = layout_for_span(C::kSpan);
       Ring r, b;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      for (int u = u0; u < u1; ++u) {
         bool ok = wait(full(r.idx), r.phase, ab, 13);
         ok = ok && wait(tempty(b.idx), b.phase ^ 1u, ab, 14);
         if (ok) {
@@ -148,8 +164,10 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
         r.next<C::kStages>();
         b.next<C::kBufs>();
       }
+      mma_commit(drain);                 // every MMA issued above has completed ...
+      wait_drain(drain, 0u, ab, 17);     // ... before TMEM is released
     }
-  } else {
+  } else if (warp < 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
@@ -160,7 +178,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     uint8_t* my_stg_ptr = stg_ptr + h * C::kStg * C::kStgBytes;
     int sidx = 0;
     Ring b;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    for (int u = u0; u < u1; ++u) {
       const int mt = u / n_nt, nt = u % n_nt;
       const bool ok = __all_sync(0xffffffffu, wait(tfull(b.idx), b.phase, ab, 15));
       tc_fence_after();
@@ -169,28 +187,39 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
         const int col0 = h * C::kHalfCols + c * C::kChunk;
         const int ncol = nt * C::kBN + col0;
         if (ncol >= Nout) break;                                     // uniform over the column half
-        uint32_t v[C::kLeaves][4][8];
-        if (ok) {
-#pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-#pragma unroll
-            for (int b8 = 0; b8 < 4; ++b8) tmem_ld8(trow + b.idx * C::kBufCols + j * C::kBN + col0 + b8 * 8, v[j][b8]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-#pragma unroll
-            for (int b8 = 0; b8 < 4; ++b8) reg_fence(v[j][b8]);
-        }
         float out[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int b8 = e / 8, k = e % 8;
-          float s;
-          if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
-          else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
-          else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
-                         __uint_as_float(v[3][b8][k]));
-          out[e] = DX ? s : __fmul_rn(s, alpha);
+        for (int sub = 0; sub < C::kSub; ++sub) {
+          constexpr int kW = 32 / C::kSub;                           // columns per TMEM load batch
+          uint32_t v[C::kLeaves][kW / 8][8];
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+            for (int b8 = 0; b8 < kW / 8; ++b8)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[j][b8][e] = 0u;
+          if (ok) {
+#pragma unroll
+            for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+              for (int b8 = 0; b8 < kW / 8; ++b8)
+                tmem_ld8(trow + b.idx * C::kBufCols + j * C::kBN + col0 + sub * kW + b8 * 8, v[j][b8]);
+            tmem_ld_wait();
+          }
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)
+#pragma unroll
+            for (int b8 = 0; b8 < kW / 8; ++b8) reg_fence(v[j][b8]);
+#pragma unroll
+          for (int e = 0; e < kW; ++e) {
+            const int b8 = e / 8, k = e % 8;
+            float s;
+            if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
+            else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
+            else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
+                           __uint_as_float(v[3][b8][k]));
+            out[sub * kW + e] = DX ? s : __fmul_rn(s, alpha);
+          }
         }
         if (leader) tma_store_wait_read<C::kStg - 1>();              // the buffer's previous store has read it
         named_bar(1 + h, 128);
@@ -213,6 +242,56 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       b.next<C::kBufs>();
     }
     if (leader) tma_store_wait_all<0>();
+  } else {
+    // ------------------------------------ prep: BF16 operand tile from the partials
+    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);           // 0..127: row within the tile
+    const int sw = ((t * C::kSpan) >> 7) & (C::kSpan / 16 - 1);     // swizzle of this row's 16-byte chunks
+    int cached_mt = -1;
+    Ring r;
+    for (int u = u0; u < u1; ++u) {
+      const int mt = u / n_nt, nt = u % n_nt;
+      if (mt != cached_mt) {
+        named_bar(3, 32 * C::kPrepWarps);                           // previous tile fully copied out
+        const int row = mt * C::kBM + t;
+        // chunk c (8 values): into the tile cache at its swizzled place; the unit owning the tile also stores it
+        auto emit = [&](int c, const float (&v)[8], bool valid) {
+          const uint4 packed = valid ? pack_bf16x8(v) : make_uint4(0u, 0u, 0u, 0u);
+          if (valid && nt == 0 && c * 8 < R) *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + c * 8) = packed;
+          *reinterpret_cast<uint4*>(tile_cache + t * C::kSpan + ((c ^ sw) * 16)) = packed;
+        };
+        const float* prow = part + size_t(row) * RP;
+        const size_t stride = size_t(M) * RP;
+        if (S <= 4) {
+#pragma unroll 1
+          for (int c = 0; c < RP / 8; c += 2) {                     // two chunks' loads in flight together
+            float v[2][8] = {};
+            if (row < M) block_slices<4, 2>(prow + c * 8, stride, S, v);
+            emit(c, v[0], row < M);
+            emit(c + 1, v[1], row < M);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < RP / 8; ++c) {
+            float v[8] = {};
+            if (row < M) sum_slices8(prow + c * 8, stride, S, v);
+            emit(c, v, row < M);
+          }
+        }
+        named_bar(3, 32 * C::kPrepWarps);                           // tile complete
+        cached_mt = mt;
+      }
+      const bool ok = __all_sync(0xffffffffu, wait(empty(r.idx), r.phase ^ 1u, ab, 18));
+      if (ok) {
+        const uint4* src = reinterpret_cast<const uint4*>(tile_cache);
+        uint4* dst = reinterpret_cast<uint4*>(gbase + r.idx * C::kStageBytes);
+#pragma unroll
+        for (int e = t; e < C::kABytes / 16; e += 32 * C::kPrepWarps) dst[e] = src[e];
+        fence_proxy_async();
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(full(r.idx));
+      r.next<C::kStages>();
+    }
   }
 
   tc_fence_before();
@@ -224,23 +303,25 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
 }
 
 template <int RP, bool DX>
-static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int M, int Nout,
-                              float alpha, uint32_t* status, int grid, cudaStream_t st) {
+static cudaError_t launch_one(const CUtensorMap& b, const CUtensorMap& out, const float* part, int S, void* out_bf16,
+                              int R, int M, int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st) {
   using C = UpCfg<RP, DX>;
   const int n_mt = int(ceil_div(M, C::kBM)), n_nt = int(ceil_div(Nout, C::kBN));
-  up_kernel<RP, DX><<<grid, C::kThreads, C::kSmem, st>>>(a, b, out, M, Nout, n_mt, n_nt, alpha, status);
+  up_kernel<RP, DX><<<grid, C::kThreads, C::kSmem, st>>>(b, out, part, S, static_cast<__nv_bfloat16*>(out_bf16), R, M,
+                                                          Nout, n_mt, n_nt, alpha, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int M,
-                      int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st) {
+cudaError_t launch_up(int RP, bool dx, const CUtensorMap& b, const CUtensorMap& out, const float* part, int S,
+                      void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
+                      cudaStream_t st) {
   switch (RP * 2 + (dx ? 1 : 0)) {
-    case 32: return launch_one<16, false>(a, b, out, M, Nout, alpha, status, grid, st);
-    case 33: return launch_one<16, true>(a, b, out, M, Nout, alpha, status, grid, st);
-    case 64: return launch_one<32, false>(a, b, out, M, Nout, alpha, status, grid, st);
-    case 65: return launch_one<32, true>(a, b, out, M, Nout, alpha, status, grid, st);
-    case 128: return launch_one<64, false>(a, b, out, M, Nout, alpha, status, grid, st);
-    case 129: return launch_one<64, true>(a, b, out, M, Nout, alpha, status, grid, st);
+    case 32: return launch_one<16, false>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 33: return launch_one<16, true>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 64: return launch_one<32, false>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 65: return launch_one<32, true>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 128: return launch_one<64, false>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 129: return launch_one<64, true>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
