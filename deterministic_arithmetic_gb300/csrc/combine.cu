@@ -17,6 +17,7 @@
 // changes no non-zero sum).
 #include <algorithm>
 
+#include "common.cuh"
 #include "kernels.h"
 
 namespace lora {
@@ -54,6 +55,8 @@ __device__ __forceinline__ float4 canonical_strided4(const float* __restrict__ p
 }
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineJob j0, CombineJob j1, int P) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const CombineJob& j = blockIdx.z == 0 ? j0 : j1;
   const int r = blockIdx.y;
   const int col0 = blockIdx.x * 128;
@@ -98,8 +101,7 @@ cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st) {
   int P = 1;
   while (8 * P < cmax) P *= 2;
   const dim3 grid(unsigned((colmax + 127) / 128), unsigned(rmax), unsigned(njobs));
-  combine_kernel<<<grid, 256, 0, st>>>(jobs[0], njobs > 1 ? jobs[1] : jobs[0], P);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, st, jobs[0], njobs > 1 ? jobs[1] : jobs[0], P);
 }
 
 }  // namespace lora

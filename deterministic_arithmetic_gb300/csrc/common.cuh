@@ -105,6 +105,17 @@ struct Ring {
   }
 };
 
+// ------------------------------------------- programmatic dependent launch
+// The kernels are launched with programmatic stream serialization: a kernel may
+// start (barrier set-up, TMEM allocation, tensor-map prefetch) while its
+// predecessor in the stream drains. Before touching global memory it waits for
+// the predecessor to finish and its writes to be visible; right after, it lets
+// its own successor start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

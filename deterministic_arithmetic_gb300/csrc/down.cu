@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
+  grid_dependents_launch();
   const Abort ab{abort_flag, status};
   const int total = n_mt * n_sl;
 
@@ -274,8 +276,8 @@ static cudaError_t launch_one(const CUtensorMap& in, const CUtensorMap& w, float
                               uint32_t* status, int grid, cudaStream_t st) {
   using C = DownCfg<RP, DV>;
   const int n_mt = int(ceil_div(M, C::kBM)), n_sl = int(ceil_div(Kred, C::kSlice));
-  down_kernel<RP, DV><<<grid, C::kThreads, C::kSmem, st>>>(in, w, part, M, Kred, n_mt, n_sl, alpha, status);
-  return cudaGetLastError();
+  return launch_pdl(down_kernel<RP, DV>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
+                    in, w, part, M, Kred, n_mt, n_sl, alpha, status);
 }
 
 cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,

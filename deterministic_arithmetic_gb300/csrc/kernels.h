@@ -24,6 +24,24 @@ constexpr int up_bn(int RP) { return 256 / (RP / 16); }
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Launch with programmatic stream serialization (the kernel calls
+// grid_dependency_wait() before its first global-memory access).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Work-unit counts (all launches use persistent CTAs over units).
 inline int64_t down_units(int64_t M, int64_t Kred, int RP) { return ceil_div(M, 128) * ceil_div(Kred, down_slice(RP)); }
 inline int64_t up_units(int64_t M, int64_t Nout, int RP) { return ceil_div(M, 128) * ceil_div(Nout, up_bn(RP)); }

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
+  grid_dependents_launch();
   const Abort ab{abort_flag, status};
   const int total = n_mt * n_nt;
   const int u0 = int(int64_t(total) * blockIdx.x / gridDim.x);
@@ -307,9 +309,9 @@ static cudaError_t launch_one(const CUtensorMap& b, const CUtensorMap& out, cons
                               int R, int M, int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st) {
   using C = UpCfg<RP, DX>;
   const int n_mt = int(ceil_div(M, C::kBM)), n_nt = int(ceil_div(Nout, C::kBN));
-  up_kernel<RP, DX><<<grid, C::kThreads, C::kSmem, st>>>(b, out, part, S, static_cast<__nv_bfloat16*>(out_bf16), R, M,
+  return launch_pdl(up_kernel<RP, DX>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
+                    b, out, part, S, static_cast<__nv_bfloat16*>(out_bf16), R, M,
                                                           Nout, n_mt, n_nt, alpha, status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_up(int RP, bool dx, const CUtensorMap& b, const CUtensorMap& out, const float* part, int S,

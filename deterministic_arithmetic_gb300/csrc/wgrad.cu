@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
+  grid_dependents_launch();
   const Abort ab{abort_flag, status};
   const int total = n_ct * n_ch;
   auto stages_of = [&](int ch) { return (min(M - ch * kWgradChunk, kWgradChunk) + C::kBR - 1) / C::kBR; };
@@ -259,8 +261,8 @@ static cudaError_t launch_one(const CUtensorMap& in, const CUtensorMap& g, float
                               uint32_t* status, int grid, cudaStream_t st) {
   using C = WgCfg<RP, DV>;
   const int n_ct = int(ceil_div(Cw, C::kBC)), n_ch = int(ceil_div(M, kWgradChunk));
-  wgrad_kernel<RP, DV><<<grid, C::kThreads, C::kSmem, st>>>(in, g, part, M, Cw, n_ct, n_ch, alpha, status);
-  return cudaGetLastError();
+  return launch_pdl(wgrad_kernel<RP, DV>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
+                    in, g, part, M, Cw, n_ct, n_ch, alpha, status);
 }
 
 cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int Cw,
