@@ -48,7 +48,8 @@ lora_status device_ready(int* num_sms) {
     d.num_sms = sms;
     d.usable = (major == 10 && minor == 3);
     if (d.usable) {
-      if (prepare_down() != cudaSuccess || prepare_up() != cudaSuccess || prepare_wgrad() != cudaSuccess) {
+      if (prepare_down() != cudaSuccess || prepare_up() != cudaSuccess || prepare_wgrad() != cudaSuccess ||
+          prepare_dy() != cudaSuccess) {
         d.probed = false;
         return LORA_ERR_CUDA;
       }
@@ -115,7 +116,7 @@ struct BwdLayout {
 };
 BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int64_t R) {
   const int RP = padded_rank(int(R));
-  const size_t S = size_t(ceil_div(N, down_slice(RP)));
+  const size_t S = size_t(ceil_div(N, du_slice(RP)));
   const size_t C = size_t(ceil_div(M, kWgradChunk));
   BwdLayout l;
   l.dupart = kStatusBytes;
@@ -224,7 +225,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
 
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
-  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_a, m_dx, m_x_chunk, m_du_chunk;
+  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_a, m_dx, m_x_chunk, m_du_chunk, m_b_128, m_u_128;
   if (!make_map(&m_dy_rows, dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_b_rows, b, false, N, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_dy_chunk, dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -232,7 +233,9 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_dx, dx, true, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_x_chunk, x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_du_chunk, du, false, M, R, RP, 64, swizzle_for_span(span)))
+      !make_map(&m_du_chunk, du, false, M, R, RP, 64, swizzle_for_span(span)) ||
+      !make_map(&m_b_128, b, false, N, R, RP, 128, swizzle_for_span(span)) ||
+      !make_map(&m_u_128, u, false, M, R, RP, 128, swizzle_for_span(span)))
     return LORA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -241,20 +244,28 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
   float* dupart = reinterpret_cast<float*>(ws + L.dupart);
   float* dbpart = reinterpret_cast<float*>(ws + L.dbpart);
   float* dapart = reinterpret_cast<float*>(ws + L.dapart);
-  const int S = int(ceil_div(N, down_slice(RP)));
+  const int S = int(ceil_div(N, du_slice(RP)));
   const int C = int(ceil_div(M, kWgradChunk));
   Recorder rec(st);
   rec.mark();
-  // dU partials over slices of N (dV formed in shared memory)
-  if (launch_down(RP, true, m_dy_rows, m_b_rows, dupart, int(M), int(N), alpha, status,
-                  grid_for(down_units(M, N, RP), nsm), st) != cudaSuccess)
-    return LORA_ERR_CUDA;
-  rec.mark();
-  // dB chunk partials over 256-row chunks of M
-  if (launch_wgrad(RP, true, m_dy_chunk, m_u_chunk, dbpart, int(M), int(N), alpha, status,
-                   grid_for(wgrad_units(M, N, RP), nsm), st) != cudaSuccess)
-    return LORA_ERR_CUDA;
-  rec.mark();
+  if (RP == 16) {
+    // one pass over dY: dU partials over 512-column slices, dB partials over 256-row chunks
+    if (launch_dy(m_dy_rows, m_b_128, m_u_128, dupart, dbpart, int(M), int(N), alpha, status,
+                  grid_for(ceil_div(M, kDyChunk) * ceil_div(N, kDySlice), nsm), st) != cudaSuccess)
+      return LORA_ERR_CUDA;
+    rec.mark();
+  } else {
+    // dU partials over slices of N (dV formed in shared memory)
+    if (launch_down(RP, true, m_dy_rows, m_b_rows, dupart, int(M), int(N), alpha, status,
+                    grid_for(down_units(M, N, RP), nsm), st) != cudaSuccess)
+      return LORA_ERR_CUDA;
+    rec.mark();
+    // dB chunk partials over 256-row chunks of M
+    if (launch_wgrad(RP, true, m_dy_chunk, m_u_chunk, dbpart, int(M), int(N), alpha, status,
+                     grid_for(wgrad_units(M, N, RP), nsm), st) != cudaSuccess)
+      return LORA_ERR_CUDA;
+    rec.mark();
+  }
   // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
   if (launch_up(RP, true, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
                 grid_for(up_units(M, K, RP), nsm), st) != cudaSuccess)
@@ -295,7 +306,8 @@ size_t lora_delta_describe(char* buf, size_t len) {
       "\"numeric_profile\": \"bf16 inputs; 16-term tcgen05 leaves (fresh FP32 accumulator); "
       "canonical pairwise FP32 tree over leaves; BF16 rounding of U, dV, dU\", "
       "\"reduction\": \"tree depends only on the reduction length; K-slices %d/%d/%d (R<=16/32/64), "
-      "batch chunks %d rows; no split-K on M, no atomics\", "
+      "batch chunks %d rows; R<=16 backward reads dY once for dU (512-column slices) and dB; "
+      "no split-K on M, no atomics\", "
       "\"tiles\": \"down 128x64 stages, up 128x(256/(RP/16)), wgrad 128 cols x 64 rows\", "
       "\"arch\": \"sm_103a\"}",
       down_slice(16), down_slice(32), down_slice(64), kWgradChunk);

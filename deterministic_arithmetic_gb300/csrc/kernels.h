@@ -19,6 +19,11 @@ constexpr int padded_rank(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
 constexpr int down_slice(int RP) { return RP == 64 ? 256 : 1024; }
 // Weight gradients (dA, dB): rows of the batch are cut into fixed chunks.
 constexpr int kWgradChunk = 256;
+// Fused dU + dB pass over dY (R <= 16): 512-column slices of N (dU partials)
+// and 256-row chunks of M (dB partials).
+constexpr int kDySlice = 512, kDyChunk = 256;
+// Slices the dU partials of the backward pass are cut into (ranks <= 16 use the fused pass).
+constexpr int du_slice(int RP) { return RP == 16 ? kDySlice : down_slice(RP); }
 // Up-projection tile width (N direction) per padded rank.
 constexpr int up_bn(int RP) { return 256 / (RP / 16); }
 
@@ -54,6 +59,8 @@ cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMa
 cudaError_t launch_up(int RP, bool dx, const CUtensorMap& b, const CUtensorMap& out, const float* part, int S,
                       void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
                       cudaStream_t st);
+cudaError_t launch_dy(const CUtensorMap& dy, const CUtensorMap& b, const CUtensorMap& u, float* du_part,
+                      float* db_part, int M, int N, float alpha, uint32_t* status, int grid, cudaStream_t st);
 cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int C,
                          float alpha, uint32_t* status, int grid, cudaStream_t st);
 
@@ -74,5 +81,6 @@ cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st);
 cudaError_t prepare_down();
 cudaError_t prepare_up();
 cudaError_t prepare_wgrad();
+cudaError_t prepare_dy();
 
 }  // namespace lora

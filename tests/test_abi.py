@@ -58,8 +58,8 @@ def test_workspace_sizes():
     b = ld.lora_delta_bwd_workspace_size(8192, 4096, 4096, 16)
     # U partials: 4 slices of 1024 x 8192 rows x 16 x fp32, plus the 256-byte status block
     assert f == 256 + 4 * 8192 * 16 * 4
-    # dU partials (4 slices), dB and dA chunk partials (32 chunks of 256 rows)
-    assert b == 256 + 4 * 8192 * 16 * 4 + 32 * 16 * 4096 * 4 + 32 * 16 * 4096 * 4
+    # dU partials (8 slices of 512 columns: the fused dY pass), dB and dA chunk partials (32 chunks of 256 rows)
+    assert b == 256 + 8 * 8192 * 16 * 4 + 32 * 16 * 4096 * 4 + 32 * 16 * 4096 * 4
     assert ld.lora_delta_fwd_workspace_size(0, 128, 96, 8) == 256
     for bad in ((8, 100, 96, 8), (8, 128, 90, 8), (8, 128, 96, 12), (8, 128, 96, 72), (-1, 128, 96, 8), (8, 0, 96, 8)):
         assert ld.lora_delta_fwd_workspace_size(*bad) == 0
