@@ -187,7 +187,7 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
   if (!make_map(&m_x, x, false, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_b, b, false, N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
-      !make_map(&m_y, delta_y, true, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&m_y, delta_y, true, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return LORA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -231,7 +231,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
       !make_map(&m_dy_chunk, dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_u_chunk, u, false, M, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_dx, dx, true, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m_dx, dx, true, M, K, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_x_chunk, x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_du_chunk, du, false, M, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_b_128, b, false, N, R, RP, 128, swizzle_for_span(span)) ||

@@ -17,9 +17,10 @@
 // it to u / du in global memory. The unit is one tcgen05 MMA per 16-wide
 // slice of R (M=128, N=BN, K=16), each into its own TMEM accumulator, summed
 // by the canonical tree. Eight epilogue warps read TMEM, finish the tree (and
-// the alpha multiply), stage 128 x 32 FP32 boxes in 128-byte-swizzled shared
-// memory and write them with TMA stores, so every output byte is written
-// exactly once, in full lines.
+// the alpha multiply); each warp stages its own 32 x 32 FP32 boxes in
+// 128-byte-swizzled shared memory (a ring of four, no barrier across warps)
+// and writes them with TMA stores, so every output byte is written exactly
+// once, in full lines.
 //
 // Warp roles: 0 = TMA producer (B / A weight tile), 1 = MMA issuer (TMEM
 // owner), 2..9 = epilogue, 10..13 = prep (operand tile from the partials).
@@ -46,10 +47,10 @@ struct UpCfg {
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
   static constexpr int kSub = kLeaves == 4 ? 2 : 1;    // TMEM loads per chunk in parts (register budget)
-  static constexpr int kStg = 3;                       // staging buffers per column half
-  static constexpr int kStgBytes = kBM * kChunk * 4;   // 16 KB
+  static constexpr int kStg = 4;                       // staging buffers per epilogue warp
+  static constexpr int kStgBytes = 32 * kChunk * 4;    // one 32-row x 32-column FP32 box: 4 KB
   static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
-  static constexpr size_t kCacheOff = kStgOff + 2 * kStg * kStgBytes;   // operand tile cache
+  static constexpr size_t kCacheOff = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;   // operand tile cache
   static constexpr size_t kBarOff = kCacheOff + kABytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1;
   static constexpr size_t kSmem = kBarOff + 1024 + kNumBars * 8 + 16;
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t stg0 = base + uint32_t(C::kStgOff);               // staging buffers [2 halves][kStg]
+  const uint32_t stg0 = base + uint32_t(C::kStgOff);               // staging buffers [epilogue warp][kStg]
   uint8_t* stg_ptr = gbase + C::kStgOff;
   uint8_t* tile_cache = gbase + C::kCacheOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
@@ -173,11 +174,9 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
-    const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
-    const int rl = q * 32 + lane;                                   // row within the tile
     const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
-    const uint32_t my_stg = stg0 + h * C::kStg * C::kStgBytes;
-    uint8_t* my_stg_ptr = stg_ptr + h * C::kStg * C::kStgBytes;
+    const uint32_t my_stg = stg0 + (warp - 2) * C::kStg * C::kStgBytes;
+    uint8_t* my_stg_ptr = stg_ptr + (warp - 2) * C::kStg * C::kStgBytes;
     int sidx = 0;
     Ring b;
     for (int u = u0; u < u1; ++u) {
@@ -223,17 +222,19 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
             out[sub * kW + e] = DX ? s : __fmul_rn(s, alpha);
           }
         }
-        if (leader) tma_store_wait_read<C::kStg - 1>();              // the buffer's previous store has read it
-        named_bar(1 + h, 128);
-        uint8_t* buf = my_stg_ptr + sidx * C::kStgBytes + rl * 128;
+        // each warp stores its own 32 rows x 32 columns: no barrier across warps
+        if (lane == 0) tma_store_wait_read<C::kStg - 1>();           // this buffer's previous store has read it
+        __syncwarp();
+        uint8_t* buf = my_stg_ptr + sidx * C::kStgBytes + lane * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)                               // 128-byte swizzle: chunk ^ (row % 8)
-          *reinterpret_cast<float4*>(buf + ((cc ^ (rl & 7)) * 16)) =
+          *reinterpret_cast<float4*>(buf + ((cc ^ (lane & 7)) * 16)) =
               make_float4(out[4 * cc], out[4 * cc + 1], out[4 * cc + 2], out[4 * cc + 3]);
         fence_proxy_async();
-        named_bar(1 + h, 128);
-        if (leader && ok) {
-          tma_store(&tm_out, my_stg + sidx * C::kStgBytes, ncol, mt * C::kBM);
+        __syncwarp();
+        const int row0 = mt * C::kBM + q * 32;
+        if (lane == 0 && ok && row0 < M) {
+          tma_store(&tm_out, my_stg + sidx * C::kStgBytes, ncol, row0);
           tma_store_commit();
         }
         sidx = sidx + 1 == C::kStg ? 0 : sidx + 1;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       if (ok && lane == 0) mbar_arrive(tempty(b.idx));
       b.next<C::kBufs>();
     }
-    if (leader) tma_store_wait_all<0>();
+    if (lane == 0) tma_store_wait_all<0>();
   } else {
     // ------------------------------------ prep: BF16 operand tile from the partials
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);           // 0..127: row within the tile
