@@ -38,7 +38,7 @@ struct UpCfg {
   static constexpr int kABytes = kBM * RP * 2;         // U / dU tile [128][RP]
   static constexpr int kBBytes = kBN * RP * 2;         // B tile [BN][RP] or A tile [RP][BN]
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = 2;
+  static constexpr int kStages = RP == 16 ? 6 : (RP == 32 ? 5 : 3);   // operand ring (weight tile from L2)
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
   static constexpr int kEpiWarps = 8, kPrepWarps = 4;
@@ -46,7 +46,9 @@ struct UpCfg {
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
-  static constexpr int kSub = kLeaves == 4 ? 2 : 1;    // TMEM loads per chunk in parts (register budget)
+  static constexpr int kCols = kLeaves == 1 ? 64 : (kLeaves == 2 ? 32 : 16);   // TMEM columns per load round
+  static constexpr int kBoxes = kCols >= kChunk ? kCols / kChunk : 1;           // store boxes per round group
+  static constexpr int kRounds = kCols >= kChunk ? 1 : kChunk / kCols;          // load rounds per box group
   static constexpr int kStg = 4;                       // staging buffers per epilogue warp
   static constexpr int kStgBytes = 32 * kChunk * 4;    // one 32-row x 32-column FP32 box: 4 KB
   static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
@@ -183,61 +185,69 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       const int mt = u / n_nt, nt = u % n_nt;
       const bool ok = __all_sync(0xffffffffu, wait(tfull(b.idx), b.phase, ab, 15));
       tc_fence_after();
+      // one TMEM round trip per group of kBoxes 32-column boxes (64 registers of leaves per round)
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) {
-        const int col0 = h * C::kHalfCols + c * C::kChunk;
-        const int ncol = nt * C::kBN + col0;
-        if (ncol >= Nout) break;                                     // uniform over the column half
-        float out[32];
+      for (int grp = 0; grp < C::kChunks / C::kBoxes; ++grp) {
+        const int col0 = h * C::kHalfCols + grp * C::kBoxes * C::kChunk;
+        if (nt * C::kBN + col0 >= Nout) break;                       // uniform over the column half
+        if (lane == 0) tma_store_wait_read<C::kStg - C::kBoxes>();   // these buffers' previous stores have read them
+        __syncwarp();
 #pragma unroll
-        for (int sub = 0; sub < C::kSub; ++sub) {
-          constexpr int kW = 32 / C::kSub;                           // columns per TMEM load batch
-          uint32_t v[C::kLeaves][kW / 8][8];
+        for (int rd = 0; rd < C::kRounds; ++rd) {
+          uint32_t v[C::kLeaves][C::kCols / 8][8];
 #pragma unroll
           for (int j = 0; j < C::kLeaves; ++j)
 #pragma unroll
-            for (int b8 = 0; b8 < kW / 8; ++b8)
+            for (int b8 = 0; b8 < C::kCols / 8; ++b8)
 #pragma unroll
               for (int e = 0; e < 8; ++e) v[j][b8][e] = 0u;
           if (ok) {
 #pragma unroll
             for (int j = 0; j < C::kLeaves; ++j)
 #pragma unroll
-              for (int b8 = 0; b8 < kW / 8; ++b8)
-                tmem_ld8(trow + b.idx * C::kBufCols + j * C::kBN + col0 + sub * kW + b8 * 8, v[j][b8]);
+              for (int b8 = 0; b8 < C::kCols / 8; ++b8)
+                tmem_ld8(trow + b.idx * C::kBufCols + j * C::kBN + col0 + rd * C::kCols + b8 * 8, v[j][b8]);
             tmem_ld_wait();
           }
 #pragma unroll
           for (int j = 0; j < C::kLeaves; ++j)
 #pragma unroll
-            for (int b8 = 0; b8 < kW / 8; ++b8) reg_fence(v[j][b8]);
+            for (int b8 = 0; b8 < C::kCols / 8; ++b8) reg_fence(v[j][b8]);
 #pragma unroll
-          for (int e = 0; e < kW; ++e) {
-            const int b8 = e / 8, k = e % 8;
-            float s;
-            if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
-            else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
-            else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
-                           __uint_as_float(v[3][b8][k]));
-            out[sub * kW + e] = DX ? s : __fmul_rn(s, alpha);
+          for (int e4 = 0; e4 < C::kCols / 4; ++e4) {
+            const int gcol = rd * C::kCols + e4 * 4;                  // column within the group
+            const int box = gcol / C::kChunk, cc = (gcol % C::kChunk) / 4;
+            float f[4];
+#pragma unroll
+            for (int t4 = 0; t4 < 4; ++t4) {
+              const int e = e4 * 4 + t4, b8 = e / 8, k = e % 8;
+              float s;
+              if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
+              else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
+              else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
+                             __uint_as_float(v[3][b8][k]));
+              f[t4] = DX ? s : __fmul_rn(s, alpha);
+            }
+            // each warp stages its own 32 rows x 32 columns: 128-byte swizzle, chunk ^ (row % 8)
+            uint8_t* buf = my_stg_ptr + ((sidx + box) % C::kStg) * C::kStgBytes + lane * 128;
+            *reinterpret_cast<float4*>(buf + ((cc ^ (lane & 7)) * 16)) = make_float4(f[0], f[1], f[2], f[3]);
           }
         }
-        // each warp stores its own 32 rows x 32 columns: no barrier across warps
-        if (lane == 0) tma_store_wait_read<C::kStg - 1>();           // this buffer's previous store has read it
-        __syncwarp();
-        uint8_t* buf = my_stg_ptr + sidx * C::kStgBytes + lane * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)                               // 128-byte swizzle: chunk ^ (row % 8)
-          *reinterpret_cast<float4*>(buf + ((cc ^ (lane & 7)) * 16)) =
-              make_float4(out[4 * cc], out[4 * cc + 1], out[4 * cc + 2], out[4 * cc + 3]);
         fence_proxy_async();
         __syncwarp();
         const int row0 = mt * C::kBM + q * 32;
-        if (lane == 0 && ok && row0 < M) {
-          tma_store(&tm_out, my_stg + sidx * C::kStgBytes, ncol, row0);
-          tma_store_commit();
+        if (lane == 0) {
+          // one bulk group per staging buffer, empty when the box lies past M or N, so that
+          // "at most kStg - kBoxes groups pending" always frees exactly the buffers reused next
+#pragma unroll
+          for (int box = 0; box < C::kBoxes; ++box) {
+            const int ncol = nt * C::kBN + col0 + box * C::kChunk;
+            if (ok && row0 < M && ncol < Nout)
+              tma_store(&tm_out, my_stg + ((sidx + box) % C::kStg) * C::kStgBytes, ncol, row0);
+            tma_store_commit();
+          }
         }
-        sidx = sidx + 1 == C::kStg ? 0 : sidx + 1;
+        sidx = (sidx + C::kBoxes) % C::kStg;
       }
       tc_fence_before();
       __syncwarp();

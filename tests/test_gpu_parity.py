@@ -113,6 +113,20 @@ def _check_subbatches(d, alpha, full, sizes):
                 G.assert_bitwise(f"{k} rows {rows.start}:{rows.stop}", sub[k], ref[k])
 
 
+def test_ragged_tails_are_stable_across_reruns():
+    """Batches whose last 128-row tile is partly empty, run several times:
+    warps whose rows lie past M skip their stores, which must not disturb the
+    staging of the rows before them (every run bit-identical to the full batch)."""
+    w = S.Workload("ragged", S.Shape(4224, 512, 4096, 16, 2.0), {"x": 1.0, "a": 512 ** -0.5, "b": 0.25, "dy": 1.0})
+    d = w.generate(4)
+    full = G.run(d, w.shape.alpha)
+    for s in (4097, 4098, 4100, 4160, 4223):
+        for _ in range(3):
+            sub = G.run(d, w.shape.alpha, rows=slice(0, s))
+            for k in ("u", "delta_y", "du", "dx"):
+                G.assert_bitwise(f"{k} rows 0:{s}", sub[k], full[k][:s])
+
+
 def test_tiny_batch_invariance():
     w = S.tiny()
     d = w.generate(0)
