@@ -347,37 +347,66 @@ def run_ours(args, world, rank, local):
                     du=torch.empty((M, R), dtype=torch.int16).pin_memory())
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
         d2h = sum(t.numel() * t.element_size() for t in outs.values())
-        xi, dyi = Xs[0], DYs[0]
+        # pipelined like a data loader: step i's inputs are copied in on one stream, its compute runs on
+        # another and its outputs are copied out on a third, so copy-in of step i+1 and copy-out of step
+        # i-1 overlap step i's kernels; device buffers are double-buffered (set i % 2)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        sets = []
+        for k in range(2):
+            sets.append(dict(x=Xs[k], dy=DYs[k], a=torch.empty_like(A), b=torch.empty_like(B),
+                             y=torch.empty_like(Y), u=torch.empty_like(U), dx=torch.empty_like(DX),
+                             da=torch.empty_like(DA), db=torch.empty_like(DB), du=torch.empty_like(DU),
+                             wf=ld.new_workspace(wf.numel(), dev), wb=ld.new_workspace(wb.numel(), dev)))
 
-        def e2e_step():
-            xi.view(torch.int16).copy_(pin["x"], non_blocking=True)
-            DYs[0].view(torch.int16).copy_(pin["dy"], non_blocking=True)
-            A.view(torch.int16).copy_(pin["a"], non_blocking=True)
-            B.view(torch.int16).copy_(pin["b"], non_blocking=True)
-            ld.lora_delta_fwd(xi, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
-            ld.lora_delta_bwd(dyi, xi, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
-            outs["y"].copy_(Y, non_blocking=True)
-            outs["u"].copy_(U.view(torch.int16), non_blocking=True)
-            outs["dx"].copy_(DX, non_blocking=True)
-            outs["da"].copy_(DA, non_blocking=True)
-            outs["db"].copy_(DB, non_blocking=True)
-            outs["du"].copy_(DU.view(torch.int16), non_blocking=True)
+        def ev():
+            return torch.cuda.Event()
 
-        for _ in range(2):
-            e2e_step()
+        def e2e_steps(n):
+            done_in, done_compute, done_out = {}, {}, {}
+            for i in range(n):
+                b_ = sets[i % 2]
+                with torch.cuda.stream(s_in):                      # copy-in (after step i-2 released the set)
+                    if i - 2 in done_compute:
+                        s_in.wait_event(done_compute[i - 2])
+                    b_["x"].view(torch.int16).copy_(pin["x"], non_blocking=True)
+                    b_["dy"].view(torch.int16).copy_(pin["dy"], non_blocking=True)
+                    b_["a"].view(torch.int16).copy_(pin["a"], non_blocking=True)
+                    b_["b"].view(torch.int16).copy_(pin["b"], non_blocking=True)
+                    done_in[i] = ev(); done_in[i].record(s_in)
+                stream.wait_event(done_in[i])                       # compute
+                if i - 2 in done_out:
+                    stream.wait_event(done_out[i - 2])
+                ld.lora_delta_fwd(b_["x"], b_["a"], b_["b"], alpha, delta_y=b_["y"], u=b_["u"], workspace=b_["wf"],
+                                  stream=stream)
+                ld.lora_delta_bwd(b_["dy"], b_["x"], b_["a"], b_["b"], b_["u"], alpha, dx=b_["dx"], da=b_["da"],
+                                  db=b_["db"], du=b_["du"], workspace=b_["wb"], stream=stream)
+                done_compute[i] = ev(); done_compute[i].record(stream)
+                with torch.cuda.stream(s_out):                     # copy-out
+                    s_out.wait_event(done_compute[i])
+                    outs["y"].copy_(b_["y"], non_blocking=True)
+                    outs["u"].copy_(b_["u"].view(torch.int16), non_blocking=True)
+                    outs["dx"].copy_(b_["dx"], non_blocking=True)
+                    outs["da"].copy_(b_["da"], non_blocking=True)
+                    outs["db"].copy_(b_["db"], non_blocking=True)
+                    outs["du"].copy_(b_["du"].view(torch.int16), non_blocking=True)
+                    done_out[i] = ev(); done_out[i].record(s_out)
+            return done_out[n - 1]
+
+        e2e_steps(3)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_in)
+        last = e2e_steps(args.e2e_steps)
+        s_out.wait_event(last)
+        e1.record(s_out)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.e2e_steps
         e2e = {"value": round(total_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": args.e2e_steps}
+               "steps": args.e2e_steps,
+               "pipeline": "copy-in, compute and copy-out of consecutive steps on three streams, 2 device buffer sets"}
 
     # ---------------------------------------------------------- CPU baseline
     cpu = None
