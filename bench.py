@@ -328,7 +328,7 @@ def run_ours(args, world, rank, local):
     value = total_bytes * world / (ms_step * 1e-3) / 1e9
     dominant = max(kavg, key=lambda k: kavg[k])
     achieved = alg[dominant] / (kavg[dominant] * 1e-3) / 1e9
-    src = {"down": "down.cu", "up": "up.cu", "wgrad": "wgrad.cu", "combine": "combine.cu"}[dominant.split()[0]]
+    src = dominant.split()[0] + ".cu"                   # down.cu, up.cu, dy.cu, wgrad.cu, combine.cu
     tr = NCU_TRAFFIC.get(dominant)
     traffic = tr["bytes"] if tr and tr.get("src_hash") == source_hash(src) else None
 
