@@ -70,7 +70,7 @@ def measured_peaks():
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by kernel, with the hash of the kernel source
 # the counters were taken on; a kernel changed since then reports null.
-NCU_TRAFFIC = {   # profiles/train_step_M8192_K4096_N4096_R16.md, section 2 (warm caches, per launch)
+NCU_TRAFFIC = {   # ncu, training step, warm caches (--cache-control none), per launch
     "down U": {"bytes": 73700000, "src_hash": "55f23a44b08732cf"},
     "up dY_lora": {"bytes": 123800000, "src_hash": "e89ff81c4b3c9243"},
     "dy dU+dB": {"bytes": 84400000, "src_hash": "697dd60deb2121b9"},
