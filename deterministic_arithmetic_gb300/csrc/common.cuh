@@ -227,6 +227,24 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= static_cast<uint64_t>(layout) << 61;
   return d;
 }
+// The same descriptor `bytes` further on in shared memory. The start-address
+// field holds address / 16 in 14 bits; every operand of these kernels lies
+// below 256 KB, so the add never carries out of the field.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+// One lane of a converged warp (the issuing thread of a tcgen05.mma / commit).
+// Running the issue loop on the whole warp keeps its descriptor arithmetic
+// warp-uniform, so it stays off the per-thread register path.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0u;
+}
+
 // Instruction descriptor, kind::f16: BF16 A and B, FP32 D, dense; a_mn / b_mn
 // select MN-major (1) or K-major (0) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -247,6 +265,29 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float alpha) {
     w[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The same transform when alpha = 2^k (alpha > 0, |k| <= 12): the packed BF16
+// multiply rounds the same exact product once, so it gives the same bits
+// (zeros, subnormals, overflow to infinity and NaNs included: checked against
+// the FP32 form above for all 65536 inputs and every such k) in a quarter of
+// the instructions. pow2_bf16x2 returns alpha as BF16 in both halves of a
+// word, or 0 when alpha is not of that form.
+__device__ __forceinline__ uint32_t pow2_bf16x2(float alpha) {
+  const uint32_t b = __float_as_uint(alpha);
+  const uint32_t e = (b >> 23) & 0xFFu;
+  if ((b & 0x807FFFFFu) != 0u || e < 127u - 12u || e > 127u + 12u) return 0u;
+  return (b >> 16) * 0x00010001u;
+}
+__device__ __forceinline__ uint4 scale_bf16x8_pow2(uint4 v, uint32_t a2) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(w[i]), "r"(a2));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// dV for one 16-byte chunk, taking the packed form when a2 != 0.
+__device__ __forceinline__ uint4 dv_bf16x8(uint4 v, float alpha, uint32_t a2) {
+  return a2 ? scale_bf16x8_pow2(v, a2) : scale_bf16x8(v, alpha);
 }
 
 // The fixed summation tree. Leaves are 16-term tensor-core dot products

@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
   } else {
     // ---------------------------------------------------- dV = bf16(dY*alpha)
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);   // 0..127
+    const uint32_t a2 = pow2_bf16x2(alpha);
     Ring r;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const int sl = u / n_mt;
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
         if (wait(full(r.idx), r.phase, ab, 7)) {
           uint4* tile = reinterpret_cast<uint4*>(smem_raw + (base - raw) + size_t(r.idx) * C::kStageBytes);
 #pragma unroll
-          for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = scale_bf16x8(tile[t + 128 * e], alpha);
+          for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = dv_bf16x8(tile[t + 128 * e], alpha, a2);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(ready(r.idx));

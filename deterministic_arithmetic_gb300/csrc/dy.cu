@@ -49,6 +49,7 @@ struct DyCfg {
   static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
   static_assert(kSliceTiles == 4 && kChunkTiles == 2, "epilogue tree shape");
   static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
+  static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
 
 // tree over 4 leaves (8 columns each) starting at TMEM column `col`, 16 columns apart
@@ -156,46 +157,53 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_du = idesc_bf16(128, RP, 0, 1);   // dV K-major, b MN-major
-      constexpr uint32_t idesc_db = idesc_bf16(128, RP, 1, 1);   // dV^T MN-major, u MN-major
-      Ring r, g;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int sl = u % n_sl, ch = u / n_sl;
-        const int nstages = n_tiles(sl) * r_tiles(ch);
-        for (int k = 0; k < nstages; ++k) {
-          bool ok = wait(ready(r.idx), r.phase, ab, 33);
-          ok = ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 34);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t st = base + r.idx * C::kStageBytes;
-            const uint32_t d = tmem + g.idx * C::kGroupCols;
+    // The whole warp follows the schedule; one elected lane issues. Operand
+    // descriptors are built once for stage 0 and advanced by the stage offset.
+    constexpr uint32_t idesc_du = idesc_bf16(128, RP, 0, 1);   // dV K-major, b MN-major
+    constexpr uint32_t idesc_db = idesc_bf16(128, RP, 1, 1);   // dV^T MN-major, u MN-major
+    uint64_t a_du[C::kLeaves], b_du[C::kLeaves], a_db[C::kLeaves], b_db[C::kLeaves];
 #pragma unroll
-            for (int j = 0; j < C::kLeaves; ++j) {
-              // dU leaf j: columns 16j..16j+15 -> slab j/2, K-major, 64-byte swizzle (8-row groups 512 B apart)
-              const uint64_t a = smem_desc(st + (j >> 1) * C::kSlabBytes + 32u * (j & 1), 16u, 512u, kLayoutSW64);
-              // b rows 16j..16j+15 of [128 n][16 r]: MN-major, 32-byte swizzle (8-row groups 256 B apart)
-              const uint64_t b = smem_desc(st + C::kTileBytes + j * 512u, 256u, 256u, kLayoutSW32);
-              mma_bf16(d + j * RP, a, b, idesc_du, 0u);
-            }
+    for (int j = 0; j < C::kLeaves; ++j) {
+      // dU leaf j: columns 16j..16j+15 -> slab j/2, K-major, 64-byte swizzle (8-row groups 512 B apart)
+      a_du[j] = smem_desc(base + (j >> 1) * C::kSlabBytes + 32u * (j & 1), 16u, 512u, kLayoutSW64);
+      // b rows 16j..16j+15 of [128 n][16 r]: MN-major, 32-byte swizzle (8-row groups 256 B apart)
+      b_du[j] = smem_desc(base + C::kTileBytes + j * 512u, 256u, 256u, kLayoutSW32);
+      // dB leaf j: rows 16j..16j+15 of the tile seen MN-major: 32-column atoms 8 KB apart (one per
+      // slab), rows of 64 bytes, 8-row groups 512 B apart; K step = 16 rows = 1 KB
+      a_db[j] = smem_desc(base + j * 1024u, uint32_t(C::kSlabBytes), 512u, kLayoutSW64);
+      b_db[j] = smem_desc(base + C::kTileBytes + C::kWBytes + j * 512u, 256u, 256u, kLayoutSW32);
+    }
+    Ring r, g;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int sl = u % n_sl, ch = u / n_sl;
+      const int nstages = n_tiles(sl) * r_tiles(ch);
+      for (int k = 0; k < nstages; ++k) {
+        bool ok = wait(ready(r.idx), r.phase, ab, 33);
+        ok = __all_sync(0xffffffffu, ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 34));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t off = r.idx * C::kStageBytes;
+          const uint32_t d = tmem + g.idx * C::kGroupCols;
 #pragma unroll
-            for (int j = 0; j < C::kLeaves; ++j) {
-              // dB leaf j: rows 16j..16j+15 of the tile seen MN-major: 32-column atoms 8 KB apart (one per
-              // slab), rows of 64 bytes, 8-row groups 512 B apart; K step = 16 rows = 1 KB
-              const uint64_t a = smem_desc(st + j * 1024u, uint32_t(C::kSlabBytes), 512u, kLayoutSW64);
-              const uint64_t b = smem_desc(st + C::kTileBytes + C::kWBytes + j * 512u, 256u, 256u, kLayoutSW32);
-              mma_bf16(d + C::kLeaves * RP + j * RP, a, b, idesc_db, 0u);
-            }
+          for (int j = 0; j < C::kLeaves; ++j)
+            if (elect_one()) mma_bf16(d + j * RP, desc_advance(a_du[j], off), desc_advance(b_du[j], off), idesc_du, 0u);
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)
+            if (elect_one())
+              mma_bf16(d + C::kLeaves * RP + j * RP, desc_advance(a_db[j], off), desc_advance(b_db[j], off), idesc_db, 0u);
+          if (elect_one()) {
             mma_commit(empty(r.idx));
             mma_commit(tfull(g.idx));
           }
-          r.next<C::kStages>();
-          g.next<C::kGroups>();
+          __syncwarp();
         }
+        r.next<C::kStages>();
+        g.next<C::kGroups>();
       }
-      mma_commit(drain);
-      wait_drain(drain, 0u, ab, 35);
     }
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    wait_drain(drain, 0u, ab, 35);
   } else if (warp < 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   } else {
     // ---------------------------------------------------- dV = bf16(dY*alpha)
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
+    const uint32_t a2 = pow2_bf16x2(alpha);
     Ring r;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const int sl = u % n_sl, ch = u / n_sl;
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
         if (wait(full(r.idx), r.phase, ab, 37)) {
           uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kStageBytes);
 #pragma unroll
-          for (int e = 0; e < C::kTileBytes / 16 / 128; ++e) tile[t + 128 * e] = scale_bf16x8(tile[t + 128 * e], alpha);
+          for (int e = 0; e < C::kTileBytes / 16 / 128; ++e) tile[t + 128 * e] = dv_bf16x8(tile[t + 128 * e], alpha, a2);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(ready(r.idx));

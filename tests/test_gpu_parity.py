@@ -75,6 +75,41 @@ def test_adversarial_same_sign_inputs(oracle):
     print("worst |err|/S:", worst)
 
 
+@pytest.mark.parametrize("alpha", [2.0, 0.5, 4096.0, 3.0, -2.0])
+def test_dv_rounding_of_every_finite_bf16(oracle, alpha):
+    """dV = bf16(dY * alpha) for every finite BF16 value of dY (signed zeros,
+    subnormals, values that overflow to infinity). B selects column 16 r of
+    each 16-column block for output column r and dY is zero elsewhere, so
+    dU[m][r] = dV[m][16 r] exactly: dU shows dV bit for bit. Powers of two take
+    the kernels' packed BF16 multiply, 3 and -2 the FP32 form."""
+    R = 16
+    pats = np.arange(65536, dtype=np.uint32)
+    pats = pats[(pats & 0x7F80) != 0x7F80].astype(np.uint16)          # finite patterns only
+    M = -(-pats.size // R)
+    N, K = 16 * R, 64
+    dy = np.zeros((M, N), np.uint16)
+    flat = np.zeros(M * R, np.uint16)
+    flat[: pats.size] = pats
+    dy[:, 0::16] = flat.reshape(M, R)
+    b = np.zeros((N, R), np.uint16)
+    b[16 * np.arange(R), np.arange(R)] = 0x3F80                      # 1.0
+    w = S.Workload("dv", S.Shape(M, K, N, R, alpha), {"x": 1.0, "a": 0.125, "b": 1.0, "dy": 1.0})
+    d = w.generate(0)
+    d.update(dy=dy, b=b)
+    out = G.run(d, alpha)
+    ref = oracle.du(oracle.dv(dy, alpha), b)
+    got = out["du"]
+    finite = (ref & 0x7F80) != 0x7F80
+    zero = ((ref & 0x7FFF) == 0) & ((got & 0x7FFF) == 0)            # +0 and -0 equal (sum of a -0 and +0s)
+    assert np.array_equal(got[finite & ~zero], ref[finite & ~zero])
+    nan = finite == False  # noqa: E712
+    ref_nan = nan & ((ref & 0x7F) != 0)
+    assert np.array_equal(got[nan] & 0x7F80, ref[nan] & 0x7F80)   # non-finite where the oracle is
+    assert np.array_equal((got[ref_nan] & 0x7F) != 0, np.ones(int(ref_nan.sum()), bool))
+    inf = nan & ~ref_nan
+    assert np.array_equal(got[inf], ref[inf])                       # same infinities, same signs
+
+
 def test_reruns_are_bitwise_identical():
     w = S.sweep(2048, 1024)
     d = w.generate(1)
