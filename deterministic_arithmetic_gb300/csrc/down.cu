@@ -48,6 +48,7 @@ struct DownCfg {
   static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
   static_assert((1 << kLevels) == kGS, "slice must hold a power-of-two number of tiles");
   static_assert(kGroups >= 2, "TMEM ring too shallow");
+  static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
 
 template <int RP, bool DV>
@@ -130,43 +131,49 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, RP, 0, DV ? 1 : 0);
-      constexpr uint32_t w_layout = layout_for_span(C::kWSpan);
-      Ring r, g;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int sl = u / n_mt;
-        const int k0 = sl * C::kSlice;
-        const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
-        for (int kb = 0; kb < nkb; ++kb) {
-          bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 3);
-          ok = ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 4);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t st = base + r.idx * C::kStageBytes;
-            const uint32_t d = tmem + g.idx * C::kGroupCols;
+    // The whole warp follows the schedule, one elected lane issues; operand
+    // descriptors are built once for stage 0 and advanced by the stage offset.
+    constexpr uint32_t idesc = idesc_bf16(128, RP, 0, DV ? 1 : 0);
+    constexpr uint32_t w_layout = layout_for_span(C::kWSpan);
+    uint64_t adesc[C::kLeaves], wdesc[C::kLeaves];
 #pragma unroll
-            for (int j = 0; j < C::kLeaves; ++j) {
-              // input slab j/2: K-major, rows of 64 bytes, 64-byte swizzle, 8-row groups 512 bytes
-              // apart; K step j = +32 bytes inside the slab's swizzle atom
-              const uint64_t adesc = smem_desc(st + (j >> 1) * C::kSlabBytes + 32u * (j & 1), 16u, 512u, kLayoutSW64);
-              uint64_t wdesc;
-              if (DV)   // b tile [64 n][RP]: MN-major (r contiguous), 8-row groups of one swizzle span
-                wdesc = smem_desc(st + C::kInBytes + j * 16u * C::kWSpan, 8u * C::kWSpan, 8u * C::kWSpan, w_layout);
-              else      // a tile [RP][64 k]: K-major, 128-byte swizzle
-                wdesc = smem_desc(st + C::kInBytes + 32u * j, 16u, 1024u, kLayoutSW128);
-              mma_bf16(d + j * RP, adesc, wdesc, idesc, 0u);   // fresh accumulator: one leaf
-            }
+    for (int j = 0; j < C::kLeaves; ++j) {
+      // input slab j/2: K-major, rows of 64 bytes, 64-byte swizzle, 8-row groups 512 bytes
+      // apart; K step j = +32 bytes inside the slab's swizzle atom
+      adesc[j] = smem_desc(base + (j >> 1) * C::kSlabBytes + 32u * (j & 1), 16u, 512u, kLayoutSW64);
+      if (DV)   // b tile [64 n][RP]: MN-major (r contiguous), 8-row groups of one swizzle span
+        wdesc[j] = smem_desc(base + C::kInBytes + j * 16u * C::kWSpan, 8u * C::kWSpan, 8u * C::kWSpan, w_layout);
+      else      // a tile [RP][64 k]: K-major, 128-byte swizzle
+        wdesc[j] = smem_desc(base + C::kInBytes + 32u * j, 16u, 1024u, kLayoutSW128);
+    }
+    Ring r, g;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int sl = u / n_mt;
+      const int k0 = sl * C::kSlice;
+      const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 3);
+        ok = __all_sync(0xffffffffu, ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 4));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t off = r.idx * C::kStageBytes;
+          const uint32_t d = tmem + g.idx * C::kGroupCols;
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)   // fresh accumulator: one leaf
+            if (elect_one()) mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(wdesc[j], off), idesc, 0u);
+          if (elect_one()) {
             mma_commit(empty(r.idx));
             mma_commit(tfull(g.idx));
           }
-          r.next<C::kStages>();
-          g.next<C::kGroups>();
+          __syncwarp();
         }
+        r.next<C::kStages>();
+        g.next<C::kGroups>();
       }
-      mma_commit(drain);                 // all MMAs issued above have completed ...
-      wait_drain(drain, 0u, ab, 5);      // ... before TMEM is released
     }
+    if (elect_one()) mma_commit(drain);   // all MMAs issued above have completed ...
+    __syncwarp();
+    wait_drain(drain, 0u, ab, 5);          // ... before TMEM is released
   } else if (warp < 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                            // TMEM lane quarter this warp may access

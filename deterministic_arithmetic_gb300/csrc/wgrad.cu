@@ -42,6 +42,7 @@ struct WgCfg {
   static constexpr int kNumBars = 3 * kStages + 2 * kGroups + 1;
   static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
   static_assert((1 << kLevels) == kGS, "chunk must hold a power-of-two number of stages");
+  static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
 
 template <int RP, bool DV>
@@ -122,40 +123,46 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, RP, 1, 1);
-      constexpr uint32_t g_layout = layout_for_span(C::kGSpan);
-      Ring r, g;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int ch = u / n_ct;
-        const int ns = stages_of(ch);
-        for (int kb = 0; kb < ns; ++kb) {
-          bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 23);
-          ok = ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 24);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t st = base + r.idx * C::kStageBytes;
-            const uint32_t d = tmem + g.idx * C::kGroupCols;
+    // The whole warp follows the schedule, one elected lane issues; operand
+    // descriptors are built once for stage 0 and advanced by the stage offset.
+    constexpr uint32_t idesc = idesc_bf16(128, RP, 1, 1);
+    constexpr uint32_t g_layout = layout_for_span(C::kGSpan);
+    uint64_t adesc[C::kLeaves], gdesc[C::kLeaves];
 #pragma unroll
-            for (int j = 0; j < C::kLeaves; ++j) {
-              // wide operand, transposed view: MN-major (columns contiguous), 128-byte swizzle,
-              // 64-column blocks 8 KB apart, 8-row groups 1 KB apart; K step = 16 rows
-              const uint64_t adesc = smem_desc(st + j * 2048u, 8192u, 1024u, kLayoutSW128);
-              // du / u rows [64][RP]: MN-major (r contiguous), one swizzle span per row
-              const uint64_t gdesc =
-                  smem_desc(st + C::kInBytes + j * 16u * C::kGSpan, 8u * C::kGSpan, 8u * C::kGSpan, g_layout);
-              mma_bf16(d + j * RP, adesc, gdesc, idesc, 0u);
-            }
+    for (int j = 0; j < C::kLeaves; ++j) {
+      // wide operand, transposed view: MN-major (columns contiguous), 128-byte swizzle,
+      // 64-column blocks 8 KB apart, 8-row groups 1 KB apart; K step = 16 rows
+      adesc[j] = smem_desc(base + j * 2048u, 8192u, 1024u, kLayoutSW128);
+      // du / u rows [64][RP]: MN-major (r contiguous), one swizzle span per row
+      gdesc[j] = smem_desc(base + C::kInBytes + j * 16u * C::kGSpan, 8u * C::kGSpan, 8u * C::kGSpan, g_layout);
+    }
+    Ring r, g;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int ch = u / n_ct;
+      const int ns = stages_of(ch);
+      for (int kb = 0; kb < ns; ++kb) {
+        bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 23);
+        ok = __all_sync(0xffffffffu, ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 24));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t off = r.idx * C::kStageBytes;
+          const uint32_t d = tmem + g.idx * C::kGroupCols;
+#pragma unroll
+          for (int j = 0; j < C::kLeaves; ++j)
+            if (elect_one()) mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(gdesc[j], off), idesc, 0u);
+          if (elect_one()) {
             mma_commit(empty(r.idx));
             mma_commit(tfull(g.idx));
           }
-          r.next<C::kStages>();
-          g.next<C::kGroups>();
+          __syncwarp();
         }
+        r.next<C::kStages>();
+        g.next<C::kGroups>();
       }
-      mma_commit(drain);
-      wait_drain(drain, 0u, ab, 25);
     }
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    wait_drain(drain, 0u, ab, 25);
   } else if (warp < 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
