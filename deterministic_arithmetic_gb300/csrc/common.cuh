@@ -140,11 +140,14 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
-// 2-D tiled store from shared memory (bulk-group completion).
-__device__ __forceinline__ void tma_store(const CUtensorMap* m, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+// 2-D tiled store from shared memory (bulk-group completion), with an L2
+// policy: the wide FP32 outputs are stored evict-first, so their lines leave
+// L2 (are written back to HBM) while the storing kernel runs instead of being
+// written back during the next kernel's read stream.
+__device__ __forceinline__ void tma_store(const CUtensorMap* m, uint32_t src, int x, int y, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
-               "r"(src), "r"(x), "r"(y)
+               "r"(src), "r"(x), "r"(y), "l"(policy)
                : "memory");
 }
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     const int h = (warp - 2) >> 2;
     const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
     const uint32_t my_stg = stg0 + (warp - 2) * C::kStg * C::kStgBytes;
+    const uint64_t pol_out = policy_evict_first();
     uint8_t* my_stg_ptr = stg_ptr + (warp - 2) * C::kStg * C::kStgBytes;
     int sidx = 0;
     Ring b;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
           for (int box = 0; box < C::kBoxes; ++box) {
             const int ncol = nt * C::kBN + col0 + box * C::kChunk;
             if (ok && row0 < M && ncol < Nout)
-              tma_store(&tm_out, my_stg + ((sidx + box) % C::kStg) * C::kStgBytes, ncol, row0);
+              tma_store(&tm_out, my_stg + ((sidx + box) % C::kStg) * C::kStgBytes, ncol, row0, pol_out);
             tma_store_commit();
           }
         }
