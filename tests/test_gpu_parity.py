@@ -162,6 +162,31 @@ def test_ragged_tails_are_stable_across_reruns():
                 G.assert_bitwise(f"{k} rows 0:{s}", sub[k], full[k][:s])
 
 
+def test_shared_workspace_across_shapes():
+    """One pair of workspaces reused by calls of different batch sizes: every
+    call equals a call with fresh workspaces bit for bit (nothing a call leaves
+    in the scratch is read by the next), and the status block stays zero."""
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    w = S.Workload("shared", S.Shape(2304, 1024, 2048, 16, 2.0), {"x": 1.0, "a": 1024 ** -0.5, "b": 0.25, "dy": 1.0})
+    d = w.generate(6)
+    M0, K, N, R = 2304, 1024, 2048, 16
+    wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M0, K, N, R), "cuda")
+    wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M0, K, N, R), "cuda")
+    A, B = G.dev_bf16(d["a"]), G.dev_bf16(d["b"])
+    for m in (2304, 37, 1000, 2304, 1, 640):
+        X, DY = G.dev_bf16(d["x"][:m]), G.dev_bf16(d["dy"][:m])
+        y, u = ld.lora_delta_fwd(X, A, B, 2.0, workspace=wf)
+        dx, da, db, du = ld.lora_delta_bwd(DY, X, A, B, u, 2.0, workspace=wb)
+        torch.cuda.synchronize()
+        assert not wf[:256].any().item() and not wb[:256].any().item(), m
+        ref = G.run(d, 2.0, rows=slice(0, m))
+        got = dict(u=G.host_bits(u), delta_y=G.host_f32(y), du=G.host_bits(du), dx=G.host_f32(dx),
+                   da=G.host_f32(da), db=G.host_f32(db))
+        for k in got:
+            G.assert_bitwise(f"{k} m={m}", got[k], ref[k])
+
+
 def test_tiny_batch_invariance():
     w = S.tiny()
     d = w.generate(0)
