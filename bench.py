@@ -38,6 +38,7 @@ METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
 KERNELS = ["down U", "up dY_lora", "dy dU+dB", "up dX", "wgrad dA", "combine dA+dB"]
 N_FWD = 2      # forward kernels; the rest are the backward's
 N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
+PROF_EVERY = 48   # one step in this many carries per-kernel events; the rest replay a CUDA graph
 
 
 def algorithmic_bytes(M, K, N, R):
@@ -281,15 +282,35 @@ def run_ours(args, world, rank, local):
         step(i)
     torch.cuda.synchronize()
 
-    # per-kernel events on a sample of the timed steps (a mark before the first kernel and after each)
-    n_prof = min(args.steps, 64)
-    prof_steps = set(np.linspace(0, args.steps - 1, n_prof).astype(int).tolist())
+    # Timed region: blocks of PROF_EVERY steps. The first step of each block runs through the API
+    # with per-kernel CUDA events (a mark before the first kernel and after each); the other
+    # PROF_EVERY - 1 steps replay one CUDA graph of those same API calls (kernel launches only,
+    # programmatic dependent launch kept between them). Steps past the last full block run
+    # through the API without events.
+    n_blocks = args.steps // PROF_EVERY
+    prof_steps = [b * PROF_EVERY for b in range(n_blocks)]
+    tail_prof = [] if n_blocks else list(range(min(args.steps, 8)))   # short runs: events on the first steps
     n_bwd = len(KERNELS) - N_FWD
     fev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(N_FWD + 1)] for i in prof_steps}
-    bev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(n_bwd + 1)] for i in prof_steps}
+    bev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(n_bwd + 1)] for i in prof_steps + tail_prof}
+    fev.update({i: [torch.cuda.Event(enable_timing=True) for _ in range(N_FWD + 1)] for i in tail_prof})
     for evs in list(fev.values()) + list(bev.values()):
         for e in evs:
             e.record(stream)
+    graph = None
+    if n_blocks:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                gst = torch.cuda.current_stream(dev)
+                for j in range(1, PROF_EVERY):
+                    x, dy = Xs[j % N_ROTATE], DYs[j % N_ROTATE]
+                    ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=gst)
+                    ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=gst)
+        stream.wait_stream(cap)
+        graph.replay()          # warm the graph
     torch.cuda.synchronize()
 
     start = torch.cuda.Event(enable_timing=True)
@@ -299,16 +320,24 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else int(
             os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])) as clocks:
         start.record(stream)
-        for i in range(args.steps):
+        for i in prof_steps:
             x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
-            if i in prof_steps:
-                ld.lora_delta_set_profile_events(fev[i])
+            ld.lora_delta_set_profile_events(fev[i])
             ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
-            if i in prof_steps:
-                ld.lora_delta_set_profile_events(bev[i])
+            ld.lora_delta_set_profile_events(bev[i])
             ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
-            if i in prof_steps:
+            ld.lora_delta_set_profile_events(None)
+            graph.replay()      # steps i + 1 .. i + PROF_EVERY - 1 (same rotation phase: PROF_EVERY % 3 == 0)
+        for i in range(n_blocks * PROF_EVERY, args.steps):
+            if i in tail_prof:
+                x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
+                ld.lora_delta_set_profile_events(fev[i])
+                ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
+                ld.lora_delta_set_profile_events(bev[i])
+                ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
                 ld.lora_delta_set_profile_events(None)
+            else:
+                step(i)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -318,7 +347,7 @@ def run_ours(args, world, rank, local):
 
     # per-kernel average durations over the sampled steps
     ktimes = {k: [] for k in KERNELS}
-    for i in prof_steps:
+    for i in prof_steps + tail_prof:
         f, b = fev[i], bev[i]
         for j, name in enumerate(KERNELS[:N_FWD]):
             ktimes[name].append(f[j].elapsed_time(f[j + 1]))
@@ -433,7 +462,10 @@ def run_ours(args, world, rank, local):
                        "M": M, "K": K, "N": N, "R": R, "alpha": alpha, "accumulate": "fp32",
                        "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
                              "output stream per step, all larger than the 129 MB L2",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       "timing": (f"{PROF_EVERY - 1} of every {PROF_EVERY} steps replay a CUDA graph of the API calls; "
+                                  "the other step goes through the API with per-kernel CUDA events"
+                                  if args.steps >= PROF_EVERY else "every step through the API")},
             "steps_per_s": round(1e3 / ms_step, 1),
             "roofline_step": {"bound": "hbm", "achieved": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
                               "peak": peak, "unit": "GB/s", "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
