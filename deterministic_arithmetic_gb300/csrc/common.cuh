@@ -380,4 +380,21 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Canonical pairwise tree over the S slice partials (slice stride `stride`
+// floats) of 8 consecutive FP32 values, rounded to BF16 and packed: the value
+// of U (or dU) from the partial sums over slices of the reduction dimension.
+// All loads of a block of slices are in flight together.
+__device__ __forceinline__ uint4 slices_to_bf16x8(const float* p, size_t stride, int S) {
+  float v[8];
+  if (S <= 4) {
+    float w[1][8];
+    block_slices<4, 1>(p, stride, S, w);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = w[0][c];
+  } else {
+    sum_slices8(p, stride, S, v);
+  }
+  return pack_bf16x8(v);
+}
+
 }  // namespace lora

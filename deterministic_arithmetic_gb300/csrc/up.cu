@@ -10,7 +10,7 @@
 //
 // Work unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16). Each CTA
 // takes a contiguous range of units (row-tile major), so it rebuilds each
-// 128 x RP BF16 operand tile once: four "prep" warps add the slice partials
+// 128 x RP BF16 operand tile once: eight "prep" warps add the slice partials
 // left by the down kernel with the canonical pairwise tree (FP32, round to
 // nearest), round to BF16, write the tile into shared memory with the same
 // swizzle a TMA load would apply, and the unit with column tile 0 also stores
@@ -23,7 +23,9 @@
 // once, in full lines.
 //
 // Warp roles: 0 = TMA producer (B / A weight tile), 1 = MMA issuer (TMEM
-// owner), 2..9 = epilogue, 10..13 = prep (operand tile from the partials).
+// owner), 2..9 = epilogue, 10..17 = prep (operand tile from the partials: one
+// group of 8 values of one row per thread, so each tree's loads are in flight
+// together).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,7 +43,7 @@ struct UpCfg {
   static constexpr int kStages = RP == 16 ? 6 : (RP == 32 ? 5 : 3);   // operand ring (weight tile from L2)
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
-  static constexpr int kEpiWarps = 8, kPrepWarps = 4;
+  static constexpr int kEpiWarps = 8, kPrepWarps = 8;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kPrepWarps);
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
@@ -258,38 +260,27 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     if (lane == 0) tma_store_wait_all<0>();
   } else {
     // ------------------------------------ prep: BF16 operand tile from the partials
-    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);           // 0..127: row within the tile
-    const int sw = ((t * C::kSpan) >> 7) & (C::kSpan / 16 - 1);     // swizzle of this row's 16-byte chunks
+    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);           // 0 .. 32 * kPrepWarps - 1
     int cached_mt = -1;
     Ring r;
     for (int u = u0; u < u1; ++u) {
       const int mt = u / n_nt, nt = u % n_nt;
       if (mt != cached_mt) {
         named_bar(3, 32 * C::kPrepWarps);                           // previous tile fully copied out
-        const int row = mt * C::kBM + t;
-        // chunk c (8 values): into the tile cache at its swizzled place; the unit owning the tile also stores it
-        auto emit = [&](int c, const float (&v)[8], bool valid) {
-          const uint4 packed = valid ? pack_bf16x8(v) : make_uint4(0u, 0u, 0u, 0u);
-          if (valid && nt == 0 && c * 8 < R) *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + c * 8) = packed;
-          *reinterpret_cast<uint4*>(tile_cache + t * C::kSpan + ((c ^ sw) * 16)) = packed;
-        };
-        const float* prow = part + size_t(row) * RP;
+        // item i: 8 values (group g) of tile row `trow`, the canonical tree over the S slice partials;
+        // into the tile cache at its swizzled place, and the unit owning the tile also stores it
         const size_t stride = size_t(M) * RP;
-        if (S <= 4) {
 #pragma unroll 1
-          for (int c = 0; c < RP / 8; c += 2) {                     // two chunks' loads in flight together
-            float v[2][8] = {};
-            if (row < M) block_slices<4, 2>(prow + c * 8, stride, S, v);
-            emit(c, v[0], row < M);
-            emit(c + 1, v[1], row < M);
+        for (int i = t; i < C::kBM * (RP / 8); i += 32 * C::kPrepWarps) {
+          const int trow = i % C::kBM, g = i / C::kBM;
+          const int row = mt * C::kBM + trow;
+          const int sw = ((trow * C::kSpan) >> 7) & (C::kSpan / 16 - 1);   // the TMA swizzle of this row
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (row < M) {
+            v = slices_to_bf16x8(part + size_t(row) * RP + g * 8, stride, S);
+            if (nt == 0 && g * 8 < R) *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) = v;
           }
-        } else {
-#pragma unroll 1
-          for (int c = 0; c < RP / 8; ++c) {
-            float v[8] = {};
-            if (row < M) sum_slices8(prow + c * 8, stride, S, v);
-            emit(c, v, row < M);
-          }
+          *reinterpret_cast<uint4*>(tile_cache + trow * C::kSpan + ((g ^ sw) * 16)) = v;
         }
         named_bar(3, 32 * C::kPrepWarps);                           // tile complete
         cached_mt = mt;
