@@ -89,11 +89,29 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int total = n_ct * n_ch;
+  auto stages_of = [&](int ch) { return (min(M - ch * kWgradChunk, kWgradChunk) + C::kBR - 1) / C::kBR; };
+  // The wide operand (X or dY) is an input of the call, which no earlier kernel of the call
+  // writes: the first ring stages' copies of it are issued before waiting for the predecessor,
+  // so the stream starts while the predecessor's last CTAs finish. (The du / u rows, which the
+  // predecessor may have written, are copied only after the wait.)
+  int pre = 0;                 // stages whose wide-operand copies are in flight
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol_stream = policy_evict_first();
+    for (int u = blockIdx.x; u < total && pre < C::kStages; u += gridDim.x) {
+      const int ct = u % n_ct, ch = u / n_ct;
+      for (int kb = 0; kb < stages_of(ch) && pre < C::kStages; ++kb, ++pre) {
+        const uint32_t st = base + pre * C::kStageBytes;
+        const int m = ch * kWgradChunk + kb * C::kBR;
+        mbar_expect_tx(full(pre), C::kStageBytes);
+        tma_load(st, &tm_in, full(pre), ct * C::kBC, m, pol_stream);
+        tma_load(st + C::kInBytes / 2, &tm_in, full(pre), ct * C::kBC + 64, m, pol_stream);
+      }
+    }
+  }
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
   const Abort ab{abort_flag, status};
-  const int total = n_ct * n_ch;
-  auto stages_of = [&](int ch) { return (min(M - ch * kWgradChunk, kWgradChunk) + C::kBR - 1) / C::kBR; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -101,11 +119,17 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
       const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
       Ring r;
       uint32_t issued = 0, parities = 0;
+      int k = 0;               // stage count of this CTA
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const int ct = u % n_ct, ch = u / n_ct;
         const int ns = stages_of(ch);
-        for (int kb = 0; kb < ns; ++kb) {
-          if (wait(empty(r.idx), r.phase ^ 1u, ab, 21)) {
+        for (int kb = 0; kb < ns; ++kb, ++k) {
+          if (k < pre) {         // first pass over the ring: wide operand already in flight
+            const uint32_t st = base + r.idx * C::kStageBytes;
+            tma_load(st + C::kInBytes, &tm_g, full(r.idx), 0, ch * kWgradChunk + kb * C::kBR, pol_keep);
+            issued |= 1u << r.idx;
+            parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
+          } else if (wait(empty(r.idx), r.phase ^ 1u, ab, 21)) {
             const uint32_t st = base + r.idx * C::kStageBytes;
             const int m = ch * kWgradChunk + kb * C::kBR;
             mbar_expect_tx(full(r.idx), C::kStageBytes);
