@@ -183,8 +183,9 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
 
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
-  CUtensorMap m_x, m_a, m_b, m_y;
+  CUtensorMap m_x, m_a, m_b, m_y, m_u;
   if (!make_map(&m_x, x, false, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&m_u, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_b, b, false, N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
       !make_map(&m_y, delta_y, true, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -201,7 +202,7 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
     return LORA_ERR_CUDA;
   rec.mark();
   // U = bf16(tree over the K-slice partials), built inside the up-projection, which also writes u
-  if (launch_up(RP, false, m_b, m_y, upart, int(ceil_div(K, down_slice(RP))), u, int(R), int(M), int(N), alpha, status,
+  if (launch_up(RP, false, m_u, m_b, m_y, upart, int(ceil_div(K, down_slice(RP))), u, int(R), int(M), int(N), alpha, status,
                 grid_for(up_units(M, N, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
@@ -225,7 +226,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
 
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
-  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_a, m_dx, m_x_chunk, m_du_chunk, m_b_128, m_u_128;
+  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_a, m_dx, m_x_chunk, m_du_chunk, m_b_128, m_u_128, m_du_128;
   if (!make_map(&m_dy_rows, dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&m_b_rows, b, false, N, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_dy_chunk, dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -235,7 +236,8 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
       !make_map(&m_x_chunk, x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_du_chunk, du, false, M, R, RP, 64, swizzle_for_span(span)) ||
       !make_map(&m_b_128, b, false, N, R, RP, 128, swizzle_for_span(span)) ||
-      !make_map(&m_u_128, u, false, M, R, RP, 128, swizzle_for_span(span)))
+      !make_map(&m_u_128, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
+      !make_map(&m_du_128, du, false, M, R, RP, 128, swizzle_for_span(span)))
     return LORA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -267,7 +269,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
     rec.mark();
   }
   // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
-  if (launch_up(RP, true, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
+  if (launch_up(RP, true, m_du_128, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
                 grid_for(up_units(M, K, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();

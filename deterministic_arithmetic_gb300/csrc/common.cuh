@@ -84,6 +84,41 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Abo
   }
 }
 
+// ------------------------------------------------------ grid-wide barrier
+// For kernels launched cooperatively (every CTA resident at once). All
+// threads of every CTA call it; on return, every global store made by any CTA
+// before its call is visible to every thread after the call. cnt: two words,
+// zero when the launch starts (arrivals, departures); the last CTA to leave
+// puts both back to zero, so the next launch finds them at zero. The wait for
+// the last arrival gives up after kWaitLimitNs (then the CTA aborts).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+static __device__ __noinline__ void grid_sync(uint32_t* cnt, uint32_t ncta, volatile uint32_t* abort_flag,
+                                              uint32_t* status, uint32_t site) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();                                   // this CTA's stores, device-visible before arriving
+    atomicAdd(&cnt[0], 1u);
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1; ld_acquire_gpu(&cnt[0]) < ncta; ++it) {
+      if ((it & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        if (status) *reinterpret_cast<volatile uint32_t*>(status) = (site << 8) | kDevTimeout;
+        break;
+      }
+      __nanosleep(100);
+    }
+    if (atomicAdd(&cnt[1], 1u) == ncta - 1u) {          // every CTA has left the wait: reset for the next launch
+      atomicExch(&cnt[0], 0u);
+      atomicExch(&cnt[1], 0u);
+    }
+  }
+  __syncthreads();
+}
+
 // Wait for the phase of `bar` with the given parity to complete, for at most
 // kWaitLimitNs. False means "abort": skip the work, keep the control flow.
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
@@ -163,6 +198,11 @@ __device__ __forceinline__ void tma_store_wait_all() {
 // async-proxy (TMA / tensor core) reads of the same bytes.
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Order generic-proxy global accesses (seen through an acquire) before later
+// async-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -47,6 +47,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The same with a cooperative launch as well (every CTA resident at once): for
+// kernels with a grid-wide barrier. grid must not exceed the SM count (these
+// kernels run one CTA per SM).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Work-unit counts (all launches use persistent CTAs over units).
 inline int64_t down_units(int64_t M, int64_t Kred, int RP) { return ceil_div(M, 128) * ceil_div(Kred, down_slice(RP)); }
 inline int64_t up_units(int64_t M, int64_t Nout, int RP) { return ceil_div(M, 128) * ceil_div(Nout, up_bn(RP)); }
@@ -56,9 +77,10 @@ inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil
 // word; `grid` the number of persistent CTAs.
 cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
                         float alpha, uint32_t* status, int grid, cudaStream_t st);
-cudaError_t launch_up(int RP, bool dx, const CUtensorMap& b, const CUtensorMap& out, const float* part, int S,
-                      void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
-                      cudaStream_t st);
+// up: a = u / du rows (box 128 x RP), written by the kernel itself in its first phase.
+cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                      const float* part, int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status,
+                      int grid, cudaStream_t st);
 cudaError_t launch_dy(const CUtensorMap& dy, const CUtensorMap& b, const CUtensorMap& u, float* du_part,
                       float* db_part, int M, int N, float alpha, uint32_t* status, int grid, cudaStream_t st);
 cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int C,

@@ -8,24 +8,25 @@
 // batch-invariant", section "Summary"; the alpha scale is fused into the
 // epilogue, as that page's "Benchmark" section proposes.)
 //
-// Work unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16). Each CTA
-// takes a contiguous range of units (row-tile major), so it rebuilds each
-// 128 x RP BF16 operand tile once: eight "prep" warps add the slice partials
-// left by the down kernel with the canonical pairwise tree (FP32, round to
-// nearest), round to BF16, write the tile into shared memory with the same
-// swizzle a TMA load would apply, and the unit with column tile 0 also stores
-// it to u / du in global memory. The unit is one tcgen05 MMA per 16-wide
-// slice of R (M=128, N=BN, K=16), each into its own TMEM accumulator, summed
-// by the canonical tree. Eight epilogue warps read TMEM, finish the tree (and
-// the alpha multiply); each warp stages its own 32 x 32 FP32 boxes in
-// 128-byte-swizzled shared memory (a ring of four, no barrier across warps)
-// and writes them with TMA stores, so every output byte is written exactly
-// once, in full lines.
+// Two phases in one cooperative launch. First every CTA adds the slice
+// partials (left by the down kernel) of its share of the batch rows with the
+// canonical pairwise tree (FP32, round to nearest), rounds to BF16 and writes
+// those rows of u / du; a grid-wide barrier follows. Then the expansion: work
+// unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16), units dealt out
+// round-robin, so that at any time the CTAs write one compact band of the
+// output (consecutive units are neighbours in memory), which the memory
+// system absorbs markedly faster than each CTA writing its own distant region.
+// The producer brings each unit's 128 rows of u / du and its weight tile with
+// TMA. The unit is one tcgen05 MMA per 16-wide slice of R (M=128, N=BN,
+// K=16), each into its own TMEM accumulator, summed by the canonical tree.
+// Eight epilogue warps read TMEM, finish the tree (and the alpha multiply);
+// each warp stages its own 32 x 32 FP32 boxes in 128-byte-swizzled shared
+// memory (a ring of four, no barrier across warps) and writes them with TMA
+// stores (L2 evict-first), so every output byte is written exactly once, in
+// full lines.
 //
-// Warp roles: 0 = TMA producer (B / A weight tile), 1 = MMA issuer (TMEM
-// owner), 2..9 = epilogue, 10..17 = prep (operand tile from the partials: one
-// group of 8 values of one row per thread, so each tree's loads are in flight
-// together).
+// Warp roles in the expansion: 0 = TMA producer (u / du rows, B / A weight
+// tile), 1 = MMA issuer (TMEM owner), 2..9 = epilogue.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -43,8 +44,8 @@ struct UpCfg {
   static constexpr int kStages = RP == 16 ? 6 : (RP == 32 ? 5 : 3);   // operand ring (weight tile from L2)
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
-  static constexpr int kEpiWarps = 8, kPrepWarps = 8;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps + kPrepWarps);
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
@@ -54,19 +55,20 @@ struct UpCfg {
   static constexpr int kStg = 4;                       // staging buffers per epilogue warp
   static constexpr int kStgBytes = 32 * kChunk * 4;    // one 32-row x 32-column FP32 box: 4 KB
   static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
-  static constexpr size_t kCacheOff = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;   // operand tile cache
-  static constexpr size_t kBarOff = kCacheOff + kABytes;
+  static constexpr size_t kBarOff = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1;
   static constexpr size_t kSmem = kBarOff + 1024 + kNumBars * 8 + 16;
-  static_assert(kStageBytes % 1024 == 0 && kCacheOff % 1024 == 0, "tiles must stay 1024-byte aligned");
+  static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
+  static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
   static_assert(kBufs == 2, "double-buffered accumulators");
 };
 
 template <int RP, bool DX>
 __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
-    up_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
-              const float* __restrict__ part, int S, __nv_bfloat16* __restrict__ out_bf16, int R, int M, int Nout,
-              int n_mt, int n_nt, float alpha, uint32_t* status) {
+    up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ part, int S,
+              __nv_bfloat16* __restrict__ out_bf16, int R, int M, int Nout, int n_mt, int n_nt, float alpha,
+              uint32_t* status, uint32_t* sync) {
   using C = UpCfg<RP, DX>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -74,7 +76,6 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t stg0 = base + uint32_t(C::kStgOff);               // staging buffers [epilogue warp][kStg]
   uint8_t* stg_ptr = gbase + C::kStgOff;
-  uint8_t* tile_cache = gbase + C::kCacheOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full(s), 1 + C::kPrepWarps);   // producer (with the weight tile's bytes) + one per prep warp
+      mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < C::kBufs; ++b) {
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0u;
     mbar_fence_init();
+    prefetch_map(&tm_a);
     prefetch_map(&tm_b);
     prefetch_map(&tm_out);
   }
@@ -113,20 +115,32 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   grid_dependents_launch();
   const Abort ab{abort_flag, status};
   const int total = n_mt * n_nt;
-  const int u0 = int(int64_t(total) * blockIdx.x / gridDim.x);
-  const int u1 = int(int64_t(total) * (blockIdx.x + 1) / gridDim.x);
+
+  // ---- phase 1: this CTA's rows of u / du = bf16(tree over the S slice partials)
+  {
+    const int r0 = int(int64_t(M) * blockIdx.x / gridDim.x), r1 = int(int64_t(M) * (blockIdx.x + 1) / gridDim.x);
+    const size_t stride = size_t(M) * RP;
+    for (int i = threadIdx.x; i < (r1 - r0) * (R / 8); i += C::kThreads) {
+      const int row = r0 + i / (R / 8), g = i % (R / 8);
+      *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) =
+          slices_to_bf16x8(part + size_t(row) * RP + g * 8, stride, S);
+    }
+  }
+  grid_sync(sync, gridDim.x, abort_flag, status, 10);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
+      fence_proxy_async_global();          // u / du rows written by the CTAs before the barrier, read by TMA
       Ring r;
       uint32_t issued = 0, parities = 0;
-      for (int u = u0; u < u1; ++u) {
-        const int nt = u % n_nt;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const int mt = u / n_nt, nt = u % n_nt;
         if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
           const uint32_t st = base + r.idx * C::kStageBytes;
-          mbar_expect_tx(full(r.idx), C::kBBytes);
+          mbar_expect_tx(full(r.idx), C::kStageBytes);
+          tma_load(st, &tm_a, full(r.idx), 0, mt * C::kBM, pol);                   // u / du rows of the tile
           if (DX) {
 #pragma unroll
             for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(128, C::kBN, 0, DX ? 1 : 0);
       constexpr uint32_t lay = layout_for_span(C::kSpan);
       Ring r, b;
-      for (int u = u0; u < u1; ++u) {
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
         bool ok = wait(full(r.idx), r.phase, ab, 13);
         ok = ok && wait(tempty(b.idx), b.phase ^ 1u, ab, 14);
         if (ok) {
@@ -184,7 +198,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     uint8_t* my_stg_ptr = stg_ptr + (warp - 2) * C::kStg * C::kStgBytes;
     int sidx = 0;
     Ring b;
-    for (int u = u0; u < u1; ++u) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const int mt = u / n_nt, nt = u % n_nt;
       const bool ok = __all_sync(0xffffffffu, wait(tfull(b.idx), b.phase, ab, 15));
       tc_fence_after();
@@ -258,45 +272,6 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       b.next<C::kBufs>();
     }
     if (lane == 0) tma_store_wait_all<0>();
-  } else {
-    // ------------------------------------ prep: BF16 operand tile from the partials
-    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);           // 0 .. 32 * kPrepWarps - 1
-    int cached_mt = -1;
-    Ring r;
-    for (int u = u0; u < u1; ++u) {
-      const int mt = u / n_nt, nt = u % n_nt;
-      if (mt != cached_mt) {
-        named_bar(3, 32 * C::kPrepWarps);                           // previous tile fully copied out
-        // item i: 8 values (group g) of tile row `trow`, the canonical tree over the S slice partials;
-        // into the tile cache at its swizzled place, and the unit owning the tile also stores it
-        const size_t stride = size_t(M) * RP;
-#pragma unroll 1
-        for (int i = t; i < C::kBM * (RP / 8); i += 32 * C::kPrepWarps) {
-          const int trow = i % C::kBM, g = i / C::kBM;
-          const int row = mt * C::kBM + trow;
-          const int sw = ((trow * C::kSpan) >> 7) & (C::kSpan / 16 - 1);   // the TMA swizzle of this row
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (row < M) {
-            v = slices_to_bf16x8(part + size_t(row) * RP + g * 8, stride, S);
-            if (nt == 0 && g * 8 < R) *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) = v;
-          }
-          *reinterpret_cast<uint4*>(tile_cache + trow * C::kSpan + ((g ^ sw) * 16)) = v;
-        }
-        named_bar(3, 32 * C::kPrepWarps);                           // tile complete
-        cached_mt = mt;
-      }
-      const bool ok = __all_sync(0xffffffffu, wait(empty(r.idx), r.phase ^ 1u, ab, 18));
-      if (ok) {
-        const uint4* src = reinterpret_cast<const uint4*>(tile_cache);
-        uint4* dst = reinterpret_cast<uint4*>(gbase + r.idx * C::kStageBytes);
-#pragma unroll
-        for (int e = t; e < C::kABytes / 16; e += 32 * C::kPrepWarps) dst[e] = src[e];
-        fence_proxy_async();
-      }
-      __syncwarp();
-      if (ok && lane == 0) mbar_arrive(full(r.idx));
-      r.next<C::kStages>();
-    }
   }
 
   tc_fence_before();
@@ -308,25 +283,25 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
 }
 
 template <int RP, bool DX>
-static cudaError_t launch_one(const CUtensorMap& b, const CUtensorMap& out, const float* part, int S, void* out_bf16,
-                              int R, int M, int Nout, float alpha, uint32_t* status, int grid, cudaStream_t st) {
+static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const float* part,
+                              int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
+                              cudaStream_t st) {
   using C = UpCfg<RP, DX>;
   const int n_mt = int(ceil_div(M, C::kBM)), n_nt = int(ceil_div(Nout, C::kBN));
-  return launch_pdl(up_kernel<RP, DX>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
-                    b, out, part, S, static_cast<__nv_bfloat16*>(out_bf16), R, M,
-                                                          Nout, n_mt, n_nt, alpha, status);
+  return launch_pdl_coop(up_kernel<RP, DX>, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, out, part, S,
+                         static_cast<__nv_bfloat16*>(out_bf16), R, M, Nout, n_mt, n_nt, alpha, status, status + 1);
 }
 
-cudaError_t launch_up(int RP, bool dx, const CUtensorMap& b, const CUtensorMap& out, const float* part, int S,
-                      void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
-                      cudaStream_t st) {
+cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                      const float* part, int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status,
+                      int grid, cudaStream_t st) {
   switch (RP * 2 + (dx ? 1 : 0)) {
-    case 32: return launch_one<16, false>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 33: return launch_one<16, true>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 64: return launch_one<32, false>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 65: return launch_one<32, true>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 128: return launch_one<64, false>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 129: return launch_one<64, true>(b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 32: return launch_one<16, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 33: return launch_one<16, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 64: return launch_one<32, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 65: return launch_one<32, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 128: return launch_one<64, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 129: return launch_one<64, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
