@@ -110,6 +110,20 @@ def test_dv_rounding_of_every_finite_bf16(oracle, alpha):
     assert np.array_equal(got[inf], ref[inf])                       # same infinities, same signs
 
 
+def test_power_of_two_alpha_with_out_of_range_weights(oracle):
+    """alpha = 2^12 with a few entries of b at 2^118 (alpha * b would leave the
+    BF16 range): the stages that meet them must take dV = bf16(dY * alpha)
+    itself, not alpha * b; dU, dB, dX and dA against the oracle as usual."""
+    M, K, N, R, alpha = 512, 256, 1024, 16, 4096.0
+    w = S.Workload("pow2big", S.Shape(M, K, N, R, alpha), {"x": 2.0 ** -10, "a": 256 ** -0.5, "b": 0.25, "dy": 2.0 ** -16})
+    d = w.generate(9)
+    b = d["b"].copy()
+    b[[3, 200, 515, 1000], [0, 7, 15, 4]] = 0x7AC0                    # 2^118 * 1.5
+    d["b"] = b
+    out = G.run(d, alpha)
+    G.check_parity(oracle, d, alpha, out)
+
+
 def test_reruns_are_bitwise_identical():
     w = S.sweep(2048, 1024)
     d = w.generate(1)
