@@ -72,12 +72,12 @@ def measured_peaks():
 # dram__bytes_write.sum), keyed by kernel, with the hash of the kernel source
 # the counters were taken on; a kernel changed since then reports null.
 NCU_TRAFFIC = {   # ncu, training step, warm caches (--cache-control none), per launch
-    "down U": {"bytes": 73700000, "src_hash": "55f23a44b08732cf"},
-    "up dY_lora": {"bytes": 123800000, "src_hash": "e89ff81c4b3c9243"},
-    "dy dU+dB": {"bytes": 84400000, "src_hash": "697dd60deb2121b9"},
-    "up dX": {"bytes": 128900000, "src_hash": "e89ff81c4b3c9243"},
-    "wgrad dA": {"bytes": 79600000, "src_hash": "e1177d12debbcb97"},
-    "combine dA+dB": {"bytes": 10800000, "src_hash": "337f1bac5b0e1c32"},
+    "down U": {"bytes": 70000000, "src_hash": "2b18d4f8984aa78d"},
+    "up dY_lora": {"bytes": 123800000, "src_hash": "edafa9efa343b533"},
+    "dy dU+dB": {"bytes": 78500000, "src_hash": "02527fdf6c200244"},
+    "up dX": {"bytes": 126000000, "src_hash": "edafa9efa343b533"},
+    "wgrad dA": {"bytes": 75400000, "src_hash": "e3813b8b0870e8f6"},
+    "combine dA+dB": {"bytes": 1500000, "src_hash": "337f1bac5b0e1c32"},
 }
 
 

@@ -39,7 +39,10 @@
  *     256 bytes are a device status block: they must be zero before the first
  *     call that uses the workspace (for example, allocate it zeroed); a kernel
  *     that gives up on an internal wait writes a non-zero code there and
- *     returns (read it with lora_delta_device_status). A workspace must not be
+ *     returns (read it with lora_delta_device_status). The block also holds
+ *     the counters of a grid-wide barrier, which every call that completes
+ *     without such a code leaves at zero; after a non-zero code, zero the
+ *     block again before reusing the workspace. A workspace must not be
  *     shared by calls that may run concurrently.
  */
 #ifndef LORA_DELTA_H
