@@ -96,27 +96,29 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-static __device__ __noinline__ void grid_sync(uint32_t* cnt, uint32_t ncta, volatile uint32_t* abort_flag,
-                                              uint32_t* status, uint32_t site) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();                                   // this CTA's stores, device-visible before arriving
-    atomicAdd(&cnt[0], 1u);
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1; ld_acquire_gpu(&cnt[0]) < ncta; ++it) {
-      if ((it & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        if (status) *reinterpret_cast<volatile uint32_t*>(status) = (site << 8) | kDevTimeout;
-        break;
-      }
-      __nanosleep(100);
+// Grid-wide barrier for one thread per CTA (cooperative launches only: every
+// CTA is resident). cnt[0] counts arrivals; the wait gives up after
+// kWaitLimitNs (abort flag and status set). grid_leave then counts departures
+// in cnt[1]; the last CTA to leave zeroes both, ready for the next launch.
+static __device__ __noinline__ void grid_arrive_wait(uint32_t* cnt, uint32_t ncta, volatile uint32_t* abort_flag,
+                                                     uint32_t* status, uint32_t site) {
+  __threadfence();                                     // this CTA's stores, device-visible before arriving
+  atomicAdd(&cnt[0], 1u);
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1; ld_acquire_gpu(&cnt[0]) < ncta; ++it) {
+    if ((it & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      if (status) *reinterpret_cast<volatile uint32_t*>(status) = (site << 8) | kDevTimeout;
+      break;
     }
-    if (atomicAdd(&cnt[1], 1u) == ncta - 1u) {          // every CTA has left the wait: reset for the next launch
-      atomicExch(&cnt[0], 0u);
-      atomicExch(&cnt[1], 0u);
-    }
+    __nanosleep(64);
   }
-  __syncthreads();
+}
+static __device__ __forceinline__ void grid_leave(uint32_t* cnt, uint32_t ncta) {
+  if (atomicAdd(&cnt[1], 1u) == ncta - 1u) {            // every CTA has left the wait
+    atomicExch(&cnt[0], 0u);
+    atomicExch(&cnt[1], 0u);
+  }
 }
 
 // Wait for the phase of `bar` with the given parity to complete, for at most
@@ -164,6 +166,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+// Prefetch one tile of a tensor into L2 (no shared memory, no completion
+// tracking). Issued before the grid dependency wait it warms L2 for the first
+// loads after it while the predecessor drains; L2 is the point of coherence for
+// those loads, so a line the predecessor writes meanwhile is read as written.
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 // 2-D tiled load into shared memory; completes `bar`'s transaction count.
 // x (innermost coordinate) must be a multiple of 16 bytes / element size.

@@ -44,6 +44,7 @@ struct DownCfg {
   static constexpr int kCPT = RP / 2;                 // columns per epilogue thread
   static constexpr int kCH = kCPT < 16 ? kCPT : 16;   // columns per TMEM load batch
   static constexpr int kWSpan = DV ? RP * 2 : 128;    // swizzle span of the weight tile
+  static constexpr int kPrefetch = 8;                 // input tiles warmed in L2 before the dependency wait
   static constexpr int kNumBars = 3 * kStages + 2 * kGroups + 1;
   static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
   static_assert((1 << kLevels) == kGS, "slice must hold a power-of-two number of tiles");
@@ -95,6 +96,15 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0 && int(blockIdx.x) < n_mt * n_sl) {
+    // the first input tiles of this CTA's first unit, into L2 while the predecessor drains
+    const int mt = int(blockIdx.x) % n_mt, k0 = (int(blockIdx.x) / n_mt) * C::kSlice;
+    const int nkb = min((min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK, C::kPrefetch);
+    for (int kb = 0; kb < nkb; ++kb) {
+      tma_prefetch_l2(&tm_in, k0 + kb * C::kBK, mt * C::kBM);
+      tma_prefetch_l2(&tm_in, k0 + kb * C::kBK + 32, mt * C::kBM);
+    }
+  }
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
   const Abort ab{abort_flag, status};

@@ -42,6 +42,7 @@ struct DyCfg {
   static constexpr int kGroups = 512 / kGroupCols;
   static constexpr int kSliceTiles = kDySlice / kBN;       // 4 column tiles per unit
   static constexpr int kChunkTiles = kDyChunk / kBM;       // 2 row tiles per unit
+  static constexpr int kPrefetch = 4;                      // dY tiles warmed in L2 before the dependency wait
   static constexpr int kEpiWarps = 8, kXfWarps = 4;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kXfWarps);
   static constexpr int kCPT = RP / 2;                      // columns of R per epilogue thread
@@ -118,13 +119,22 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
-  grid_dependents_launch();
-  const Abort ab{abort_flag, status};
   const int total = n_sl * n_ch;
   // valid column tiles of a slice and row tiles of a chunk (ragged N and M)
   auto n_tiles = [&](int sl) { return (min(N - sl * kDySlice, kDySlice) + C::kBN - 1) / C::kBN; };
   auto r_tiles = [&](int ch) { return (min(M - ch * kDyChunk, kDyChunk) + C::kBM - 1) / C::kBM; };
+  if (threadIdx.x == 0 && int(blockIdx.x) < total) {
+    // the first dY tiles of this CTA's first unit, into L2 while the predecessor drains
+    const int sl = int(blockIdx.x) % n_sl, ch = int(blockIdx.x) / n_sl;
+    const int nnt = n_tiles(sl), nrt = r_tiles(ch);
+    int n = 0;
+    for (int i = 0; i < nnt && n < C::kPrefetch; ++i)
+      for (int j = 0; j < nrt && n < C::kPrefetch; ++j, ++n)
+        for (int q = 0; q < 4; ++q) tma_prefetch_l2(&tm_dy, sl * kDySlice + i * C::kBN + 32 * q, ch * kDyChunk + j * C::kBM);
+  }
+  grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
+  grid_dependents_launch();
+  const Abort ab{abort_flag, status};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -8,25 +8,28 @@
 // batch-invariant", section "Summary"; the alpha scale is fused into the
 // epilogue, as that page's "Benchmark" section proposes.)
 //
-// Two phases in one cooperative launch. First every CTA adds the slice
-// partials (left by the down kernel) of its share of the batch rows with the
-// canonical pairwise tree (FP32, round to nearest), rounds to BF16 and writes
-// those rows of u / du; a grid-wide barrier follows. Then the expansion: work
-// unit = (128-row tile, BN-column tile), BN = 256 / (RP / 16), units dealt out
-// round-robin, so that at any time the CTAs write one compact band of the
-// output (consecutive units are neighbours in memory), which the memory
-// system absorbs markedly faster than each CTA writing its own distant region.
-// The producer brings each unit's 128 rows of u / du and its weight tile with
-// TMA. The unit is one tcgen05 MMA per 16-wide slice of R (M=128, N=BN,
-// K=16), each into its own TMEM accumulator, summed by the canonical tree.
-// Eight epilogue warps read TMEM, finish the tree (and the alpha multiply);
-// each warp stages its own 32 x 32 FP32 boxes in 128-byte-swizzled shared
-// memory (a ring of four, no barrier across warps) and writes them with TMA
-// stores (L2 evict-first), so every output byte is written exactly once, in
-// full lines.
+// One cooperative launch. The u / du rows are the canonical pairwise tree
+// (FP32, round to nearest) over the slice partials left by the down kernel,
+// rounded to BF16. Two prep warps per CTA form its share of the batch rows,
+// write them to u / du and meet the other CTAs at a grid-wide barrier. The
+// expansion does not wait for that barrier at first: the epilogue warps form
+// the rows of the CTA's first two units themselves, straight into those
+// units' operand stages, so the stores start at once and the barrier's wait
+// overlaps them; from the third unit on the producer loads the rows with TMA
+// after the barrier. Work unit = (128-row tile, BN-column tile), BN = 256 /
+// (RP / 16), units dealt out round-robin, so that at any time the CTAs write
+// one compact band of the output (consecutive units are neighbours in
+// memory), which the memory system absorbs markedly faster than each CTA
+// writing its own distant region. The unit is one tcgen05 MMA per 16-wide
+// slice of R (M=128, N=BN, K=16), each into its own TMEM accumulator, summed
+// by the canonical tree. Eight epilogue warps read TMEM, finish the tree (and
+// the alpha multiply); each warp stages its own 32 x 32 FP32 boxes in
+// 128-byte-swizzled shared memory (a ring of four, no barrier across warps)
+// and writes them with TMA stores (L2 evict-first), so every output byte is
+// written exactly once, in full lines.
 //
-// Warp roles in the expansion: 0 = TMA producer (u / du rows, B / A weight
-// tile), 1 = MMA issuer (TMEM owner), 2..9 = epilogue.
+// Warp roles: 0 = TMA producer (u / du rows, B / A weight tile), 1 = MMA
+// issuer (TMEM owner), 2..9 = epilogue, 10..11 = prep (u / du share, barrier).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -44,8 +47,11 @@ struct UpCfg {
   static constexpr int kStages = RP == 16 ? 6 : (RP == 32 ? 5 : 3);   // operand ring (weight tile from L2)
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kEpiWarps = 8, kPrepWarps = 2;
+  static constexpr int kLocal = 2;                     // units whose u / du rows a CTA forms itself
+  static_assert(kLocal * kBM * (RP / 8) % (32 * kEpiWarps) == 0, "whole items per epilogue thread");
+  static_assert(kLocal <= kStages, "locally formed rows sit in the first stages");
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kPrepWarps);
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
@@ -56,7 +62,7 @@ struct UpCfg {
   static constexpr int kStgBytes = 32 * kChunk * 4;    // one 32-row x 32-column FP32 box: 4 KB
   static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
   static constexpr size_t kBarOff = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1;
+  static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 3;
   static constexpr size_t kSmem = kBarOff + 1024 + kNumBars * 8 + 16;
   static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
@@ -83,6 +89,8 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   auto tfull = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
   auto tempty = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kBufs + b); };
   const uint32_t drain = bar0 + 8u * (2 * C::kStages + 2 * C::kBufs);
+  const uint32_t ufirst = drain + 8u;   // the first kLocal units' u / du rows are in their stages
+  const uint32_t gdone = drain + 16u;   // every CTA's share of u / du is in global memory (prep warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -97,6 +105,8 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       mbar_init(tempty(b), C::kEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(ufirst, C::kEpiWarps);
+    mbar_init(gdone, 1);
     *abort_flag = 0u;
     mbar_fence_init();
     prefetch_map(&tm_a);
@@ -116,31 +126,24 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   const Abort ab{abort_flag, status};
   const int total = n_mt * n_nt;
 
-  // ---- phase 1: this CTA's rows of u / du = bf16(tree over the S slice partials)
-  {
-    const int r0 = int(int64_t(M) * blockIdx.x / gridDim.x), r1 = int(int64_t(M) * (blockIdx.x + 1) / gridDim.x);
-    const size_t stride = size_t(M) * RP;
-    for (int i = threadIdx.x; i < (r1 - r0) * (R / 8); i += C::kThreads) {
-      const int row = r0 + i / (R / 8), g = i % (R / 8);
-      *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) =
-          slices_to_bf16x8(part + size_t(row) * RP + g * 8, stride, S);
-    }
-  }
-  grid_sync(sync, gridDim.x, abort_flag, status, 10);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
-      fence_proxy_async_global();          // u / du rows written by the CTAs before the barrier, read by TMA
       Ring r;
       uint32_t issued = 0, parities = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const int mt = u / n_nt, nt = u % n_nt;
+        const int k = (u - int(blockIdx.x)) / int(gridDim.x);     // this CTA's k-th unit
+        if (k == C::kLocal) {
+          wait(gdone, 0u, ab, 16);           // the rows of later units come from every CTA's share
+          fence_proxy_async_global();        // written by generic stores, read by TMA
+        }
         if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
           const uint32_t st = base + r.idx * C::kStageBytes;
-          mbar_expect_tx(full(r.idx), C::kStageBytes);
-          tma_load(st, &tm_a, full(r.idx), 0, mt * C::kBM, pol);                   // u / du rows of the tile
+          mbar_expect_tx(full(r.idx), k < C::kLocal ? C::kBBytes : C::kStageBytes);
+          if (k >= C::kLocal) tma_load(st, &tm_a, full(r.idx), 0, mt * C::kBM, pol);   // u / du rows of the tile
           if (DX) {
 #pragma unroll
             for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       Ring r, b;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         bool ok = wait(full(r.idx), r.phase, ab, 13);
+        if (u < int(blockIdx.x) + C::kLocal * int(gridDim.x)) ok = ok && wait(ufirst, 0u, ab, 18);
         ok = ok && wait(tempty(b.idx), b.phase ^ 1u, ab, 14);
         if (ok) {
           tc_fence_after();
@@ -196,6 +200,34 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     const uint32_t my_stg = stg0 + (warp - 2) * C::kStg * C::kStgBytes;
     const uint64_t pol_out = policy_evict_first();
     uint8_t* my_stg_ptr = stg_ptr + (warp - 2) * C::kStg * C::kStgBytes;
+    {
+      // the rows of u / du of this CTA's first kLocal units = bf16(tree over the S slice partials),
+      // straight into stages 0 .. kLocal-1 in the layout their TMA loads would give (rows of
+      // RP * 2 bytes, 16-byte chunks swizzled by the row's place in the 8-row swizzle atom);
+      // all loads of a thread are issued before its first store
+      constexpr int kItems = C::kLocal * C::kBM * (RP / 8) / (32 * C::kEpiWarps);
+      const size_t stride = size_t(M) * RP;
+      uint4 v[kItems];
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const int i = int(threadIdx.x) - 64 + j * 32 * C::kEpiWarps;
+        const int k = i / (C::kBM * (RP / 8)), row = (i / (RP / 8)) % C::kBM, g = i % (RP / 8);
+        const int u = int(blockIdx.x) + k * int(gridDim.x);
+        const int grow = (u / n_nt) * C::kBM + row;
+        v[j] = u < total && grow < M && g < R / 8 ? slices_to_bf16x8(part + size_t(grow) * RP + g * 8, stride, S)
+                                                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const int i = int(threadIdx.x) - 64 + j * 32 * C::kEpiWarps;
+        const int k = i / (C::kBM * (RP / 8)), row = (i / (RP / 8)) % C::kBM, g = i % (RP / 8);
+        const uint32_t o = uint32_t(row * C::kSpan + g * 16);
+        *reinterpret_cast<uint4*>(gbase + size_t(k) * C::kStageBytes + (o ^ (((o >> 7) & uint32_t(C::kSpan / 16 - 1)) << 4))) = v[j];
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ufirst);
+    }
     int sidx = 0;
     Ring b;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -272,6 +304,27 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       b.next<C::kBufs>();
     }
     if (lane == 0) tma_store_wait_all<0>();
+  } else {
+    // ------------------------------------------------------- prep warps
+    // This CTA's share of the batch rows of u / du = bf16(tree over the S slice partials), then
+    // the grid-wide barrier (cooperative launch: every CTA is resident); its wait overlaps the
+    // first unit, whose rows the epilogue warps formed themselves.
+    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
+    const int r0 = int(int64_t(M) * blockIdx.x / gridDim.x), r1 = int(int64_t(M) * (blockIdx.x + 1) / gridDim.x);
+    const size_t stride = size_t(M) * RP;
+    for (int i = t; i < (r1 - r0) * (R / 8); i += 32 * C::kPrepWarps) {
+      const int row = r0 + i / (R / 8), g = i % (R / 8);
+      *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) =
+          slices_to_bf16x8(part + size_t(row) * RP + g * 8, stride, S);
+    }
+    __threadfence();
+    named_bar(1, 32 * C::kPrepWarps);
+    if (t == 0) {
+      grid_arrive_wait(sync, gridDim.x, abort_flag, status, 10);
+      fence_proxy_async_global();
+      mbar_arrive(gdone);
+      grid_leave(sync, gridDim.x);
+    }
   }
 
   tc_fence_before();
