@@ -72,12 +72,12 @@ def measured_peaks():
 # dram__bytes_write.sum), keyed by kernel, with the hash of the kernel source
 # the counters were taken on; a kernel changed since then reports null.
 NCU_TRAFFIC = {   # ncu, training step, warm caches (--cache-control none), per launch
-    "down U": {"bytes": 70000000, "src_hash": "2b18d4f8984aa78d"},
-    "up dY_lora": {"bytes": 123800000, "src_hash": "edafa9efa343b533"},
-    "dy dU+dB": {"bytes": 78500000, "src_hash": "02527fdf6c200244"},
-    "up dX": {"bytes": 126000000, "src_hash": "edafa9efa343b533"},
-    "wgrad dA": {"bytes": 75400000, "src_hash": "e3813b8b0870e8f6"},
-    "combine dA+dB": {"bytes": 1500000, "src_hash": "337f1bac5b0e1c32"},
+    "down U": {"bytes": 71600000, "src_hash": "e57e2cb6ea3afff6"},
+    "up dY_lora": {"bytes": 125100000, "src_hash": "ef3ff4a0da20658b"},
+    "dy dU+dB": {"bytes": 79700000, "src_hash": "87a5fe328aafbc61"},
+    "up dX": {"bytes": 127400000, "src_hash": "ef3ff4a0da20658b"},
+    "wgrad dA": {"bytes": 75500000, "src_hash": "e3813b8b0870e8f6"},
+    "combine dA+dB": {"bytes": 860000, "src_hash": "337f1bac5b0e1c32"},
 }
 
 
