@@ -237,6 +237,45 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
+    """Forward only, FP32 dY_lora against the BF16 output variant: CUDA-graph
+    timed like the main step (inputs rotated over the same copies of X)."""
+    import torch
+
+    out = {}
+    bf, f4 = 2, 4
+    for name, ydt, ysz in (("fwd_fp32_dy", torch.float32, f4), ("fwd_bf16_dy", torch.bfloat16, bf)):
+        Y = torch.empty((M, N), dtype=ydt, device=dev)
+        U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+        wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+        for i in range(5):
+            ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                gst = torch.cuda.current_stream(dev)
+                for i in range(steps):
+                    ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=gst)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * steps)
+        nbytes = M * K * bf + R * K * bf + 2 * M * R * bf + N * R * bf + M * N * ysz
+        out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "launches_per_step": 2}
+        assert ld.lora_delta_device_status(wf) == 0
+    return out
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, world, rank, local):
     import torch
@@ -368,6 +407,11 @@ def run_ours(args, world, rank, local):
     tr = NCU_TRAFFIC.get(dominant)
     traffic = tr["bytes"] if tr and tr.get("src_hash") == source_hash(src) else None
 
+    # ---------------------------------------- forward variants (FP32 / BF16 dY_lora)
+    variants = None
+    if not args.no_variants:
+        variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev)
+
     # ----------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
@@ -479,6 +523,7 @@ def run_ours(args, world, rank, local):
                         for k in KERNELS},
             "gpu_launches": len(KERNELS) * args.steps,
             "e2e": e2e,
+            "variants": variants,
             "cpu_baseline": cpu,
             "clocks": clk,
             "provenance": json.loads(ld.lora_delta_describe()),
@@ -497,6 +542,7 @@ def main():
     p.add_argument("--reference-budget-s", type=float, default=120.0,
                    help="CPU seconds the --impl reference run may spend in total")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-variants", action="store_true", help="skip the forward-only FP32 / BF16 dY_lora timing")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args()
     if args.warmup < 3:

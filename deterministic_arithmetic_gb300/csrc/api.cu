@@ -167,9 +167,10 @@ size_t lora_delta_bwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R)
   return bwd_layout(M, K, N, R).total;
 }
 
-lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K, int64_t N,
-                           int64_t R, float* delta_y, void* u, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+namespace {
+lora_status fwd_impl(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K, int64_t N,
+                     int64_t R, void* delta_y, bool y_bf16, void* u, void* workspace, size_t workspace_bytes,
+                     void* stream) {
   lora_status s = check_shape(M, K, N, R);
   if (s != LORA_OK) return s;
   if (M == 0) return LORA_OK;
@@ -188,7 +189,8 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
       !make_map(&m_u, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
       !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m_b, b, false, N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
-      !make_map(&m_y, delta_y, true, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+      !(y_bf16 ? make_map(&m_y, delta_y, false, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
+              : make_map(&m_y, delta_y, true, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
     return LORA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -202,11 +204,24 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
     return LORA_ERR_CUDA;
   rec.mark();
   // U = bf16(tree over the K-slice partials), built inside the up-projection, which also writes u
-  if (launch_up(RP, false, m_u, m_b, m_y, upart, int(ceil_div(K, down_slice(RP))), u, int(R), int(M), int(N), alpha, status,
-                grid_for(up_units(M, N, RP), nsm), st) != cudaSuccess)
+  if (launch_up(RP, false, y_bf16, m_u, m_b, m_y, upart, int(ceil_div(K, down_slice(RP))), u, int(R), int(M), int(N),
+                alpha, status, grid_for(up_units(M, N, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();
   return LORA_OK;
+}
+}  // namespace
+
+lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K, int64_t N,
+                           int64_t R, float* delta_y, void* u, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return fwd_impl(x, a, b, alpha, M, K, N, R, delta_y, false, u, workspace, workspace_bytes, stream);
+}
+
+lora_status lora_delta_fwd_bf16(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K,
+                                int64_t N, int64_t R, void* delta_y, void* u, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return fwd_impl(x, a, b, alpha, M, K, N, R, delta_y, true, u, workspace, workspace_bytes, stream);
 }
 
 lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const void* b, const void* u, float alpha,
@@ -269,7 +284,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
     rec.mark();
   }
   // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
-  if (launch_up(RP, true, m_du_128, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
+  if (launch_up(RP, true, false, m_du_128, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
                 grid_for(up_units(M, K, RP), nsm), st) != cudaSuccess)
     return LORA_ERR_CUDA;
   rec.mark();

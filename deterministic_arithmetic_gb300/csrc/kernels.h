@@ -77,8 +77,9 @@ inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil
 // word; `grid` the number of persistent CTAs.
 cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
                         float alpha, uint32_t* status, int grid, cudaStream_t st);
-// up: a = u / du rows (box 128 x RP), written by the kernel itself in its first phase.
-cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+// up: a = u / du rows (box 128 x RP), written by the kernel itself in its first phase;
+// y_bf16 (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte swizzle.
+cudaError_t launch_up(int RP, bool dx, bool y_bf16, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                       const float* part, int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status,
                       int grid, cudaStream_t st);
 cudaError_t launch_dy(const CUtensorMap& dy, const CUtensorMap& b, const CUtensorMap& u, float* du_part,

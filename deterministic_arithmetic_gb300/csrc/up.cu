@@ -28,6 +28,10 @@
 // and writes them with TMA stores (L2 evict-first), so every output byte is
 // written exactly once, in full lines.
 //
+// YBF (forward only): dY_lora is written as BF16, bf16(fp32(sum) * alpha): the
+// FP32 value rounded once more (round to nearest even), half the bytes. Each
+// 32-column box is then 32 rows x 64 bytes (64-byte swizzle).
+//
 // Warp roles: 0 = TMA producer (u / du rows, B / A weight tile), 1 = MMA
 // issuer (TMEM owner), 2..9 = epilogue, 10..11 = prep (u / du share, barrier).
 #include "common.cuh"
@@ -69,13 +73,14 @@ struct UpCfg {
   static_assert(kBufs == 2, "double-buffered accumulators");
 };
 
-template <int RP, bool DX>
+template <int RP, bool DX, bool YBF>
 __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ part, int S,
               __nv_bfloat16* __restrict__ out_bf16, int R, int M, int Nout, int n_mt, int n_nt, float alpha,
               uint32_t* status, uint32_t* sync) {
   using C = UpCfg<RP, DX>;
+  static_assert(!(DX && YBF), "BF16 output is the forward's");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -262,24 +267,38 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
           for (int j = 0; j < C::kLeaves; ++j)
 #pragma unroll
             for (int b8 = 0; b8 < C::kCols / 8; ++b8) reg_fence(v[j][b8]);
+          // leaf tree of column e of this round (and the alpha multiply of the forward)
+          auto value = [&](int e) {
+            const int b8 = e / 8, k = e % 8;
+            float s;
+            if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
+            else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
+            else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
+                           __uint_as_float(v[3][b8][k]));
+            return DX ? s : __fmul_rn(s, alpha);
+          };
+          if constexpr (YBF) {
 #pragma unroll
-          for (int e4 = 0; e4 < C::kCols / 4; ++e4) {
-            const int gcol = rd * C::kCols + e4 * 4;                  // column within the group
-            const int box = gcol / C::kChunk, cc = (gcol % C::kChunk) / 4;
-            float f[4];
+            for (int e8 = 0; e8 < C::kCols / 8; ++e8) {
+              const int gcol = rd * C::kCols + e8 * 8;                // column within the group
+              const int box = gcol / C::kChunk, cc = (gcol % C::kChunk) / 8;
+              float f[8];
 #pragma unroll
-            for (int t4 = 0; t4 < 4; ++t4) {
-              const int e = e4 * 4 + t4, b8 = e / 8, k = e % 8;
-              float s;
-              if (C::kLeaves == 1) s = __uint_as_float(v[0][b8][k]);
-              else if (C::kLeaves == 2) s = __fadd_rn(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]));
-              else s = tree4(__uint_as_float(v[0][b8][k]), __uint_as_float(v[1][b8][k]), __uint_as_float(v[2][b8][k]),
-                             __uint_as_float(v[3][b8][k]));
-              f[t4] = DX ? s : __fmul_rn(s, alpha);
+              for (int t8 = 0; t8 < 8; ++t8) f[t8] = value(e8 * 8 + t8);
+              // 32 rows x 32 BF16 columns per box: 64-byte rows, 64-byte swizzle, chunk ^ ((row / 2) % 4)
+              uint8_t* buf = my_stg_ptr + ((sidx + box) % C::kStg) * C::kStgBytes + lane * 64;
+              *reinterpret_cast<uint4*>(buf + ((cc ^ ((lane >> 1) & 3)) * 16)) = pack_bf16x8(f);
             }
-            // each warp stages its own 32 rows x 32 columns: 128-byte swizzle, chunk ^ (row % 8)
-            uint8_t* buf = my_stg_ptr + ((sidx + box) % C::kStg) * C::kStgBytes + lane * 128;
-            *reinterpret_cast<float4*>(buf + ((cc ^ (lane & 7)) * 16)) = make_float4(f[0], f[1], f[2], f[3]);
+          } else {
+#pragma unroll
+            for (int e4 = 0; e4 < C::kCols / 4; ++e4) {
+              const int gcol = rd * C::kCols + e4 * 4;                // column within the group
+              const int box = gcol / C::kChunk, cc = (gcol % C::kChunk) / 4;
+              // each warp stages its own 32 rows x 32 columns: 128-byte swizzle, chunk ^ (row % 8)
+              uint8_t* buf = my_stg_ptr + ((sidx + box) % C::kStg) * C::kStgBytes + lane * 128;
+              *reinterpret_cast<float4*>(buf + ((cc ^ (lane & 7)) * 16)) =
+                  make_float4(value(e4 * 4), value(e4 * 4 + 1), value(e4 * 4 + 2), value(e4 * 4 + 3));
+            }
           }
         }
         fence_proxy_async();
@@ -335,43 +354,51 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   }
 }
 
-template <int RP, bool DX>
+template <int RP, bool DX, bool YBF>
 static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const float* part,
                               int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
                               cudaStream_t st) {
   using C = UpCfg<RP, DX>;
   const int n_mt = int(ceil_div(M, C::kBM)), n_nt = int(ceil_div(Nout, C::kBN));
-  return launch_pdl_coop(up_kernel<RP, DX>, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, out, part, S,
+  return launch_pdl_coop(up_kernel<RP, DX, YBF>, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, out, part, S,
                          static_cast<__nv_bfloat16*>(out_bf16), R, M, Nout, n_mt, n_nt, alpha, status, status + 1);
 }
 
-cudaError_t launch_up(int RP, bool dx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+cudaError_t launch_up(int RP, bool dx, bool y_bf16, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                       const float* part, int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status,
                       int grid, cudaStream_t st) {
-  switch (RP * 2 + (dx ? 1 : 0)) {
-    case 32: return launch_one<16, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 33: return launch_one<16, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 64: return launch_one<32, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 65: return launch_one<32, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 128: return launch_one<64, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 129: return launch_one<64, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+  if (dx && y_bf16) return cudaErrorInvalidValue;
+  switch (RP * 4 + (dx ? 1 : 0) + (y_bf16 ? 2 : 0)) {
+    case 64: return launch_one<16, false, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 65: return launch_one<16, true, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 66: return launch_one<16, false, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 128: return launch_one<32, false, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 129: return launch_one<32, true, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 130: return launch_one<32, false, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 256: return launch_one<64, false, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 257: return launch_one<64, true, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 258: return launch_one<64, false, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int RP, bool DX>
+template <int RP, bool DX, bool YBF>
 static cudaError_t prep_one() {
-  return cudaFuncSetAttribute(up_kernel<RP, DX>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(UpCfg<RP, DX>::kSmem));
+  return cudaFuncSetAttribute(up_kernel<RP, DX, YBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(UpCfg<RP, DX>::kSmem));
 }
 
 cudaError_t prepare_up() {
   cudaError_t e;
-  if ((e = prep_one<16, false>()) != cudaSuccess) return e;
-  if ((e = prep_one<16, true>()) != cudaSuccess) return e;
-  if ((e = prep_one<32, false>()) != cudaSuccess) return e;
-  if ((e = prep_one<32, true>()) != cudaSuccess) return e;
-  if ((e = prep_one<64, false>()) != cudaSuccess) return e;
-  return prep_one<64, true>();
+  if ((e = prep_one<16, false, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<16, true, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<16, false, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, false, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, true, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, false, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<64, false, false>()) != cudaSuccess) return e;
+  if ((e = prep_one<64, true, false>()) != cudaSuccess) return e;
+  return prep_one<64, false, true>();
 }
 
 }  // namespace lora

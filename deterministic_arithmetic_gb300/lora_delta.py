@@ -46,6 +46,8 @@ def _lib() -> ctypes.CDLL:
         lib.lora_delta_fwd.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
                                        ctypes.c_size_t, _vp]
         lib.lora_delta_fwd.restype = ctypes.c_int
+        lib.lora_delta_fwd_bf16.argtypes = lib.lora_delta_fwd.argtypes
+        lib.lora_delta_fwd_bf16.restype = ctypes.c_int
         lib.lora_delta_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
                                        _vp, _vp, ctypes.c_size_t, _vp]
         lib.lora_delta_bwd.restype = ctypes.c_int
@@ -100,7 +102,10 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def lora_delta_fwd(x, a, b, alpha: float, *, delta_y=None, u=None, workspace=None, stream=None):
-    """Forward: ``u = bf16(x @ a.T)``, ``delta_y = fp32(u @ b.T) * alpha``."""
+    """Forward: ``u = bf16(x @ a.T)``, ``delta_y = fp32(u @ b.T) * alpha``.
+
+    A BF16 ``delta_y`` selects ``lora_delta_fwd_bf16`` (the same FP32 value,
+    rounded to BF16 inside the kernel)."""
     M, K = x.shape
     R = a.shape[0]
     N = b.shape[0]
@@ -109,14 +114,16 @@ def lora_delta_fwd(x, a, b, alpha: float, *, delta_y=None, u=None, workspace=Non
         delta_y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     if u is None:
         u = torch.empty((M, R), dtype=torch.bfloat16, device=x.device)
-    _check(delta_y, "delta_y", torch.float32, (M, N)); _check(u, "u", torch.bfloat16, (M, R))
+    y_bf16 = delta_y.dtype == torch.bfloat16
+    _check(delta_y, "delta_y", torch.bfloat16 if y_bf16 else torch.float32, (M, N)); _check(u, "u", torch.bfloat16, (M, R))
     need = lora_delta_fwd_workspace_size(M, K, N, R)
     if workspace is None:
         workspace = new_workspace(need, x.device)
-    rc = _lib().lora_delta_fwd(_ptr(x), _ptr(a), _ptr(b), float(alpha), M, K, N, R, _ptr(delta_y), _ptr(u),
+    name = "lora_delta_fwd_bf16" if y_bf16 else "lora_delta_fwd"
+    rc = getattr(_lib(), name)(_ptr(x), _ptr(a), _ptr(b), float(alpha), M, K, N, R, _ptr(delta_y), _ptr(u),
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != LORA_OK:
-        raise LoraDeltaError(rc, "lora_delta_fwd")
+        raise LoraDeltaError(rc, name)
     return delta_y, u
 
 

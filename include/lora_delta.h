@@ -83,6 +83,21 @@ lora_status lora_delta_fwd(const void *x, const void *a, const void *b, float al
                            int64_t R, float *delta_y, void *u, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Forward pass with a BF16 delta_y: the half-size output a reviewer asks for
+ * in the review thread of page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA +
+ * Triton, both batch-invariant" (the FP32 output doubles the bytes of the
+ * widest tensor; casting inside the operator adds one rounding).
+ *   delta_y  [M][N] bf16   out: bf16((U @ B^T) * alpha), the FP32 result of
+ *                          lora_delta_fwd rounded to nearest even: bit for bit
+ *                          that FP32 output converted to BF16
+ * Every other argument, the workspace, u and the error behaviour are those of
+ * lora_delta_fwd (delta_y must be 16-byte aligned as well).
+ */
+lora_status lora_delta_fwd_bf16(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K,
+                                int64_t N, int64_t R, void *delta_y, void *u, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
  * Backward pass (no base-weight gradient).
  *   dy       [M][N] bf16   upstream gradient of delta_y
  *   x, a, b               as in the forward pass

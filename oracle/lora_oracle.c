@@ -216,6 +216,31 @@ int ora_delta_y(const uint16_t *u, const uint16_t *b, float alpha, int64_t M, in
 }
 
 /*
+ * delta_y_bf16[m][n] = rnbf(delta_y[m][n]): the BF16 output variant, the FP32
+ * result of ora_delta_y rounded once more to bfloat16 (round to nearest even);
+ * the half-size output asked for in the review thread of page "[DSv4][P5-3]
+ * shared_grouped_lora_delta: CUDA + Triton, both batch-invariant".
+ */
+int ora_delta_y_bf16(const uint16_t *u, const uint16_t *b, float alpha, int64_t M, int64_t N,
+                     int64_t R, uint16_t *delta_y_bf16, int threads)
+{
+    float *y = (float *)malloc((size_t)(M * N > 0 ? M * N : 1) * sizeof(float));
+    if (!y) return 1;
+    int rc = ora_delta_y(u, b, alpha, M, N, R, y, NULL, threads);
+    for (int64_t e = 0; rc == 0 && e < M * N; ++e) {
+#if ORACLE_MUTANT == 10  /* planted: the BF16 output truncated instead of rounded */
+        uint32_t bits;
+        memcpy(&bits, &y[e], 4);
+        delta_y_bf16[e] = (uint16_t)(bits >> 16);
+#else
+        delta_y_bf16[e] = rnbf(y[e]);
+#endif
+    }
+    free(y);
+    return rc;
+}
+
+/*
  * dv[m][n] = rnbf(rn32(dy[m][n] * alpha))  ("dV = dY * alpha", rounded to BF16
  * between the GEMMs: "D4", section "Summary").
  */

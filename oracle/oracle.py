@@ -69,6 +69,7 @@ class Oracle:
         sigs = {
             "ora_u": [_u16p, _u16p, _i64, _i64, _i64, _u16p, _f32p, _f64p, ctypes.c_int],
             "ora_delta_y": [_u16p, _u16p, ctypes.c_float, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
+            "ora_delta_y_bf16": [_u16p, _u16p, ctypes.c_float, _i64, _i64, _i64, _u16p, ctypes.c_int],
             "ora_dv": [_u16p, ctypes.c_float, _i64, _i64, _u16p],
             "ora_du": [_u16p, _u16p, _i64, _i64, _i64, _u16p, _f32p, _f64p, ctypes.c_int],
             "ora_db": [_u16p, _u16p, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
@@ -121,6 +122,16 @@ class Oracle:
         rc = self.lib.ora_delta_y(_p(u, _u16p), _p(b, _u16p), float(alpha), M, N, R, _p(y, _f32p), _p(s, _f64p), self.threads)
         assert rc == 0
         return (y, s) if want_s else y
+
+    def delta_y_bf16(self, u, b, alpha):
+        """The BF16 output variant: delta_y rounded to bfloat16 (bits)."""
+        u = self._c(u, np.uint16); b = self._c(b, np.uint16)
+        M, R = u.shape; N = b.shape[0]
+        assert b.shape == (N, R)
+        y = np.empty((M, N), np.uint16)
+        rc = self.lib.ora_delta_y_bf16(_p(u, _u16p), _p(b, _u16p), float(alpha), M, N, R, _p(y, _u16p), self.threads)
+        assert rc == 0
+        return y
 
     def dv(self, dy, alpha):
         dy = self._c(dy, np.uint16)

@@ -11,7 +11,9 @@ when the oracle disagrees with:
 * ``pin_permutation``       R = K, A a permutation matrix: U is X with permuted columns;
 * ``pin_library_matmul``    dY_lora from a given U against numpy's binary64 matmul;
 * ``pin_invariants``        B = 0, A = 0, linearity in alpha;
-* ``pin_finite_differences`` the gradients against central differences of the scalar loss.
+* ``pin_finite_differences`` the gradients against central differences of the scalar loss;
+* ``pin_bf16_output``       the BF16 dY_lora variant: exact rationals rounded at its extra
+                            rounding point, and constructed ties of round-to-nearest-even.
 
 The test suite also runs every pin against builds of the oracle with a planted
 mistake and requires that some pin fails for each.
@@ -224,5 +226,34 @@ def pin_finite_differences(o, M=6, K=10, N=7, R=3, seed=4):
     np.testing.assert_array_equal(out["dx"].astype(np.float64), fd(X, "X"))
 
 
+# ------------------------------------------------------ BF16 output variant
+def pin_bf16_output(o, seed=13):
+    # (1) the whole forward with exact rationals, correctly rounded at U, at the FP32 result and
+    # then once more to BF16
+    w = S.Workload("rational_bf16", S.Shape(5, 7, 6, 3, 0.3), {"x": 1.0, "a": 0.4, "b": 0.6, "dy": 1.0})
+    d = w.generate(seed)
+    a32 = np.float32(0.3)
+    want = ex.exact_chain(d["x"], d["a"], d["b"], d["dy"], a32)
+    got = o.delta_y_bf16(o.u(d["x"], d["a"]), d["b"], float(a32))
+    exp = np.empty(want["delta_y"].shape, np.uint16)
+    for idx, v in np.ndenumerate(want["delta_y"]):
+        q = ex.rnbf_of_f32(Fraction(float(v)))
+        exp[idx] = (0x7F80 if q > 0 else 0xFF80) if isinstance(q, float) else ex.bf16_bits(q)
+    _eq_bits("bf16_output:rational", got, exp)
+    # (2) sums placed exactly on and next to BF16 midpoints (alpha = 1, every product exact):
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7 and goes to the even 1; 1 + 3*2^-8 goes up to
+    # 1 + 2^-6; just above a midpoint goes up; the signs mirror
+    u = _bits([[1.0, 2.0 ** -8, 2.0 ** -20, 0, 0, 0, 0, 0]])
+    b = _bits([[1, 1, 0, 0, 0, 0, 0, 0],          # 1 + 2^-8           -> 1
+               [1, 3, 0, 0, 0, 0, 0, 0],          # 1 + 3 * 2^-8       -> 1 + 2^-6
+               [1, 1, 1, 0, 0, 0, 0, 0],          # 1 + 2^-8 + 2^-20   -> 1 + 2^-7
+               [-1, -1, 0, 0, 0, 0, 0, 0],        # -(1 + 2^-8)        -> -1
+               [-1, -3, 0, 0, 0, 0, 0, 0],        # -(1 + 3 * 2^-8)    -> -(1 + 2^-6)
+               [1, -1, 0, 0, 0, 0, 0, 0]])        # 1 - 2^-8 (exact)   -> 1 - 2^-8
+    got = o.delta_y_bf16(u, b, 1.0)
+    _eq_bits("bf16_output:midpoints", got, _bits([[1.0, 1.0 + 2.0 ** -6, 1.0 + 2.0 ** -7, -1.0,
+                                                   -(1.0 + 2.0 ** -6), 1.0 - 2.0 ** -8]]))
+
+
 ALL_PINS = [pin_golden, pin_rounding, pin_rational, pin_headroom_integers, pin_permutation,
-            pin_library_matmul, pin_invariants, pin_finite_differences]
+            pin_library_matmul, pin_invariants, pin_finite_differences, pin_bf16_output]

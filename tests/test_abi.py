@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("lora_delta_fwd", "lora_delta_bwd", "lora_delta_fwd_workspace_size", "lora_delta_bwd_workspace_size",
+    for n in ("lora_delta_fwd", "lora_delta_fwd_bf16", "lora_delta_bwd", "lora_delta_fwd_workspace_size",
+              "lora_delta_bwd_workspace_size",
               "lora_status_str", "lora_delta_device_status", "lora_delta_set_profile_events", "lora_delta_describe"):
         assert n in names, n
 
@@ -67,8 +68,8 @@ def test_workspace_sizes():
     assert ld.lora_delta_fwd_workspace_size(100, 128, 96, 8) <= ld.lora_delta_fwd_workspace_size(200, 128, 96, 8)
 
 
-def _fwd(lib, ptrs, M=64, K=128, N=96, R=8, ws_bytes=1 << 20):
-    f = lib.lora_delta_fwd
+def _fwd(lib, ptrs, M=64, K=128, N=96, R=8, ws_bytes=1 << 20, name="lora_delta_fwd"):
+    f = getattr(lib, name)
     f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float] + [ctypes.c_int64] * 4 + [ctypes.c_void_p] * 3 + \
                  [ctypes.c_size_t, ctypes.c_void_p]
     f.restype = ctypes.c_int
@@ -99,6 +100,12 @@ def test_argument_errors_are_host_side(lib):
     assert _fwd(lib, ok6, R=72) == 4
     assert _fwd(lib, [FAKE + 2] + ok6[1:]) == 3                       # LORA_ERR_ALIGN
     assert _fwd(lib, ok6, ws_bytes=16) == 5                           # LORA_ERR_WORKSPACE
+    # the BF16-output forward shares the checks
+    assert _fwd(lib, ok6, M=0, name="lora_delta_fwd_bf16") == 0
+    assert _fwd(lib, ok6[:3] + [None] + ok6[4:], name="lora_delta_fwd_bf16") == 1
+    assert _fwd(lib, ok6, R=12, name="lora_delta_fwd_bf16") == 4
+    assert _fwd(lib, ok6[:3] + [FAKE + 4] + ok6[4:], name="lora_delta_fwd_bf16") == 3
+    assert _fwd(lib, ok6, ws_bytes=16, name="lora_delta_fwd_bf16") == 5
     ok10 = [FAKE] * 10
     assert _bwd(lib, ok10, M=0) == 0
     assert _bwd(lib, ok10[:8] + [None, FAKE]) == 1
@@ -114,6 +121,7 @@ def test_valid_call_without_gpu_fails_loudly(lib):
         pytest.skip("a GPU is present; this case is for hosts without one")
     # all arguments valid: the call reaches the device check and must report an error, not compute on the CPU
     assert _fwd(lib, [FAKE] * 6) in (6, 7)
+    assert _fwd(lib, [FAKE] * 6, name="lora_delta_fwd_bf16") in (6, 7)
 
 
 def test_describe(lib):

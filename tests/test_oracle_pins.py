@@ -8,7 +8,7 @@ import pytest
 import pins
 from oracle import oracle as oracle_mod
 
-N_MUTANTS = 9
+N_MUTANTS = 10
 
 
 @pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
