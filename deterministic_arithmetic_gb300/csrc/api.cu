@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -167,136 +168,314 @@ size_t lora_delta_bwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R)
   return bwd_layout(M, K, N, R).total;
 }
 
+}  // extern "C"
+
 namespace {
-lora_status fwd_impl(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K, int64_t N,
-                     int64_t R, void* delta_y, bool y_bf16, void* u, void* workspace, size_t workspace_bytes,
-                     void* stream) {
-  lora_status s = check_shape(M, K, N, R);
-  if (s != LORA_OK) return s;
-  if (M == 0) return LORA_OK;
-  if (!x || !a || !b || !delta_y || !u || !workspace) return LORA_ERR_NULL;
-  if (!aligned16(x) || !aligned16(a) || !aligned16(b) || !aligned16(delta_y) || !aligned16(u) || !aligned16(workspace))
-    return LORA_ERR_ALIGN;
-  const FwdLayout L = fwd_layout(M, K, R);
-  if (workspace_bytes < L.total) return LORA_ERR_WORKSPACE;
+
+// One site of a call: the arguments of the single-site entry points, or one
+// element of a grouped call.
+struct FwdIn {
+  const void *x, *a, *b;
+  float alpha;
+  int64_t M, K, N;
+  void* delta_y;
+  void* u;
+};
+struct BwdIn {
+  const void *dy, *x, *a, *b, *u;
+  float alpha;
+  int64_t M, K, N;
+  float *dx, *da, *db;
+  void* du;
+};
+
+// Workspace: the 256-byte status block, then each site's partial-sum regions in site order.
+size_t fwd_site_bytes(int64_t M, int64_t K, int64_t R) { return fwd_layout(M, K, R).total - kStatusBytes; }
+size_t bwd_site_bytes(int64_t M, int64_t K, int64_t N, int64_t R) {
+  return bwd_layout(M, K, N, R).total - kStatusBytes;
+}
+
+// Shared checks, in the order the single-site entry points document: shapes, NULL pointers,
+// alignment, workspace size. *active = sites with M > 0 (indices), *need = workspace bytes.
+template <class In, class Ptrs>
+lora_status check_sites(const In* in, int n, int64_t R, const void* workspace, size_t workspace_bytes, Ptrs ptrs,
+                        int* active, int* n_active) {
+  if (n < 1 || n > kMaxSites) return LORA_ERR_SHAPE;
+  for (int i = 0; i < n; ++i) {
+    const lora_status s = check_shape(in[i].M, in[i].K, in[i].N, R);
+    if (s != LORA_OK) return s;
+  }
+  *n_active = 0;
+  for (int i = 0; i < n; ++i)
+    if (in[i].M > 0) active[(*n_active)++] = i;
+  if (*n_active == 0) return LORA_OK;
+  for (int j = 0; j < *n_active; ++j)
+    for (const void* p : ptrs(in[active[j]]))
+      if (!p) return LORA_ERR_NULL;
+  if (!workspace) return LORA_ERR_NULL;
+  for (int j = 0; j < *n_active; ++j)
+    for (const void* p : ptrs(in[active[j]]))
+      if (!aligned16(p)) return LORA_ERR_ALIGN;
+  if (!aligned16(workspace)) return LORA_ERR_ALIGN;
+  return LORA_OK;
+}
+
+struct FwdPtrs {
+  std::array<const void*, 5> operator()(const FwdIn& s) const { return {s.x, s.a, s.b, s.delta_y, s.u}; }
+};
+struct BwdPtrs {
+  std::array<const void*, 9> operator()(const BwdIn& s) const {
+    return {s.dy, s.x, s.a, s.b, s.u, s.dx, s.da, s.db, s.du};
+  }
+};
+
+size_t fwd_need(const FwdIn* in, int n, int64_t R) {
+  size_t t = kStatusBytes;
+  for (int i = 0; i < n; ++i)
+    if (in[i].M > 0) t += fwd_site_bytes(in[i].M, in[i].K, R);
+  return t;
+}
+size_t bwd_need(const BwdIn* in, int n, int64_t R) {
+  size_t t = kStatusBytes;
+  for (int i = 0; i < n; ++i)
+    if (in[i].M > 0) t += bwd_site_bytes(in[i].M, in[i].K, in[i].N, R);
+  return t;
+}
+
+// The forward of every site in two launches (down over all sites' units, then up).
+lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  int active[kMaxSites], m = 0;
+  lora_status s = check_sites(in, n, R, workspace, workspace_bytes, FwdPtrs{}, active, &m);
+  if (s != LORA_OK || m == 0) return s;
+  if (workspace_bytes < fwd_need(in, n, R)) return LORA_ERR_WORKSPACE;
   int nsm = 0;
   if ((s = device_ready(&nsm)) != LORA_OK) return s;
 
   const int RP = padded_rank(int(R));
   const int span = RP * 2;
-  CUtensorMap m_x, m_a, m_b, m_y, m_u;
-  if (!make_map(&m_x, x, false, M, K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&m_u, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
-      !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_b, b, false, N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
-      !(y_bf16 ? make_map(&m_y, delta_y, false, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
-              : make_map(&m_y, delta_y, true, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
-    return LORA_ERR_CUDA;
-
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  float* upart = reinterpret_cast<float*>(ws + L.upart);
+  DownArgs dargs{};
+  UpArgs uargs{};
+  dargs.n = uargs.n = m;
+  uargs.R = int(R);
+  size_t off = kStatusBytes;
+  int64_t n_down = 0, n_up = 0;
+  for (int j = 0; j < m; ++j) {
+    const FwdIn& p = in[active[j]];
+    float* upart = reinterpret_cast<float*>(ws + off);
+    off += fwd_site_bytes(p.M, p.K, R);
+    DownSite& d = dargs.s[j];
+    UpSite& q = uargs.s[j];
+    if (!make_map(&d.in, p.x, false, p.M, p.K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&d.w, p.a, false, R, p.K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&q.a, p.u, false, p.M, R, RP, 128, swizzle_for_span(span)) ||
+        !make_map(&q.b, p.b, false, p.N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
+        !(y_bf16 ? make_map(&q.out, p.delta_y, false, p.M, p.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
+                 : make_map(&q.out, p.delta_y, true, p.M, p.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return LORA_ERR_CUDA;
+    d.part = upart;
+    d.M = int(p.M);
+    d.Kred = int(p.K);
+    d.alpha = 1.0f;
+    q.part = upart;
+    q.out_bf16 = static_cast<__nv_bfloat16*>(p.u);
+    q.S = int(ceil_div(p.K, down_slice(RP)));
+    q.M = int(p.M);
+    q.Nout = int(p.N);
+    q.alpha = p.alpha;
+    n_down += down_units(p.M, p.K, RP);
+    n_up += up_units(p.M, p.N, RP);
+  }
   Recorder rec(st);
   rec.mark();
-  if (launch_down(RP, false, m_x, m_a, upart, int(M), int(K), 1.0f, status, grid_for(down_units(M, K, RP), nsm), st) !=
-      cudaSuccess)
-    return LORA_ERR_CUDA;
+  if (launch_down(RP, false, dargs, status, grid_for(n_down, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   // U = bf16(tree over the K-slice partials), built inside the up-projection, which also writes u
-  if (launch_up(RP, false, y_bf16, m_u, m_b, m_y, upart, int(ceil_div(K, down_slice(RP))), u, int(R), int(M), int(N),
-                alpha, status, grid_for(up_units(M, N, RP), nsm), st) != cudaSuccess)
-    return LORA_ERR_CUDA;
+  if (launch_up(RP, false, y_bf16, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+  rec.mark();
+  return LORA_OK;
+}
+
+// The backward of every site: R <= 16: dy, dX (+ du), dA, combine; larger ranks: dU, dB, dX
+// (+ du), dA, combine; each launch covers all sites' units.
+lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
+  int active[kMaxSites], m = 0;
+  lora_status s = check_sites(in, n, R, workspace, workspace_bytes, BwdPtrs{}, active, &m);
+  if (s != LORA_OK || m == 0) return s;
+  if (workspace_bytes < bwd_need(in, n, R)) return LORA_ERR_WORKSPACE;
+  int nsm = 0;
+  if ((s = device_ready(&nsm)) != LORA_OK) return s;
+
+  const int RP = padded_rank(int(R));
+  const int span = RP * 2;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  DyArgs yargs{};
+  DownArgs dargs{};
+  WgArgs bargs{}, aargs{};
+  UpArgs uargs{};
+  CombineJobs jobs{};
+  yargs.n = dargs.n = bargs.n = aargs.n = uargs.n = m;
+  uargs.R = int(R);
+  jobs.n = 2 * m;
+  size_t off = kStatusBytes;
+  int64_t n_dy = 0, n_du = 0, n_db = 0, n_up = 0, n_da = 0;
+  for (int j = 0; j < m; ++j) {
+    const BwdIn& p = in[active[j]];
+    const BwdLayout L = bwd_layout(p.M, p.K, p.N, R);
+    float* dupart = reinterpret_cast<float*>(ws + off + (L.dupart - kStatusBytes));
+    float* dbpart = reinterpret_cast<float*>(ws + off + (L.dbpart - kStatusBytes));
+    float* dapart = reinterpret_cast<float*>(ws + off + (L.dapart - kStatusBytes));
+    off += bwd_site_bytes(p.M, p.K, p.N, R);
+    const int M = int(p.M), K = int(p.K), N = int(p.N);
+    const int C = int(ceil_div(p.M, kWgradChunk));
+    UpSite& q = uargs.s[j];
+    WgSite& wa = aargs.s[j];
+    if (!make_map(&q.a, p.du, false, M, R, RP, 128, swizzle_for_span(span)) ||
+        !make_map(&q.b, p.a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&q.out, p.dx, true, M, K, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&wa.in, p.x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&wa.g, p.du, false, M, R, RP, 64, swizzle_for_span(span)))
+      return LORA_ERR_CUDA;
+    if (RP == 16) {
+      DySite& y = yargs.s[j];
+      if (!make_map(&y.dy, p.dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+          !make_map(&y.b, p.b, false, N, R, RP, 128, swizzle_for_span(span)) ||
+          !make_map(&y.u, p.u, false, M, R, RP, 128, swizzle_for_span(span)))
+        return LORA_ERR_CUDA;
+      y.du_part = dupart;
+      y.db_part = dbpart;
+      y.M = M;
+      y.N = N;
+      y.alpha = p.alpha;
+      n_dy += ceil_div(M, kDyChunk) * ceil_div(N, kDySlice);
+    } else {
+      DownSite& d = dargs.s[j];
+      WgSite& wb = bargs.s[j];
+      if (!make_map(&d.in, p.dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+          !make_map(&d.w, p.b, false, N, R, RP, 64, swizzle_for_span(span)) ||
+          !make_map(&wb.in, p.dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_map(&wb.g, p.u, false, M, R, RP, 64, swizzle_for_span(span)))
+        return LORA_ERR_CUDA;
+      d.part = dupart;
+      d.M = M;
+      d.Kred = N;
+      d.alpha = p.alpha;
+      wb.part = dbpart;
+      wb.M = M;
+      wb.Cw = N;
+      wb.alpha = p.alpha;
+      n_du += down_units(M, N, RP);
+      n_db += wgrad_units(M, N, RP);
+    }
+    q.part = dupart;
+    q.out_bf16 = static_cast<__nv_bfloat16*>(p.du);
+    q.S = int(ceil_div(N, du_slice(RP)));
+    q.M = M;
+    q.Nout = K;
+    q.alpha = 1.0f;
+    wa.part = dapart;
+    wa.M = M;
+    wa.Cw = K;
+    wa.alpha = 1.0f;
+    jobs.j[2 * j] = CombineJob{dapart, p.da, C, K, int(R), RP, 0};
+    jobs.j[2 * j + 1] = CombineJob{dbpart, p.db, C, N, int(R), RP, 1};
+    n_up += up_units(M, K, RP);
+    n_da += wgrad_units(M, K, RP);
+  }
+  Recorder rec(st);
+  rec.mark();
+  if (RP == 16) {
+    // one pass over dY: dU partials over 512-column slices, dB partials over 256-row chunks
+    if (launch_dy(yargs, status, grid_for(n_dy, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+    rec.mark();
+  } else {
+    // dU partials over slices of N (dV formed in shared memory)
+    if (launch_down(RP, true, dargs, status, grid_for(n_du, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+    rec.mark();
+    // dB chunk partials over 256-row chunks of M
+    if (launch_wgrad(RP, true, bargs, status, grid_for(n_db, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+    rec.mark();
+  }
+  // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
+  if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+  rec.mark();
+  if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+  rec.mark();
+  // dA and dB: canonical tree over the chunk partials
+  if (launch_combine(jobs, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   return LORA_OK;
 }
 }  // namespace
 
+extern "C" {
+
 lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K, int64_t N,
                            int64_t R, float* delta_y, void* u, void* workspace, size_t workspace_bytes,
                            void* stream) {
-  return fwd_impl(x, a, b, alpha, M, K, N, R, delta_y, false, u, workspace, workspace_bytes, stream);
+  const FwdIn in{x, a, b, alpha, M, K, N, delta_y, u};
+  return fwd_group(&in, 1, R, false, workspace, workspace_bytes, stream);
 }
 
 lora_status lora_delta_fwd_bf16(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K,
                                 int64_t N, int64_t R, void* delta_y, void* u, void* workspace, size_t workspace_bytes,
                                 void* stream) {
-  return fwd_impl(x, a, b, alpha, M, K, N, R, delta_y, true, u, workspace, workspace_bytes, stream);
+  const FwdIn in{x, a, b, alpha, M, K, N, delta_y, u};
+  return fwd_group(&in, 1, R, true, workspace, workspace_bytes, stream);
 }
 
 lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const void* b, const void* u, float alpha,
                            int64_t M, int64_t K, int64_t N, int64_t R, float* dx, float* da, float* db, void* du,
                            void* workspace, size_t workspace_bytes, void* stream) {
-  lora_status s = check_shape(M, K, N, R);
-  if (s != LORA_OK) return s;
-  if (M == 0) return LORA_OK;
-  if (!dy || !x || !a || !b || !u || !dx || !da || !db || !du || !workspace) return LORA_ERR_NULL;
-  for (const void* p : {dy, x, a, b, u, static_cast<const void*>(dx), static_cast<const void*>(da),
-                        static_cast<const void*>(db), static_cast<const void*>(du), static_cast<const void*>(workspace)})
-    if (!aligned16(p)) return LORA_ERR_ALIGN;
-  const BwdLayout L = bwd_layout(M, K, N, R);
-  if (workspace_bytes < L.total) return LORA_ERR_WORKSPACE;
-  int nsm = 0;
-  if ((s = device_ready(&nsm)) != LORA_OK) return s;
+  const BwdIn in{dy, x, a, b, u, alpha, M, K, N, dx, da, db, du};
+  return bwd_group(&in, 1, R, workspace, workspace_bytes, stream);
+}
 
-  const int RP = padded_rank(int(R));
-  const int span = RP * 2;
-  CUtensorMap m_dy_rows, m_b_rows, m_dy_chunk, m_u_chunk, m_a, m_dx, m_x_chunk, m_du_chunk, m_b_128, m_u_128, m_du_128;
-  if (!make_map(&m_dy_rows, dy, false, M, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&m_b_rows, b, false, N, R, RP, 64, swizzle_for_span(span)) ||
-      !make_map(&m_dy_chunk, dy, false, M, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_u_chunk, u, false, M, R, RP, 64, swizzle_for_span(span)) ||
-      !make_map(&m_a, a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_dx, dx, true, M, K, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_x_chunk, x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m_du_chunk, du, false, M, R, RP, 64, swizzle_for_span(span)) ||
-      !make_map(&m_b_128, b, false, N, R, RP, 128, swizzle_for_span(span)) ||
-      !make_map(&m_u_128, u, false, M, R, RP, 128, swizzle_for_span(span)) ||
-      !make_map(&m_du_128, du, false, M, R, RP, 128, swizzle_for_span(span)))
-    return LORA_ERR_CUDA;
-
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  float* dupart = reinterpret_cast<float*>(ws + L.dupart);
-  float* dbpart = reinterpret_cast<float*>(ws + L.dbpart);
-  float* dapart = reinterpret_cast<float*>(ws + L.dapart);
-  const int S = int(ceil_div(N, du_slice(RP)));
-  const int C = int(ceil_div(M, kWgradChunk));
-  Recorder rec(st);
-  rec.mark();
-  if (RP == 16) {
-    // one pass over dY: dU partials over 512-column slices, dB partials over 256-row chunks
-    if (launch_dy(m_dy_rows, m_b_128, m_u_128, dupart, dbpart, int(M), int(N), alpha, status,
-                  grid_for(ceil_div(M, kDyChunk) * ceil_div(N, kDySlice), nsm), st) != cudaSuccess)
-      return LORA_ERR_CUDA;
-    rec.mark();
-  } else {
-    // dU partials over slices of N (dV formed in shared memory)
-    if (launch_down(RP, true, m_dy_rows, m_b_rows, dupart, int(M), int(N), alpha, status,
-                    grid_for(down_units(M, N, RP), nsm), st) != cudaSuccess)
-      return LORA_ERR_CUDA;
-    rec.mark();
-    // dB chunk partials over 256-row chunks of M
-    if (launch_wgrad(RP, true, m_dy_chunk, m_u_chunk, dbpart, int(M), int(N), alpha, status,
-                     grid_for(wgrad_units(M, N, RP), nsm), st) != cudaSuccess)
-      return LORA_ERR_CUDA;
-    rec.mark();
+size_t lora_delta_fwd_grouped_workspace_size(const lora_fwd_site* sites, int count, int64_t R) {
+  if (!sites || count < 1 || count > kMaxSites) return 0;
+  size_t t = kStatusBytes;
+  for (int i = 0; i < count; ++i) {
+    if (check_shape(sites[i].M, sites[i].K, sites[i].N, R) != LORA_OK) return 0;
+    t += fwd_site_bytes(sites[i].M, sites[i].K, R);
   }
-  // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
-  if (launch_up(RP, true, false, m_du_128, m_a, m_dx, dupart, S, du, int(R), int(M), int(K), 1.0f, status,
-                grid_for(up_units(M, K, RP), nsm), st) != cudaSuccess)
-    return LORA_ERR_CUDA;
-  rec.mark();
-  if (launch_wgrad(RP, false, m_x_chunk, m_du_chunk, dapart, int(M), int(K), 1.0f, status,
-                   grid_for(wgrad_units(M, K, RP), nsm), st) != cudaSuccess)
-    return LORA_ERR_CUDA;
-  rec.mark();
-  // dA and dB: canonical tree over the chunk partials
-  CombineJob jobs[2] = {{dapart, da, C, int(K), int(R), RP, 0}, {dbpart, db, C, int(N), int(R), RP, 1}};
-  if (launch_combine(jobs, 2, st) != cudaSuccess) return LORA_ERR_CUDA;
-  rec.mark();
-  return LORA_OK;
+  return t;
+}
+
+size_t lora_delta_bwd_grouped_workspace_size(const lora_bwd_site* sites, int count, int64_t R) {
+  if (!sites || count < 1 || count > kMaxSites) return 0;
+  size_t t = kStatusBytes;
+  for (int i = 0; i < count; ++i) {
+    if (check_shape(sites[i].M, sites[i].K, sites[i].N, R) != LORA_OK) return 0;
+    t += bwd_site_bytes(sites[i].M, sites[i].K, sites[i].N, R);
+  }
+  return t;
+}
+
+lora_status lora_delta_fwd_grouped(const lora_fwd_site* sites, int count, int64_t R, int y_bf16, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!sites) return LORA_ERR_NULL;
+  if (count < 1 || count > kMaxSites) return LORA_ERR_SHAPE;
+  FwdIn in[kMaxSites];
+  for (int i = 0; i < count; ++i)
+    in[i] = FwdIn{sites[i].x, sites[i].a, sites[i].b, sites[i].alpha, sites[i].M, sites[i].K, sites[i].N,
+                  sites[i].delta_y, sites[i].u};
+  return fwd_group(in, count, R, y_bf16 != 0, workspace, workspace_bytes, stream);
+}
+
+lora_status lora_delta_bwd_grouped(const lora_bwd_site* sites, int count, int64_t R, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!sites) return LORA_ERR_NULL;
+  if (count < 1 || count > kMaxSites) return LORA_ERR_SHAPE;
+  BwdIn in[kMaxSites];
+  for (int i = 0; i < count; ++i)
+    in[i] = BwdIn{sites[i].dy, sites[i].x, sites[i].a, sites[i].b, sites[i].u, sites[i].alpha, sites[i].M,
+                  sites[i].K, sites[i].N, sites[i].dx, sites[i].da, sites[i].db, sites[i].du};
+  return bwd_group(in, count, R, workspace, workspace_bytes, stream);
 }
 
 lora_status lora_delta_device_status(const void* workspace, int* code) {

@@ -54,10 +54,13 @@ __device__ __forceinline__ float4 canonical_strided4(const float* __restrict__ p
   return r;
 }
 
-__global__ void __launch_bounds__(256) combine_kernel(CombineJob j0, CombineJob j1, int P) {
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineJobs jobs) {
   grid_dependency_wait();
   grid_dependents_launch();
-  const CombineJob& j = blockIdx.z == 0 ? j0 : j1;
+  const CombineJob& j = jobs.j[blockIdx.z];
+  // chunks per warp: the smallest power of two with 8 * P >= C (warp blocks stay power-of-two aligned)
+  int P = 1;
+  while (8 * P < j.C) P *= 2;
   const int r = blockIdx.y;
   const int col0 = blockIdx.x * 128;
   if (r >= j.R || col0 >= j.cols) return;                // uniform over the block
@@ -88,20 +91,17 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineJob j0, CombineJob 
   }
 }
 
-cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st) {
-  if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+cudaError_t launch_combine(const CombineJobs& jobs, cudaStream_t st) {
+  if (jobs.n < 1 || jobs.n > 2 * kMaxSites) return cudaErrorInvalidValue;
   int cmax = 0, colmax = 0, rmax = 0;
-  for (int i = 0; i < njobs; ++i) {
-    cmax = std::max(cmax, jobs[i].C);
-    colmax = std::max(colmax, jobs[i].cols);
-    rmax = std::max(rmax, jobs[i].R);
+  for (int i = 0; i < jobs.n; ++i) {
+    cmax = std::max(cmax, jobs.j[i].C);
+    colmax = std::max(colmax, jobs.j[i].cols);
+    rmax = std::max(rmax, jobs.j[i].R);
   }
   if (cmax == 0 || colmax == 0) return cudaSuccess;
-  // chunks per warp: the smallest power of two with 8 * P >= C (warp blocks stay power-of-two aligned)
-  int P = 1;
-  while (8 * P < cmax) P *= 2;
-  const dim3 grid(unsigned((colmax + 127) / 128), unsigned(rmax), unsigned(njobs));
-  return launch_pdl(combine_kernel, grid, dim3(256), 0, st, jobs[0], njobs > 1 ? jobs[1] : jobs[0], P);
+  const dim3 grid(unsigned((colmax + 127) / 128), unsigned(rmax), unsigned(jobs.n));
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, st, jobs);
 }
 
 }  // namespace lora

@@ -52,11 +52,19 @@ struct DownCfg {
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
 
-template <int RP, bool DV>
+// GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
+template <int RP, bool DV, bool GR>
 __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
-    down_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_w,
-                float* __restrict__ part, int M, int Kred, int n_mt, int n_sl, float alpha, uint32_t* status) {
+    down_kernel(const __grid_constant__ Sites<DownSite, GR ? kMaxSites : 1> args, uint32_t* status) {
   using C = DownCfg<RP, DV>;
+  // site of unit u (sites are few and ordered by first unit)
+  auto site = [&](int u) -> const DownSite& {
+    if constexpr (!GR) return args.s[0];
+    int i = 0;
+    while (i + 1 < args.n && u >= args.s[i + 1].u0) ++i;
+    return args.s[i];
+  };
+  const int total = args.total;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;                      // 1024-byte aligned tiles
@@ -85,8 +93,10 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0u;
     mbar_fence_init();
-    prefetch_map(&tm_in);
-    prefetch_map(&tm_w);
+    for (int i = 0; i < (GR ? args.n : 1); ++i) {
+      prefetch_map(&args.s[i].in);
+      prefetch_map(&args.s[i].w);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -96,19 +106,20 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (threadIdx.x == 0 && int(blockIdx.x) < n_mt * n_sl) {
+  if (threadIdx.x == 0 && int(blockIdx.x) < total) {
     // the first input tiles of this CTA's first unit, into L2 while the predecessor drains
-    const int mt = int(blockIdx.x) % n_mt, k0 = (int(blockIdx.x) / n_mt) * C::kSlice;
-    const int nkb = min((min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK, C::kPrefetch);
+    const DownSite& S = site(blockIdx.x);
+    const int lu = int(blockIdx.x) - S.u0;
+    const int mt = lu % S.n_mt, k0 = (lu / S.n_mt) * C::kSlice;
+    const int nkb = min((min(S.Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK, C::kPrefetch);
     for (int kb = 0; kb < nkb; ++kb) {
-      tma_prefetch_l2(&tm_in, k0 + kb * C::kBK, mt * C::kBM);
-      tma_prefetch_l2(&tm_in, k0 + kb * C::kBK + 32, mt * C::kBM);
+      tma_prefetch_l2(&S.in, k0 + kb * C::kBK, mt * C::kBM);
+      tma_prefetch_l2(&S.in, k0 + kb * C::kBK + 32, mt * C::kBM);
     }
   }
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
   const Abort ab{abort_flag, status};
-  const int total = n_mt * n_sl;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -117,18 +128,20 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
       Ring r;
       uint32_t issued = 0, parities = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int mt = u % n_mt, sl = u / n_mt;
+        const DownSite& S = site(u);
+        const int lu = u - S.u0;
+        const int mt = lu % S.n_mt, sl = lu / S.n_mt;
         const int k0 = sl * C::kSlice;
-        const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+        const int nkb = (min(S.Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (wait(empty(r.idx), r.phase ^ 1u, ab, 1)) {
             const uint32_t st = base + r.idx * C::kStageBytes;
             const int k = k0 + kb * C::kBK;
             mbar_expect_tx(full(r.idx), C::kStageBytes);
-            tma_load(st, &tm_in, full(r.idx), k, mt * C::kBM, pol_stream);                     // k .. k+31
-            tma_load(st + C::kSlabBytes, &tm_in, full(r.idx), k + 32, mt * C::kBM, pol_stream);  // k+32 .. k+63
-            if (DV) tma_load(st + C::kInBytes, &tm_w, full(r.idx), 0, k, pol_keep);   // b[n][r], n = k..k+63
-            else tma_load(st + C::kInBytes, &tm_w, full(r.idx), k, 0, pol_keep);      // a[r][k..k+63]
+            tma_load(st, &S.in, full(r.idx), k, mt * C::kBM, pol_stream);                     // k .. k+31
+            tma_load(st + C::kSlabBytes, &S.in, full(r.idx), k + 32, mt * C::kBM, pol_stream);  // k+32 .. k+63
+            if (DV) tma_load(st + C::kInBytes, &S.w, full(r.idx), 0, k, pol_keep);   // b[n][r], n = k..k+63
+            else tma_load(st + C::kInBytes, &S.w, full(r.idx), k, 0, pol_keep);      // a[r][k..k+63]
             issued |= 1u << r.idx;
             parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
           }
@@ -158,9 +171,10 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
     }
     Ring r, g;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int sl = u / n_mt;
+      const DownSite& S = site(u);
+      const int sl = (u - S.u0) / S.n_mt;
       const int k0 = sl * C::kSlice;
-      const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+      const int nkb = (min(S.Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
       for (int kb = 0; kb < nkb; ++kb) {
         bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 3);
         ok = __all_sync(0xffffffffu, ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 4));
@@ -191,9 +205,11 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
     const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + h * C::kCPT;
     Ring g;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int mt = u % n_mt, sl = u / n_mt;
+      const DownSite& S = site(u);
+      const int lu = u - S.u0;
+      const int mt = lu % S.n_mt, sl = lu / S.n_mt;
       const int k0 = sl * C::kSlice;
-      const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+      const int nkb = (min(S.Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
       float stack[C::kLevels > 0 ? C::kLevels : 1][C::kCPT];
       float node[C::kCPT];
       bool ok_all = true;
@@ -252,8 +268,9 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
       }
       // after the last group (i = kGS - 1, all ones) `node` holds the slice sum
       const int row = mt * C::kBM + q * 32 + lane;
-      if (ok_all && row < M) {
-        float4* dst = reinterpret_cast<float4*>(part + (size_t(sl) * M + row) * RP + h * C::kCPT);
+      if (ok_all && row < S.M) {
+        float* __restrict__ part = S.part;
+        float4* dst = reinterpret_cast<float4*>(part + (size_t(sl) * S.M + row) * RP + h * C::kCPT);
 #pragma unroll
         for (int c = 0; c < C::kCPT; c += 4) dst[c / 4] = make_float4(node[c], node[c + 1], node[c + 2], node[c + 3]);
       }
@@ -261,12 +278,14 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
   } else {
     // ---------------------------------------------------- dV = bf16(dY*alpha)
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);   // 0..127
-    const uint32_t a2 = pow2_bf16x2(alpha);
     Ring r;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int sl = u / n_mt;
+      const DownSite& S = site(u);
+      const float alpha = S.alpha;
+      const uint32_t a2 = pow2_bf16x2(alpha);
+      const int sl = (u - S.u0) / S.n_mt;
       const int k0 = sl * C::kSlice;
-      const int nkb = (min(Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
+      const int nkb = (min(S.Kred - k0, C::kSlice) + C::kBK - 1) / C::kBK;
       for (int kb = 0; kb < nkb; ++kb) {
         if (wait(full(r.idx), r.phase, ab, 7)) {
           uint4* tile = reinterpret_cast<uint4*>(smem_raw + (base - raw) + size_t(r.idx) * C::kStageBytes);
@@ -289,31 +308,48 @@ __global__ void __launch_bounds__(DownCfg<RP, DV>::kThreads, 1)
   }
 }
 
-template <int RP, bool DV>
-static cudaError_t launch_one(const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred, float alpha,
-                              uint32_t* status, int grid, cudaStream_t st) {
+template <int RP, bool DV, bool GR>
+static cudaError_t launch_one(DownArgs& args, uint32_t* status, int grid, cudaStream_t st) {
   using C = DownCfg<RP, DV>;
-  const int n_mt = int(ceil_div(M, C::kBM)), n_sl = int(ceil_div(Kred, C::kSlice));
-  return launch_pdl(down_kernel<RP, DV>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
-                    in, w, part, M, Kred, n_mt, n_sl, alpha, status);
+  int u0 = 0;
+  for (int i = 0; i < args.n; ++i) {
+    DownSite& s = args.s[i];
+    s.n_mt = int(ceil_div(s.M, C::kBM));
+    s.n_sl = int(ceil_div(s.Kred, C::kSlice));
+    s.u0 = u0;
+    u0 += s.n_mt * s.n_sl;
+  }
+  args.total = u0;
+  if constexpr (GR) return launch_pdl(down_kernel<RP, DV, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, args, status);
+  else return launch_pdl(down_kernel<RP, DV, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, first_site(args), status);
 }
 
-cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
-                        float alpha, uint32_t* status, int grid, cudaStream_t st) {
-  switch (RP * 2 + (dv ? 1 : 0)) {
-    case 32: return launch_one<16, false>(in, w, part, M, Kred, alpha, status, grid, st);
-    case 33: return launch_one<16, true>(in, w, part, M, Kred, alpha, status, grid, st);
-    case 64: return launch_one<32, false>(in, w, part, M, Kred, alpha, status, grid, st);
-    case 65: return launch_one<32, true>(in, w, part, M, Kred, alpha, status, grid, st);
-    case 128: return launch_one<64, false>(in, w, part, M, Kred, alpha, status, grid, st);
-    case 129: return launch_one<64, true>(in, w, part, M, Kred, alpha, status, grid, st);
+cudaError_t launch_down(int RP, bool dv, DownArgs& args, uint32_t* status, int grid, cudaStream_t st) {
+  if (args.n < 1 || args.n > kMaxSites) return cudaErrorInvalidValue;
+  const bool gr = args.n > 1;
+  switch (RP * 4 + (dv ? 1 : 0) + (gr ? 2 : 0)) {
+    case 64: return launch_one<16, false, false>(args, status, grid, st);
+    case 65: return launch_one<16, true, false>(args, status, grid, st);
+    case 66: return launch_one<16, false, true>(args, status, grid, st);
+    case 67: return launch_one<16, true, true>(args, status, grid, st);
+    case 128: return launch_one<32, false, false>(args, status, grid, st);
+    case 129: return launch_one<32, true, false>(args, status, grid, st);
+    case 130: return launch_one<32, false, true>(args, status, grid, st);
+    case 131: return launch_one<32, true, true>(args, status, grid, st);
+    case 256: return launch_one<64, false, false>(args, status, grid, st);
+    case 257: return launch_one<64, true, false>(args, status, grid, st);
+    case 258: return launch_one<64, false, true>(args, status, grid, st);
+    case 259: return launch_one<64, true, true>(args, status, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int RP, bool DV>
 static cudaError_t prep_one() {
-  return cudaFuncSetAttribute(down_kernel<RP, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(down_kernel<RP, DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(DownCfg<RP, DV>::kSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(down_kernel<RP, DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(DownCfg<RP, DV>::kSmem));
 }
 

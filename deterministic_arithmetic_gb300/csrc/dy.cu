@@ -72,10 +72,17 @@ __device__ __forceinline__ void leaves4(uint32_t taddr, bool ok, float (&o)[8]) 
     o[c] = tree4(__uint_as_float(v[0][c]), __uint_as_float(v[1][c]), __uint_as_float(v[2][c]), __uint_as_float(v[3][c]));
 }
 
+// GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
+template <bool GR>
 __global__ void __launch_bounds__(DyCfg::kThreads, 1)
-    dy_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_b,
-              const __grid_constant__ CUtensorMap tm_u, float* __restrict__ du_part, float* __restrict__ db_part,
-              int M, int N, int n_sl, int n_ch, float alpha, uint32_t* status) {
+    dy_kernel(const __grid_constant__ Sites<DySite, GR ? kMaxSites : 1> args, uint32_t* status) {
+  // site of unit u (sites are few and ordered by first unit)
+  auto site = [&](int u) -> const DySite& {
+    if constexpr (!GR) return args.s[0];
+    int i = 0;
+    while (i + 1 < args.n && u >= args.s[i + 1].u0) ++i;
+    return args.s[i];
+  };
   using C = DyCfg;
   constexpr int RP = C::RP;
   extern __shared__ uint8_t smem_raw[];
@@ -107,9 +114,11 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0u;
     mbar_fence_init();
-    prefetch_map(&tm_dy);
-    prefetch_map(&tm_b);
-    prefetch_map(&tm_u);
+    for (int i = 0; i < (GR ? args.n : 1); ++i) {
+      prefetch_map(&args.s[i].dy);
+      prefetch_map(&args.s[i].b);
+      prefetch_map(&args.s[i].u);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -119,18 +128,19 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = n_sl * n_ch;
+  const int total = args.total;
   // valid column tiles of a slice and row tiles of a chunk (ragged N and M)
-  auto n_tiles = [&](int sl) { return (min(N - sl * kDySlice, kDySlice) + C::kBN - 1) / C::kBN; };
-  auto r_tiles = [&](int ch) { return (min(M - ch * kDyChunk, kDyChunk) + C::kBM - 1) / C::kBM; };
+  auto n_tiles = [&](const DySite& P, int sl) { return (min(P.N - sl * kDySlice, kDySlice) + C::kBN - 1) / C::kBN; };
+  auto r_tiles = [&](const DySite& P, int ch) { return (min(P.M - ch * kDyChunk, kDyChunk) + C::kBM - 1) / C::kBM; };
   if (threadIdx.x == 0 && int(blockIdx.x) < total) {
     // the first dY tiles of this CTA's first unit, into L2 while the predecessor drains
-    const int sl = int(blockIdx.x) % n_sl, ch = int(blockIdx.x) / n_sl;
-    const int nnt = n_tiles(sl), nrt = r_tiles(ch);
+    const DySite& P = site(blockIdx.x);
+    const int sl = (int(blockIdx.x) - P.u0) % P.n_sl, ch = (int(blockIdx.x) - P.u0) / P.n_sl;
+    const int nnt = n_tiles(P, sl), nrt = r_tiles(P, ch);
     int n = 0;
     for (int i = 0; i < nnt && n < C::kPrefetch; ++i)
       for (int j = 0; j < nrt && n < C::kPrefetch; ++j, ++n)
-        for (int q = 0; q < 4; ++q) tma_prefetch_l2(&tm_dy, sl * kDySlice + i * C::kBN + 32 * q, ch * kDyChunk + j * C::kBM);
+        for (int q = 0; q < 4; ++q) tma_prefetch_l2(&P.dy, sl * kDySlice + i * C::kBN + 32 * q, ch * kDyChunk + j * C::kBM);
   }
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
@@ -143,8 +153,9 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
       Ring r;
       uint32_t issued = 0, parities = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int sl = u % n_sl, ch = u / n_sl;
-        const int nnt = n_tiles(sl), nrt = r_tiles(ch);
+        const DySite& P = site(u);
+        const int sl = (u - P.u0) % P.n_sl, ch = (u - P.u0) / P.n_sl;
+        const int nnt = n_tiles(P, sl), nrt = r_tiles(P, ch);
         for (int i = 0; i < nnt; ++i)
           for (int j = 0; j < nrt; ++j) {
             if (wait(empty(r.idx), r.phase ^ 1u, ab, 31)) {
@@ -153,9 +164,9 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
               mbar_expect_tx(full(r.idx), C::kStageBytes);
 #pragma unroll
               for (int q = 0; q < 4; ++q)                                       // dy[m0..+127][n0+32q..+31]
-                tma_load(st + q * C::kSlabBytes, &tm_dy, full(r.idx), n0 + 32 * q, m0, pol_stream);
-              tma_load(st + C::kTileBytes, &tm_b, full(r.idx), 0, n0, pol_keep);               // b[n0..+127][.]
-              tma_load(st + C::kTileBytes + C::kWBytes, &tm_u, full(r.idx), 0, m0, pol_keep);  // u[m0..+127][.]
+                tma_load(st + q * C::kSlabBytes, &P.dy, full(r.idx), n0 + 32 * q, m0, pol_stream);
+              tma_load(st + C::kTileBytes, &P.b, full(r.idx), 0, n0, pol_keep);               // b[n0..+127][.]
+              tma_load(st + C::kTileBytes + C::kWBytes, &P.u, full(r.idx), 0, m0, pol_keep);  // u[m0..+127][.]
               issued |= 1u << r.idx;
               parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
             }
@@ -185,8 +196,9 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
     }
     Ring r, g;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int sl = u % n_sl, ch = u / n_sl;
-      const int nstages = n_tiles(sl) * r_tiles(ch);
+      const DySite& P = site(u);
+      const int sl = (u - P.u0) % P.n_sl, ch = (u - P.u0) / P.n_sl;
+      const int nstages = n_tiles(P, sl) * r_tiles(P, ch);
       for (int k = 0; k < nstages; ++k) {
         bool ok = wait(ready(r.idx), r.phase, ab, 33);
         ok = __all_sync(0xffffffffu, ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 34));
@@ -222,8 +234,12 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
     const int tr = q * 32 + lane;                         // TMEM lane: row (dU) or column (dB) within the tile
     Ring g;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int sl = u % n_sl, ch = u / n_sl;
-      const int nnt = n_tiles(sl), nrt = r_tiles(ch);
+      const DySite& P = site(u);
+      const int sl = (u - P.u0) % P.n_sl, ch = (u - P.u0) / P.n_sl;
+      const int nnt = n_tiles(P, sl), nrt = r_tiles(P, ch);
+      const int M = P.M, N = P.N;
+      float* __restrict__ du_part = P.du_part;
+      float* __restrict__ db_part = P.db_part;
       float du_stk[C::kChunkTiles][2][C::kCPT];           // per row tile: canonical-tree stack over column tiles
       float db_first[C::kCPT];
       bool ok_all = true;
@@ -293,11 +309,13 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   } else {
     // ---------------------------------------------------- dV = bf16(dY*alpha)
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
-    const uint32_t a2 = pow2_bf16x2(alpha);
     Ring r;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int sl = u % n_sl, ch = u / n_sl;
-      const int nstages = n_tiles(sl) * r_tiles(ch);
+      const DySite& P = site(u);
+      const float alpha = P.alpha;
+      const uint32_t a2 = pow2_bf16x2(alpha);
+      const int sl = (u - P.u0) % P.n_sl, ch = (u - P.u0) / P.n_sl;
+      const int nstages = n_tiles(P, sl) * r_tiles(P, ch);
       for (int k = 0; k < nstages; ++k) {
         if (wait(full(r.idx), r.phase, ab, 37)) {
           uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kStageBytes);
@@ -321,15 +339,26 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   }
 }
 
-cudaError_t launch_dy(const CUtensorMap& dy, const CUtensorMap& b, const CUtensorMap& u, float* du_part,
-                      float* db_part, int M, int N, float alpha, uint32_t* status, int grid, cudaStream_t st) {
-  const int n_sl = int(ceil_div(N, kDySlice)), n_ch = int(ceil_div(M, kDyChunk));
-  return launch_pdl(dy_kernel, dim3(grid), dim3(DyCfg::kThreads), DyCfg::kSmem, st, dy, b, u, du_part, db_part, M, N,
-                    n_sl, n_ch, alpha, status);
+cudaError_t launch_dy(DyArgs& args, uint32_t* status, int grid, cudaStream_t st) {
+  if (args.n < 1 || args.n > kMaxSites) return cudaErrorInvalidValue;
+  int u0 = 0;
+  for (int i = 0; i < args.n; ++i) {
+    DySite& s = args.s[i];
+    s.n_sl = int(ceil_div(s.N, kDySlice));
+    s.n_ch = int(ceil_div(s.M, kDyChunk));
+    s.u0 = u0;
+    u0 += s.n_sl * s.n_ch;
+  }
+  args.total = u0;
+  if (args.n > 1) return launch_pdl(dy_kernel<true>, dim3(grid), dim3(DyCfg::kThreads), DyCfg::kSmem, st, args, status);
+  return launch_pdl(dy_kernel<false>, dim3(grid), dim3(DyCfg::kThreads), DyCfg::kSmem, st, first_site(args), status);
 }
 
 cudaError_t prepare_dy() {
-  return cudaFuncSetAttribute(dy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(DyCfg::kSmem));
+  const cudaError_t e =
+      cudaFuncSetAttribute(dy_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(DyCfg::kSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dy_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(DyCfg::kSmem));
 }
 
 }  // namespace lora

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +29,69 @@ constexpr int du_slice(int RP) { return RP == 16 ? kDySlice : down_slice(RP); }
 constexpr int up_bn(int RP) { return 256 / (RP / 16); }
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Grouped launches: every kernel takes a table of up to kMaxSites independent
+// problems ("sites", e.g. the fc1 and fc2 LoRA insertion points of one MLP),
+// all of the same padded rank, and deals their work units out as one unit
+// space: site i owns units [u0, u0 + its unit count). A single-site call is a
+// table of one. The table is a __grid_constant__ kernel parameter, so its
+// tensor maps stay in parameter space (what TMA needs) when indexed by site.
+constexpr int kMaxSites = 4;
+// A table of NS sites (NS = kMaxSites for grouped launches, 1 otherwise: a
+// smaller parameter block per launch). R: the rank (up-projection only).
+template <class Site, int NS>
+struct Sites {
+  Site s[NS];
+  int n, total, R;
+};
+// The one-site table of a launch built as a kMaxSites table.
+template <class Site>
+inline Sites<Site, 1> first_site(const Sites<Site, kMaxSites>& a) {
+  Sites<Site, 1> b;
+  b.s[0] = a.s[0];
+  b.n = 1;
+  b.total = a.total;
+  b.R = a.R;
+  return b;
+}
+
+// Down-projection (U or, with dV, dU partials): reduction over Kred in slices.
+struct DownSite {
+  CUtensorMap in, w;   // input rows (X or dY, boxes 128 x 32) and weight (A [R][Kred] or B [Kred][R])
+  float* part;         // [n_sl][M][RP] slice partials
+  int M, Kred, n_mt, n_sl, u0;
+  float alpha;         // dV = bf16(dY * alpha) (dV launches)
+};
+using DownArgs = Sites<DownSite, kMaxSites>;
+
+// Up-projection (dY_lora, or dX) with the U / dU combine folded in.
+struct UpSite {
+  CUtensorMap a, b, out;   // u / du rows (box 128 x RP), weight (B rows or A columns), output
+  const float* part;       // [S][M][RP] slice partials of u / du
+  __nv_bfloat16* out_bf16; // u / du [M][R], written here
+  int S, M, Nout, n_mt, n_nt, u0;
+  float alpha;             // forward scale (1 for dX)
+};
+using UpArgs = Sites<UpSite, kMaxSites>;
+
+// Fused dU + dB pass over dY (R <= 16).
+struct DySite {
+  CUtensorMap dy, b, u;   // dY rows (boxes 128 x 32), b rows, u rows (boxes 128 x RP)
+  float* du_part;         // [n_sl][M][RP]
+  float* db_part;         // [n_ch][RP][N]
+  int M, N, n_sl, n_ch, u0;
+  float alpha;
+};
+using DyArgs = Sites<DySite, kMaxSites>;
+
+// Weight-gradient chunk partials (dA from X and du; dB from dY and u for R > 16).
+struct WgSite {
+  CUtensorMap in, g;      // wide operand (X or dY, boxes 64 x 64) and du / u rows (boxes 64 x RP)
+  float* part;            // [n_ch][RP][Cw]
+  int M, Cw, n_ct, n_ch, u0;
+  float alpha;            // dV = bf16(dY * alpha) (dB launches)
+};
+using WgArgs = Sites<WgSite, kMaxSites>;
 
 // Launch with programmatic stream serialization (the kernel calls
 // grid_dependency_wait() before its first global-memory access).
@@ -75,17 +139,16 @@ inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil
 
 // Launchers (return the launch error, if any). `status` is the device status
 // word; `grid` the number of persistent CTAs.
-cudaError_t launch_down(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& w, float* part, int M, int Kred,
-                        float alpha, uint32_t* status, int grid, cudaStream_t st);
-// up: a = u / du rows (box 128 x RP), written by the kernel itself in its first phase;
-// y_bf16 (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte swizzle.
-cudaError_t launch_up(int RP, bool dx, bool y_bf16, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
-                      const float* part, int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status,
-                      int grid, cudaStream_t st);
-cudaError_t launch_dy(const CUtensorMap& dy, const CUtensorMap& b, const CUtensorMap& u, float* du_part,
-                      float* db_part, int M, int N, float alpha, uint32_t* status, int grid, cudaStream_t st);
-cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int C,
-                         float alpha, uint32_t* status, int grid, cudaStream_t st);
+// args: sites filled in except n_mt, n_sl, u0 and total (set here)
+cudaError_t launch_down(int RP, bool dv, DownArgs& args, uint32_t* status, int grid, cudaStream_t st);
+// up: a = u / du rows (box 128 x RP), written by the kernel itself (prep warps); y_bf16
+// (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte swizzle. args: sites
+// filled in except n_mt, n_nt, u0 and total (set here).
+cudaError_t launch_up(int RP, bool dx, bool y_bf16, UpArgs& args, uint32_t* status, int grid, cudaStream_t st);
+// args: sites filled in except n_sl, n_ch, u0 and total (set here)
+cudaError_t launch_dy(DyArgs& args, uint32_t* status, int grid, cudaStream_t st);
+// args: sites filled in except n_ct, n_ch, u0 and total (set here)
+cudaError_t launch_wgrad(int RP, bool dv, WgArgs& args, uint32_t* status, int grid, cudaStream_t st);
 
 // Final combine of the weight-gradient chunk partials: canonical tree over
 // the C chunks, FP32 out. part is [C][RP][cols] (cols = K for dA, N for dB).
@@ -97,7 +160,11 @@ struct CombineJob {
   int R, RP;           // rank and padded rank
   int transpose;       // 0: out[R][cols] (dA); 1: out[cols][R] (dB)
 };
-cudaError_t launch_combine(const CombineJob* jobs, int njobs, cudaStream_t st);
+struct CombineJobs {
+  CombineJob j[2 * kMaxSites];   // dA and dB of every site
+  int n;
+};
+cudaError_t launch_combine(const CombineJobs& jobs, cudaStream_t st);
 
 // Raise the dynamic shared-memory limit of every kernel instance in a
 // translation unit (once per device, with that device current).

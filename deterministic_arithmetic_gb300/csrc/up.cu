@@ -73,13 +73,19 @@ struct UpCfg {
   static_assert(kBufs == 2, "double-buffered accumulators");
 };
 
-template <int RP, bool DX, bool YBF>
+// GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
+template <int RP, bool DX, bool YBF, bool GR>
 __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
-    up_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-              const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ part, int S,
-              __nv_bfloat16* __restrict__ out_bf16, int R, int M, int Nout, int n_mt, int n_nt, float alpha,
-              uint32_t* status, uint32_t* sync) {
+    up_kernel(const __grid_constant__ Sites<UpSite, GR ? kMaxSites : 1> args, uint32_t* status, uint32_t* sync) {
   using C = UpCfg<RP, DX>;
+  // site of unit u (sites are few and ordered by first unit)
+  auto site = [&](int u) -> const UpSite& {
+    if constexpr (!GR) return args.s[0];
+    int i = 0;
+    while (i + 1 < args.n && u >= args.s[i + 1].u0) ++i;
+    return args.s[i];
+  };
+  const int R = args.R;
   static_assert(!(DX && YBF), "BF16 output is the forward's");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -114,9 +120,11 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     mbar_init(gdone, 1);
     *abort_flag = 0u;
     mbar_fence_init();
-    prefetch_map(&tm_a);
-    prefetch_map(&tm_b);
-    prefetch_map(&tm_out);
+    for (int i = 0; i < (GR ? args.n : 1); ++i) {
+      prefetch_map(&args.s[i].a);
+      prefetch_map(&args.s[i].b);
+      prefetch_map(&args.s[i].out);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -129,7 +137,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
   const Abort ab{abort_flag, status};
-  const int total = n_mt * n_nt;
+  const int total = args.total;
 
 
   if (warp == 0) {
@@ -139,7 +147,8 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       Ring r;
       uint32_t issued = 0, parities = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int mt = u / n_nt, nt = u % n_nt;
+        const UpSite& P = site(u);
+        const int mt = (u - P.u0) / P.n_nt, nt = (u - P.u0) % P.n_nt;
         const int k = (u - int(blockIdx.x)) / int(gridDim.x);     // this CTA's k-th unit
         if (k == C::kLocal) {
           wait(gdone, 0u, ab, 16);           // the rows of later units come from every CTA's share
@@ -148,13 +157,13 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
         if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
           const uint32_t st = base + r.idx * C::kStageBytes;
           mbar_expect_tx(full(r.idx), k < C::kLocal ? C::kBBytes : C::kStageBytes);
-          if (k >= C::kLocal) tma_load(st, &tm_a, full(r.idx), 0, mt * C::kBM, pol);   // u / du rows of the tile
+          if (k >= C::kLocal) tma_load(st, &P.a, full(r.idx), 0, mt * C::kBM, pol);    // u / du rows of the tile
           if (DX) {
 #pragma unroll
             for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
-              tma_load(st + C::kABytes + i * (RP * 128), &tm_b, full(r.idx), nt * C::kBN + 64 * i, 0, pol);
+              tma_load(st + C::kABytes + i * (RP * 128), &P.b, full(r.idx), nt * C::kBN + 64 * i, 0, pol);
           } else {
-            tma_load(st + C::kABytes, &tm_b, full(r.idx), 0, nt * C::kBN, pol);    // b rows n..n+BN
+            tma_load(st + C::kABytes, &P.b, full(r.idx), 0, nt * C::kBN, pol);     // b rows n..n+BN
           }
           issued |= 1u << r.idx;
           parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
@@ -211,16 +220,19 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       // RP * 2 bytes, 16-byte chunks swizzled by the row's place in the 8-row swizzle atom);
       // all loads of a thread are issued before its first store
       constexpr int kItems = C::kLocal * C::kBM * (RP / 8) / (32 * C::kEpiWarps);
-      const size_t stride = size_t(M) * RP;
       uint4 v[kItems];
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {
         const int i = int(threadIdx.x) - 64 + j * 32 * C::kEpiWarps;
         const int k = i / (C::kBM * (RP / 8)), row = (i / (RP / 8)) % C::kBM, g = i % (RP / 8);
         const int u = int(blockIdx.x) + k * int(gridDim.x);
-        const int grow = (u / n_nt) * C::kBM + row;
-        v[j] = u < total && grow < M && g < R / 8 ? slices_to_bf16x8(part + size_t(grow) * RP + g * 8, stride, S)
-                                                   : make_uint4(0u, 0u, 0u, 0u);
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (u < total) {
+          const UpSite& P = site(u);
+          const int grow = ((u - P.u0) / P.n_nt) * C::kBM + row;
+          if (grow < P.M && g < R / 8)
+            v[j] = slices_to_bf16x8(P.part + size_t(grow) * RP + g * 8, size_t(P.M) * RP, P.S);
+        }
       }
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {
@@ -236,7 +248,10 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     int sidx = 0;
     Ring b;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int mt = u / n_nt, nt = u % n_nt;
+      const UpSite& P = site(u);
+      const int mt = (u - P.u0) / P.n_nt, nt = (u - P.u0) % P.n_nt;
+      const int M = P.M, Nout = P.Nout;
+      const float alpha = P.alpha;
       const bool ok = __all_sync(0xffffffffu, wait(tfull(b.idx), b.phase, ab, 15));
       tc_fence_after();
       // one TMEM round trip per group of kBoxes 32-column boxes (64 registers of leaves per round)
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
           for (int box = 0; box < C::kBoxes; ++box) {
             const int ncol = nt * C::kBN + col0 + box * C::kChunk;
             if (ok && row0 < M && ncol < Nout)
-              tma_store(&tm_out, my_stg + ((sidx + box) % C::kStg) * C::kStgBytes, ncol, row0, pol_out);
+              tma_store(&P.out, my_stg + ((sidx + box) % C::kStg) * C::kStgBytes, ncol, row0, pol_out);
             tma_store_commit();
           }
         }
@@ -329,12 +344,16 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     // the grid-wide barrier (cooperative launch: every CTA is resident); its wait overlaps the
     // first unit, whose rows the epilogue warps formed themselves.
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
-    const int r0 = int(int64_t(M) * blockIdx.x / gridDim.x), r1 = int(int64_t(M) * (blockIdx.x + 1) / gridDim.x);
-    const size_t stride = size_t(M) * RP;
-    for (int i = t; i < (r1 - r0) * (R / 8); i += 32 * C::kPrepWarps) {
-      const int row = r0 + i / (R / 8), g = i % (R / 8);
-      *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) =
-          slices_to_bf16x8(part + size_t(row) * RP + g * 8, stride, S);
+    for (int si = 0; si < (GR ? args.n : 1); ++si) {
+      const UpSite& P = args.s[si];
+      const int r0 = int(int64_t(P.M) * blockIdx.x / gridDim.x), r1 = int(int64_t(P.M) * (blockIdx.x + 1) / gridDim.x);
+      const float* __restrict__ part = P.part;
+      __nv_bfloat16* __restrict__ out_bf16 = P.out_bf16;
+      for (int i = t; i < (r1 - r0) * (R / 8); i += 32 * C::kPrepWarps) {
+        const int row = r0 + i / (R / 8), g = i % (R / 8);
+        *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) =
+            slices_to_bf16x8(part + size_t(row) * RP + g * 8, size_t(P.M) * RP, P.S);
+      }
     }
     __threadfence();
     named_bar(1, 32 * C::kPrepWarps);
@@ -354,37 +373,55 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   }
 }
 
-template <int RP, bool DX, bool YBF>
-static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const float* part,
-                              int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status, int grid,
-                              cudaStream_t st) {
+template <int RP, bool DX, bool YBF, bool GR>
+static cudaError_t launch_one(UpArgs& args, uint32_t* status, int grid, cudaStream_t st) {
   using C = UpCfg<RP, DX>;
-  const int n_mt = int(ceil_div(M, C::kBM)), n_nt = int(ceil_div(Nout, C::kBN));
-  return launch_pdl_coop(up_kernel<RP, DX, YBF>, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, out, part, S,
-                         static_cast<__nv_bfloat16*>(out_bf16), R, M, Nout, n_mt, n_nt, alpha, status, status + 1);
+  int u0 = 0;
+  for (int i = 0; i < args.n; ++i) {
+    UpSite& s = args.s[i];
+    s.n_mt = int(ceil_div(s.M, C::kBM));
+    s.n_nt = int(ceil_div(s.Nout, C::kBN));
+    s.u0 = u0;
+    u0 += s.n_mt * s.n_nt;
+  }
+  args.total = u0;
+  if constexpr (GR)
+    return launch_pdl_coop(up_kernel<RP, DX, YBF, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, args, status,
+                           status + 1);
+  else
+    return launch_pdl_coop(up_kernel<RP, DX, YBF, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, first_site(args),
+                           status, status + 1);
 }
 
-cudaError_t launch_up(int RP, bool dx, bool y_bf16, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
-                      const float* part, int S, void* out_bf16, int R, int M, int Nout, float alpha, uint32_t* status,
-                      int grid, cudaStream_t st) {
+template <int RP, bool DX, bool YBF>
+static cudaError_t launch_gr(UpArgs& args, uint32_t* status, int grid, cudaStream_t st) {
+  return args.n > 1 ? launch_one<RP, DX, YBF, true>(args, status, grid, st)
+                    : launch_one<RP, DX, YBF, false>(args, status, grid, st);
+}
+
+cudaError_t launch_up(int RP, bool dx, bool y_bf16, UpArgs& args, uint32_t* status, int grid, cudaStream_t st) {
   if (dx && y_bf16) return cudaErrorInvalidValue;
+  if (args.n < 1 || args.n > kMaxSites) return cudaErrorInvalidValue;
   switch (RP * 4 + (dx ? 1 : 0) + (y_bf16 ? 2 : 0)) {
-    case 64: return launch_one<16, false, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 65: return launch_one<16, true, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 66: return launch_one<16, false, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 128: return launch_one<32, false, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 129: return launch_one<32, true, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 130: return launch_one<32, false, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 256: return launch_one<64, false, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 257: return launch_one<64, true, false>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
-    case 258: return launch_one<64, false, true>(a, b, out, part, S, out_bf16, R, M, Nout, alpha, status, grid, st);
+    case 64: return launch_gr<16, false, false>(args, status, grid, st);
+    case 65: return launch_gr<16, true, false>(args, status, grid, st);
+    case 66: return launch_gr<16, false, true>(args, status, grid, st);
+    case 128: return launch_gr<32, false, false>(args, status, grid, st);
+    case 129: return launch_gr<32, true, false>(args, status, grid, st);
+    case 130: return launch_gr<32, false, true>(args, status, grid, st);
+    case 256: return launch_gr<64, false, false>(args, status, grid, st);
+    case 257: return launch_gr<64, true, false>(args, status, grid, st);
+    case 258: return launch_gr<64, false, true>(args, status, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int RP, bool DX, bool YBF>
 static cudaError_t prep_one() {
-  return cudaFuncSetAttribute(up_kernel<RP, DX, YBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(up_kernel<RP, DX, YBF, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(UpCfg<RP, DX>::kSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(up_kernel<RP, DX, YBF, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(UpCfg<RP, DX>::kSmem));
 }
 

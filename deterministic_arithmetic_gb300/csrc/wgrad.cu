@@ -45,11 +45,18 @@ struct WgCfg {
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
 
-template <int RP, bool DV>
+// GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
+template <int RP, bool DV, bool GR>
 __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
-    wgrad_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_g,
-                 float* __restrict__ part, int M, int Cw, int n_ct, int n_ch, float alpha, uint32_t* status) {
+    wgrad_kernel(const __grid_constant__ Sites<WgSite, GR ? kMaxSites : 1> args, uint32_t* status) {
   using C = WgCfg<RP, DV>;
+  // site of unit u (sites are few and ordered by first unit)
+  auto site = [&](int u) -> const WgSite& {
+    if constexpr (!GR) return args.s[0];
+    int i = 0;
+    while (i + 1 < args.n && u >= args.s[i + 1].u0) ++i;
+    return args.s[i];
+  };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -78,8 +85,10 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0u;
     mbar_fence_init();
-    prefetch_map(&tm_in);
-    prefetch_map(&tm_g);
+    for (int i = 0; i < (GR ? args.n : 1); ++i) {
+      prefetch_map(&args.s[i].in);
+      prefetch_map(&args.s[i].g);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -89,8 +98,10 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = n_ct * n_ch;
-  auto stages_of = [&](int ch) { return (min(M - ch * kWgradChunk, kWgradChunk) + C::kBR - 1) / C::kBR; };
+  const int total = args.total;
+  auto stages_of = [&](const WgSite& P, int ch) {
+    return (min(P.M - ch * kWgradChunk, kWgradChunk) + C::kBR - 1) / C::kBR;
+  };
   // The wide operand (X or dY) is an input of the call, which no earlier kernel of the call
   // writes: the first ring stages' copies of it are issued before waiting for the predecessor,
   // so the stream starts while the predecessor's last CTAs finish. (The du / u rows, which the
@@ -99,13 +110,14 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     const uint64_t pol_stream = policy_evict_first();
     for (int u = blockIdx.x; u < total && pre < C::kStages; u += gridDim.x) {
-      const int ct = u % n_ct, ch = u / n_ct;
-      for (int kb = 0; kb < stages_of(ch) && pre < C::kStages; ++kb, ++pre) {
+      const WgSite& P = site(u);
+      const int ct = (u - P.u0) % P.n_ct, ch = (u - P.u0) / P.n_ct;
+      for (int kb = 0; kb < stages_of(P, ch) && pre < C::kStages; ++kb, ++pre) {
         const uint32_t st = base + pre * C::kStageBytes;
         const int m = ch * kWgradChunk + kb * C::kBR;
         mbar_expect_tx(full(pre), C::kStageBytes);
-        tma_load(st, &tm_in, full(pre), ct * C::kBC, m, pol_stream);
-        tma_load(st + C::kInBytes / 2, &tm_in, full(pre), ct * C::kBC + 64, m, pol_stream);
+        tma_load(st, &P.in, full(pre), ct * C::kBC, m, pol_stream);
+        tma_load(st + C::kInBytes / 2, &P.in, full(pre), ct * C::kBC + 64, m, pol_stream);
       }
     }
   }
@@ -121,21 +133,22 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
       uint32_t issued = 0, parities = 0;
       int k = 0;               // stage count of this CTA
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const int ct = u % n_ct, ch = u / n_ct;
-        const int ns = stages_of(ch);
+        const WgSite& P = site(u);
+        const int ct = (u - P.u0) % P.n_ct, ch = (u - P.u0) / P.n_ct;
+        const int ns = stages_of(P, ch);
         for (int kb = 0; kb < ns; ++kb, ++k) {
           if (k < pre) {         // first pass over the ring: wide operand already in flight
             const uint32_t st = base + r.idx * C::kStageBytes;
-            tma_load(st + C::kInBytes, &tm_g, full(r.idx), 0, ch * kWgradChunk + kb * C::kBR, pol_keep);
+            tma_load(st + C::kInBytes, &P.g, full(r.idx), 0, ch * kWgradChunk + kb * C::kBR, pol_keep);
             issued |= 1u << r.idx;
             parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
           } else if (wait(empty(r.idx), r.phase ^ 1u, ab, 21)) {
             const uint32_t st = base + r.idx * C::kStageBytes;
             const int m = ch * kWgradChunk + kb * C::kBR;
             mbar_expect_tx(full(r.idx), C::kStageBytes);
-            tma_load(st, &tm_in, full(r.idx), ct * C::kBC, m, pol_stream);
-            tma_load(st + C::kInBytes / 2, &tm_in, full(r.idx), ct * C::kBC + 64, m, pol_stream);
-            tma_load(st + C::kInBytes, &tm_g, full(r.idx), 0, m, pol_keep);
+            tma_load(st, &P.in, full(r.idx), ct * C::kBC, m, pol_stream);
+            tma_load(st + C::kInBytes / 2, &P.in, full(r.idx), ct * C::kBC + 64, m, pol_stream);
+            tma_load(st + C::kInBytes, &P.g, full(r.idx), 0, m, pol_keep);
             issued |= 1u << r.idx;
             parities = (parities & ~(1u << r.idx)) | (r.phase << r.idx);
           }
@@ -162,8 +175,9 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
     }
     Ring r, g;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int ch = u / n_ct;
-      const int ns = stages_of(ch);
+      const WgSite& P = site(u);
+      const int ch = (u - P.u0) / P.n_ct;
+      const int ns = stages_of(P, ch);
       for (int kb = 0; kb < ns; ++kb) {
         bool ok = wait(DV ? ready(r.idx) : full(r.idx), r.phase, ab, 23);
         ok = __all_sync(0xffffffffu, ok && wait(tempty(g.idx), g.phase ^ 1u, ab, 24));
@@ -194,8 +208,10 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
     const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + h * C::kCPT;
     Ring g;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int ct = u % n_ct, ch = u / n_ct;
-      const int ns = stages_of(ch);
+      const WgSite& P = site(u);
+      const int ct = (u - P.u0) % P.n_ct, ch = (u - P.u0) / P.n_ct;
+      const int ns = stages_of(P, ch);
+      const int Cw = P.Cw;
       float stack[C::kLevels][C::kCPT];
       float node[C::kCPT];
       bool ok_all = true;
@@ -253,6 +269,7 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
       }
       const int col = ct * C::kBC + q * 32 + lane;
       if (ok_all && col < Cw) {
+        float* __restrict__ part = P.part;
         float* dst = part + size_t(ch) * RP * Cw + size_t(h * C::kCPT) * Cw + col;
 #pragma unroll
         for (int c = 0; c < C::kCPT; ++c) dst[size_t(c) * Cw] = node[c];
@@ -261,11 +278,13 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
   } else {
     // ---------------------------------------------------- dV = bf16(dY*alpha)
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
-    const uint32_t a2 = pow2_bf16x2(alpha);
     Ring r;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int ch = u / n_ct;
-      const int ns = stages_of(ch);
+      const WgSite& P = site(u);
+      const float alpha = P.alpha;
+      const uint32_t a2 = pow2_bf16x2(alpha);
+      const int ch = (u - P.u0) / P.n_ct;
+      const int ns = stages_of(P, ch);
       for (int kb = 0; kb < ns; ++kb) {
         if (wait(full(r.idx), r.phase, ab, 27)) {
           uint4* tile = reinterpret_cast<uint4*>(smem_raw + (base - raw) + size_t(r.idx) * C::kStageBytes);
@@ -289,30 +308,41 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
 }
 
 template <int RP, bool DV>
-static cudaError_t launch_one(const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int Cw, float alpha,
-                              uint32_t* status, int grid, cudaStream_t st) {
+static cudaError_t launch_one(WgArgs& args, uint32_t* status, int grid, cudaStream_t st) {
   using C = WgCfg<RP, DV>;
-  const int n_ct = int(ceil_div(Cw, C::kBC)), n_ch = int(ceil_div(M, kWgradChunk));
-  return launch_pdl(wgrad_kernel<RP, DV>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
-                    in, g, part, M, Cw, n_ct, n_ch, alpha, status);
+  int u0 = 0;
+  for (int i = 0; i < args.n; ++i) {
+    WgSite& s = args.s[i];
+    s.n_ct = int(ceil_div(s.Cw, C::kBC));
+    s.n_ch = int(ceil_div(s.M, kWgradChunk));
+    s.u0 = u0;
+    u0 += s.n_ct * s.n_ch;
+  }
+  args.total = u0;
+  if (args.n > 1)
+    return launch_pdl(wgrad_kernel<RP, DV, true>, dim3(grid), dim3(C::kThreads), C::kSmem, st, args, status);
+  return launch_pdl(wgrad_kernel<RP, DV, false>, dim3(grid), dim3(C::kThreads), C::kSmem, st, first_site(args), status);
 }
 
-cudaError_t launch_wgrad(int RP, bool dv, const CUtensorMap& in, const CUtensorMap& g, float* part, int M, int Cw,
-                         float alpha, uint32_t* status, int grid, cudaStream_t st) {
+cudaError_t launch_wgrad(int RP, bool dv, WgArgs& args, uint32_t* status, int grid, cudaStream_t st) {
+  if (args.n < 1 || args.n > kMaxSites) return cudaErrorInvalidValue;
   switch (RP * 2 + (dv ? 1 : 0)) {
-    case 32: return launch_one<16, false>(in, g, part, M, Cw, alpha, status, grid, st);
-    case 33: return launch_one<16, true>(in, g, part, M, Cw, alpha, status, grid, st);
-    case 64: return launch_one<32, false>(in, g, part, M, Cw, alpha, status, grid, st);
-    case 65: return launch_one<32, true>(in, g, part, M, Cw, alpha, status, grid, st);
-    case 128: return launch_one<64, false>(in, g, part, M, Cw, alpha, status, grid, st);
-    case 129: return launch_one<64, true>(in, g, part, M, Cw, alpha, status, grid, st);
+    case 32: return launch_one<16, false>(args, status, grid, st);
+    case 33: return launch_one<16, true>(args, status, grid, st);
+    case 64: return launch_one<32, false>(args, status, grid, st);
+    case 65: return launch_one<32, true>(args, status, grid, st);
+    case 128: return launch_one<64, false>(args, status, grid, st);
+    case 129: return launch_one<64, true>(args, status, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int RP, bool DV>
 static cudaError_t prep_one() {
-  return cudaFuncSetAttribute(wgrad_kernel<RP, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(wgrad_kernel<RP, DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(WgCfg<RP, DV>::kSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(wgrad_kernel<RP, DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(WgCfg<RP, DV>::kSmem));
 }
 

@@ -34,6 +34,19 @@ class LoraDeltaError(RuntimeError):
 _LIB = None
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
+MAX_SITES = 4
+
+
+class FwdSite(ctypes.Structure):
+    """``lora_fwd_site`` of include/lora_delta.h."""
+    _fields_ = [("x", _vp), ("a", _vp), ("b", _vp), ("alpha", ctypes.c_float), ("M", _i64), ("K", _i64),
+                ("N", _i64), ("delta_y", _vp), ("u", _vp)]
+
+
+class BwdSite(ctypes.Structure):
+    """``lora_bwd_site`` of include/lora_delta.h."""
+    _fields_ = [("dy", _vp), ("x", _vp), ("a", _vp), ("b", _vp), ("u", _vp), ("alpha", ctypes.c_float),
+                ("M", _i64), ("K", _i64), ("N", _i64), ("dx", _vp), ("da", _vp), ("db", _vp), ("du", _vp)]
 
 
 def _lib() -> ctypes.CDLL:
@@ -54,6 +67,17 @@ def _lib() -> ctypes.CDLL:
         for fn in (lib.lora_delta_fwd_workspace_size, lib.lora_delta_bwd_workspace_size):
             fn.argtypes = [_i64, _i64, _i64, _i64]
             fn.restype = ctypes.c_size_t
+        if hasattr(lib, "lora_delta_fwd_grouped"):
+            lib.lora_delta_fwd_grouped_workspace_size.argtypes = [ctypes.POINTER(FwdSite), ctypes.c_int, _i64]
+            lib.lora_delta_fwd_grouped_workspace_size.restype = ctypes.c_size_t
+            lib.lora_delta_bwd_grouped_workspace_size.argtypes = [ctypes.POINTER(BwdSite), ctypes.c_int, _i64]
+            lib.lora_delta_bwd_grouped_workspace_size.restype = ctypes.c_size_t
+            lib.lora_delta_fwd_grouped.argtypes = [ctypes.POINTER(FwdSite), ctypes.c_int, _i64, ctypes.c_int, _vp,
+                                                   ctypes.c_size_t, _vp]
+            lib.lora_delta_fwd_grouped.restype = ctypes.c_int
+            lib.lora_delta_bwd_grouped.argtypes = [ctypes.POINTER(BwdSite), ctypes.c_int, _i64, _vp, ctypes.c_size_t,
+                                                   _vp]
+            lib.lora_delta_bwd_grouped.restype = ctypes.c_int
         lib.lora_status_str.argtypes = [ctypes.c_int]
         lib.lora_status_str.restype = ctypes.c_char_p
         lib.lora_delta_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
@@ -184,3 +208,77 @@ def lora_delta_describe() -> str:
 
 def lora_status_str(code: int) -> str:
     return _lib().lora_status_str(code).decode()
+
+
+def lora_delta_fwd_grouped(sites, *, y_bf16: bool = False, workspace=None, stream=None):
+    """Forward of several sites in one call. ``sites``: sequence of dicts with
+    ``x, a, b, alpha`` and optional ``delta_y, u`` outputs (allocated when
+    absent; BF16 ``delta_y`` when ``y_bf16``). All sites share the rank R.
+    Returns ``[(delta_y, u), ...]``."""
+    n = len(sites)
+    if not 1 <= n <= MAX_SITES:
+        raise ValueError(f"1 to {MAX_SITES} sites per call, got {n}")
+    R = sites[0]["a"].shape[0]
+    arr = (FwdSite * n)()
+    outs = []
+    for i, s in enumerate(sites):
+        x, a, b = s["x"], s["a"], s["b"]
+        M, K = x.shape
+        N = b.shape[0]
+        _check(x, "x", torch.bfloat16, (M, K)); _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R))
+        ydt = torch.bfloat16 if y_bf16 else torch.float32
+        y = s.get("delta_y")
+        y = torch.empty((M, N), dtype=ydt, device=x.device) if y is None else y
+        u = s.get("u")
+        u = torch.empty((M, R), dtype=torch.bfloat16, device=x.device) if u is None else u
+        _check(y, "delta_y", ydt, (M, N)); _check(u, "u", torch.bfloat16, (M, R))
+        arr[i] = FwdSite(_ptr(x), _ptr(a), _ptr(b), float(s["alpha"]), M, K, N, _ptr(y), _ptr(u))
+        outs.append((y, u))
+    need = int(_lib().lora_delta_fwd_grouped_workspace_size(arr, n, R))
+    if need == 0:
+        raise LoraDeltaError(2, "lora_delta_fwd_grouped_workspace_size")
+    if workspace is None:
+        workspace = new_workspace(need, sites[0]["x"].device)
+    rc = _lib().lora_delta_fwd_grouped(arr, n, R, int(bool(y_bf16)), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_fwd_grouped")
+    return outs
+
+
+def lora_delta_bwd_grouped(sites, *, workspace=None, stream=None):
+    """Backward of several sites in one call. ``sites``: sequence of dicts
+    with ``dy, x, a, b, u, alpha`` and optional ``dx, da, db, du`` outputs.
+    Returns ``[(dx, da, db, du), ...]``."""
+    n = len(sites)
+    if not 1 <= n <= MAX_SITES:
+        raise ValueError(f"1 to {MAX_SITES} sites per call, got {n}")
+    R = sites[0]["a"].shape[0]
+    arr = (BwdSite * n)()
+    outs = []
+    for i, s in enumerate(sites):
+        dy, x, a, b, u = s["dy"], s["x"], s["a"], s["b"], s["u"]
+        M, K = x.shape
+        N = b.shape[0]
+        _check(dy, "dy", torch.bfloat16, (M, N)); _check(x, "x", torch.bfloat16, (M, K))
+        _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R)); _check(u, "u", torch.bfloat16, (M, R))
+        dev = x.device
+        dx = torch.empty((M, K), dtype=torch.float32, device=dev) if s.get("dx") is None else s["dx"]
+        da = torch.empty((R, K), dtype=torch.float32, device=dev) if s.get("da") is None else s["da"]
+        db = torch.empty((N, R), dtype=torch.float32, device=dev) if s.get("db") is None else s["db"]
+        du = torch.empty((M, R), dtype=torch.bfloat16, device=dev) if s.get("du") is None else s["du"]
+        _check(dx, "dx", torch.float32, (M, K)); _check(da, "da", torch.float32, (R, K))
+        _check(db, "db", torch.float32, (N, R)); _check(du, "du", torch.bfloat16, (M, R))
+        arr[i] = BwdSite(_ptr(dy), _ptr(x), _ptr(a), _ptr(b), _ptr(u), float(s["alpha"]), M, K, N, _ptr(dx), _ptr(da),
+                         _ptr(db), _ptr(du))
+        outs.append((dx, da, db, du))
+    need = int(_lib().lora_delta_bwd_grouped_workspace_size(arr, n, R))
+    if need == 0:
+        raise LoraDeltaError(2, "lora_delta_bwd_grouped_workspace_size")
+    if workspace is None:
+        workspace = new_workspace(need, sites[0]["x"].device)
+    rc = _lib().lora_delta_bwd_grouped(arr, n, R, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_bwd_grouped")
+    return outs

@@ -98,6 +98,44 @@ lora_status lora_delta_fwd_bf16(const void *x, const void *a, const void *b, flo
                                 void *stream);
 
 /*
+ * Grouped calls: up to 4 independent sites (LoRA insertion points, e.g. the
+ * fc1 and fc2 adapters of one MLP, page "[DSv4][P5-3] shared_grouped_lora_delta:
+ * CUDA + Triton, both batch-invariant", section "Summary": one operator for a
+ * group of sites) of the same rank R, each with its own M, K, N, alpha and
+ * buffers, in the launches of one single-site call: every kernel deals the
+ * work units of all sites out as one space. Each site's results are bit for
+ * bit those of the single-site call on the same arguments. Sites with M = 0
+ * are skipped; count outside [1, 4] is LORA_ERR_SHAPE; the argument checks and
+ * errors are those of the single-site calls, applied to every site.
+ */
+typedef struct lora_fwd_site {
+  const void *x, *a, *b;   /* [M][K], [R][K], [N][R] bf16 */
+  float alpha;
+  int64_t M, K, N;
+  void *delta_y;           /* [M][N] out: fp32, or bf16 when the call's y_bf16 is set */
+  void *u;                 /* [M][R] bf16 out */
+} lora_fwd_site;
+
+typedef struct lora_bwd_site {
+  const void *dy, *x, *a, *b, *u;   /* [M][N], [M][K], [R][K], [N][R], [M][R] bf16 */
+  float alpha;
+  int64_t M, K, N;
+  float *dx, *da, *db;     /* [M][K], [R][K], [N][R] fp32 out */
+  void *du;                /* [M][R] bf16 out */
+} lora_bwd_site;
+
+/* Workspace bytes of a grouped call (0: invalid count or shape). */
+size_t lora_delta_fwd_grouped_workspace_size(const lora_fwd_site *sites, int count, int64_t R);
+size_t lora_delta_bwd_grouped_workspace_size(const lora_bwd_site *sites, int count, int64_t R);
+
+/* Forward of every site (two launches); y_bf16: every delta_y is BF16 (as lora_delta_fwd_bf16). */
+lora_status lora_delta_fwd_grouped(const lora_fwd_site *sites, int count, int64_t R, int y_bf16, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+/* Backward of every site (the launches of one lora_delta_bwd). */
+lora_status lora_delta_bwd_grouped(const lora_bwd_site *sites, int count, int64_t R, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * Backward pass (no base-weight gradient).
  *   dy       [M][N] bf16   upstream gradient of delta_y
  *   x, a, b               as in the forward pass

@@ -138,3 +138,55 @@ def test_python_binding_fails_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(ld, "_LIB", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         ld.library()
+
+
+def test_grouped_calls_host_checks(lib):
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    def fsite(M=64, K=128, N=96, ptr=FAKE, **kw):
+        s = dict(x=ptr, a=ptr, b=ptr, alpha=2.0, M=M, K=K, N=N, delta_y=ptr, u=ptr)
+        s.update(kw)
+        return ld.FwdSite(**s)
+
+    def bsite(M=64, K=128, N=96, ptr=FAKE, **kw):
+        s = dict(dy=ptr, x=ptr, a=ptr, b=ptr, u=ptr, alpha=2.0, M=M, K=K, N=N, dx=ptr, da=ptr, db=ptr, du=ptr)
+        s.update(kw)
+        return ld.BwdSite(**s)
+
+    def arr(cls, sites):
+        a = (cls * len(sites))()
+        for i, s in enumerate(sites):
+            a[i] = s
+        return a
+
+    f = lib.lora_delta_fwd_grouped
+    g = lib.lora_delta_bwd_grouped
+    big = 1 << 30
+    # workspace: one status block plus every site's partial sums
+    two = arr(ld.FwdSite, [fsite(), fsite(M=300, K=264, N=136)])
+    assert lib.lora_delta_fwd_grouped_workspace_size(two, 2, 8) == \
+        ld.lora_delta_fwd_workspace_size(64, 128, 96, 8) + ld.lora_delta_fwd_workspace_size(300, 264, 136, 8) - 256
+    btwo = arr(ld.BwdSite, [bsite(), bsite(M=300, K=264, N=136)])
+    assert lib.lora_delta_bwd_grouped_workspace_size(btwo, 2, 16) == \
+        ld.lora_delta_bwd_workspace_size(64, 128, 96, 16) + ld.lora_delta_bwd_workspace_size(300, 264, 136, 16) - 256
+    assert lib.lora_delta_fwd_grouped_workspace_size(two, 5, 8) == 0
+    assert lib.lora_delta_fwd_grouped_workspace_size(arr(ld.FwdSite, [fsite(), fsite(K=100)]), 2, 8) == 0
+    # errors, each site checked as a single-site call would be
+    assert f(None, 1, 8, 0, FAKE, big, None) == 1                                        # LORA_ERR_NULL
+    assert f(two, 0, 8, 0, FAKE, big, None) == 2 and f(two, 5, 8, 0, FAKE, big, None) == 2   # count
+    assert f(arr(ld.FwdSite, [fsite(), fsite(N=90)]), 2, 8, 0, FAKE, big, None) == 2    # LORA_ERR_SHAPE
+    assert f(two, 2, 12, 0, FAKE, big, None) == 4                                       # LORA_ERR_RANK
+    assert f(arr(ld.FwdSite, [fsite(), fsite(u=None)]), 2, 8, 0, FAKE, big, None) == 1
+    assert f(arr(ld.FwdSite, [fsite(), fsite(x=FAKE + 2)]), 2, 8, 0, FAKE, big, None) == 3
+    assert f(two, 2, 8, 0, FAKE, 300, None) == 5                                        # LORA_ERR_WORKSPACE
+    assert f(two, 2, 8, 0, None, big, None) == 1
+    assert f(arr(ld.FwdSite, [fsite(M=0, ptr=None), fsite(M=0, ptr=None)]), 2, 8, 0, None, 0, None) == 0
+    assert g(arr(ld.BwdSite, [bsite(), bsite(db=None)]), 2, 16, FAKE, big, None) == 1
+    assert g(arr(ld.BwdSite, [bsite(), bsite(dx=FAKE + 4)]), 2, 16, FAKE, big, None) == 3
+    assert g(btwo, 2, 16, FAKE, 1000, None) == 5
+    import torch
+
+    if not torch.cuda.is_available():
+        # valid arguments reach the device check and fail there: never a CPU computation
+        assert f(two, 2, 8, 0, FAKE, big, None) in (6, 7)
+        assert g(btwo, 2, 16, FAKE, big, None) in (6, 7)
