@@ -276,6 +276,79 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
     return out
 
 
+def grouped_variants(ld, dev, steps=10, reps=20):
+    """The MLP insertion points of the pages (fc1 K5120 -> N17408, fc2 K17408 -> N5120,
+    M4096, R16, alpha 1; random BF16 inputs drawn on the device), forward + backward of
+    both sites: one grouped call per pass against two single-site calls per pass, each
+    CUDA-graph timed."""
+    import torch
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    M, R = 4096, 16
+
+    def rnd(*shape, s=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * s).to(torch.bfloat16)
+
+    sites = []
+    for K, N in ((5120, 17408), (17408, 5120)):
+        sites.append(dict(x=rnd(M, K), a=rnd(R, K, s=K ** -0.5), b=rnd(N, R, s=R ** -0.5), dy=rnd(M, N, s=0.1),
+                          alpha=1.0, delta_y=torch.empty((M, N), dtype=torch.float32, device=dev),
+                          u=torch.empty((M, R), dtype=torch.bfloat16, device=dev),
+                          dx=torch.empty((M, K), dtype=torch.float32, device=dev),
+                          da=torch.empty((R, K), dtype=torch.float32, device=dev),
+                          db=torch.empty((N, R), dtype=torch.float32, device=dev),
+                          du=torch.empty((M, R), dtype=torch.bfloat16, device=dev),
+                          wf=ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev),
+                          wb=ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)))
+    fw_sites = [{k: s[k] for k in ("x", "a", "b", "alpha", "delta_y", "u")} for s in sites]
+    bw_sites = [{k: s[k] for k in ("dy", "x", "a", "b", "u", "alpha", "dx", "da", "db", "du")} for s in sites]
+    wfg = ld.new_workspace(sum(s["wf"].numel() for s in sites), dev)
+    wbg = ld.new_workspace(sum(s["wb"].numel() for s in sites), dev)
+
+    def separate(st):
+        for s in sites:
+            ld.lora_delta_fwd(s["x"], s["a"], s["b"], s["alpha"], delta_y=s["delta_y"], u=s["u"], workspace=s["wf"],
+                              stream=st)
+        for s in sites:
+            ld.lora_delta_bwd(s["dy"], s["x"], s["a"], s["b"], s["u"], s["alpha"], dx=s["dx"], da=s["da"], db=s["db"],
+                              du=s["du"], workspace=s["wb"], stream=st)
+
+    def grouped(st):
+        ld.lora_delta_fwd_grouped(fw_sites, workspace=wfg, stream=st)
+        ld.lora_delta_bwd_grouped(bw_sites, workspace=wbg, stream=st)
+
+    out = {}
+    nbytes = sum(sum(algorithmic_bytes(M, s["x"].shape[1], s["b"].shape[0], R).values()) for s in sites)
+    for name, fn, launches in (("mlp_fc1_fc2_separate", separate, 2 * (2 + 4)), ("mlp_fc1_fc2_grouped", grouped, 2 + 4)):
+        for _ in range(3):
+            fn(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for _ in range(steps):
+                    fn(torch.cuda.current_stream(dev))
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * steps)
+        out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "launches_per_step": launches}
+    for s in sites:
+        assert ld.lora_delta_device_status(s["wf"]) == 0 and ld.lora_delta_device_status(s["wb"]) == 0
+    assert ld.lora_delta_device_status(wfg) == 0 and ld.lora_delta_device_status(wbg) == 0
+    return out
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, world, rank, local):
     import torch
@@ -411,6 +484,7 @@ def run_ours(args, world, rank, local):
     variants = None
     if not args.no_variants:
         variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev)
+        variants.update(grouped_variants(ld, dev))
 
     # ----------------------------------------------------------- end to end
     e2e = None
