@@ -276,6 +276,54 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
     return out
 
 
+def bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
+    """Backward only, BF16 dY against the FP32-dY input variant (dV = bf16(fp32(dY * alpha))
+    formed by a first launch), CUDA-graph timed, inputs rotated like the main step."""
+    import torch
+
+    out = {}
+    bf, f4 = 2, 4
+    U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+    ld.lora_delta_fwd(Xs[0], A, B, alpha, u=U, workspace=wf)
+    DY32 = [d.float() for d in DYs]
+    outs = dict(dx=torch.empty((M, K), dtype=torch.float32, device=dev),
+                da=torch.empty((R, K), dtype=torch.float32, device=dev),
+                db=torch.empty((N, R), dtype=torch.float32, device=dev),
+                du=torch.empty((M, R), dtype=torch.bfloat16, device=dev))
+    for name, dys, dsz, wsize in (("bwd_bf16_dy", DYs, bf, ld.lora_delta_bwd_workspace_size),
+                                  ("bwd_f32_dy", DY32, f4, ld.lora_delta_bwd_f32dy_workspace_size)):
+        wb = ld.new_workspace(wsize(M, K, N, R), dev)
+        for i in range(5):
+            ld.lora_delta_bwd(dys[i % N_ROTATE], Xs[i % N_ROTATE], A, B, U, alpha, workspace=wb, **outs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                gst = torch.cuda.current_stream(dev)
+                for i in range(steps):
+                    ld.lora_delta_bwd(dys[i % N_ROTATE], Xs[i % N_ROTATE], A, B, U, alpha, workspace=wb, stream=gst,
+                                      **outs)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * steps)
+        nbytes = M * N * dsz + N * R * bf + M * R * bf + M * K * bf + R * K * bf + M * K * f4 + 2 * M * R * bf \
+            + R * K * f4 + N * R * f4
+        out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "launches_per_step": 4 if dsz == bf else 5}
+        assert ld.lora_delta_device_status(wb) == 0
+    return out
+
+
 def grouped_variants(ld, dev, steps=10, reps=20):
     """The MLP insertion points of the pages (fc1 K5120 -> N17408, fc2 K17408 -> N5120,
     M4096, R16, alpha 1; random BF16 inputs drawn on the device), forward + backward of
@@ -484,6 +532,7 @@ def run_ours(args, world, rank, local):
     variants = None
     if not args.no_variants:
         variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev)
+        variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(grouped_variants(ld, dev))
 
     # ----------------------------------------------------------- end to end

@@ -436,6 +436,35 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
   return bwd_group(&in, 1, R, workspace, workspace_bytes, stream);
 }
 
+size_t lora_delta_bwd_f32dy_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
+  if (check_shape(M, K, N, R) != LORA_OK) return 0;
+  return bwd_layout(M, K, N, R).total + round256(size_t(M) * size_t(N) * 2);
+}
+
+lora_status lora_delta_bwd_f32dy(const float* dy, const void* x, const void* a, const void* b, const void* u,
+                                 float alpha, int64_t M, int64_t K, int64_t N, int64_t R, float* dx, float* da,
+                                 float* db, void* du, void* workspace, size_t workspace_bytes, void* stream) {
+  lora_status s = check_shape(M, K, N, R);
+  if (s != LORA_OK) return s;
+  if (M == 0) return LORA_OK;
+  if (!dy || !x || !a || !b || !u || !dx || !da || !db || !du || !workspace) return LORA_ERR_NULL;
+  for (const void* p : {static_cast<const void*>(dy), x, a, b, u, static_cast<const void*>(dx),
+                        static_cast<const void*>(da), static_cast<const void*>(db), static_cast<const void*>(du),
+                        static_cast<const void*>(workspace)})
+    if (!aligned16(p)) return LORA_ERR_ALIGN;
+  const size_t bwd_bytes = bwd_layout(M, K, N, R).total;
+  if (workspace_bytes < lora_delta_bwd_f32dy_workspace_size(M, K, N, R)) return LORA_ERR_WORKSPACE;
+  int nsm = 0;
+  if ((s = device_ready(&nsm)) != LORA_OK) return s;
+  // dV = bf16(fp32(dy * alpha)) into the workspace after the backward's own regions; the backward
+  // then reads it as its dY with alpha = 1 (bf16(fp32(dv * 1)) = dv)
+  void* dv = static_cast<uint8_t*>(workspace) + bwd_bytes;
+  if (launch_dv_from_f32(dy, alpha, M * N, dv, nsm, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  const BwdIn in{dv, x, a, b, u, 1.0f, M, K, N, dx, da, db, du};
+  return bwd_group(&in, 1, R, workspace, bwd_bytes, stream);
+}
+
 size_t lora_delta_fwd_grouped_workspace_size(const lora_fwd_site* sites, int count, int64_t R) {
   if (!sites || count < 1 || count > kMaxSites) return 0;
   size_t t = kStatusBytes;

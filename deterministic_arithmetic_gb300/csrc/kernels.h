@@ -166,6 +166,9 @@ struct CombineJobs {
 };
 cudaError_t launch_combine(const CombineJobs& jobs, cudaStream_t st);
 
+// dV = bf16(fp32(dy * alpha)) from a binary32 dY of n values (n a multiple of 8), into dv.
+cudaError_t launch_dv_from_f32(const float* dy, float alpha, int64_t n, void* dv, int nsm, cudaStream_t st);
+
 // Raise the dynamic shared-memory limit of every kernel instance in a
 // translation unit (once per device, with that device current).
 cudaError_t prepare_down();

@@ -64,6 +64,11 @@ def _lib() -> ctypes.CDLL:
         lib.lora_delta_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
                                        _vp, _vp, ctypes.c_size_t, _vp]
         lib.lora_delta_bwd.restype = ctypes.c_int
+        if hasattr(lib, "lora_delta_bwd_f32dy"):
+            lib.lora_delta_bwd_f32dy.argtypes = lib.lora_delta_bwd.argtypes
+            lib.lora_delta_bwd_f32dy.restype = ctypes.c_int
+            lib.lora_delta_bwd_f32dy_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
+            lib.lora_delta_bwd_f32dy_workspace_size.restype = ctypes.c_size_t
         for fn in (lib.lora_delta_fwd_workspace_size, lib.lora_delta_bwd_workspace_size):
             fn.argtypes = [_i64, _i64, _i64, _i64]
             fn.restype = ctypes.c_size_t
@@ -151,12 +156,19 @@ def lora_delta_fwd(x, a, b, alpha: float, *, delta_y=None, u=None, workspace=Non
     return delta_y, u
 
 
+def lora_delta_bwd_f32dy_workspace_size(M: int, K: int, N: int, R: int) -> int:
+    return int(_lib().lora_delta_bwd_f32dy_workspace_size(M, K, N, R))
+
+
 def lora_delta_bwd(dy, x, a, b, u, alpha: float, *, dx=None, da=None, db=None, du=None, workspace=None, stream=None):
-    """Backward: returns ``(dx, da, db, du)``; no base-weight gradient."""
+    """Backward: returns ``(dx, da, db, du)``; no base-weight gradient.
+
+    An FP32 ``dy`` selects ``lora_delta_bwd_f32dy`` (dV = bf16(fp32(dy * alpha)))."""
     M, K = x.shape
     R = a.shape[0]
     N = b.shape[0]
-    _check(dy, "dy", torch.bfloat16, (M, N)); _check(x, "x", torch.bfloat16, (M, K))
+    dy_f32 = dy.dtype == torch.float32
+    _check(dy, "dy", torch.float32 if dy_f32 else torch.bfloat16, (M, N)); _check(x, "x", torch.bfloat16, (M, K))
     _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R)); _check(u, "u", torch.bfloat16, (M, R))
     dev = x.device
     dx = torch.empty((M, K), dtype=torch.float32, device=dev) if dx is None else dx
@@ -165,14 +177,15 @@ def lora_delta_bwd(dy, x, a, b, u, alpha: float, *, dx=None, da=None, db=None, d
     du = torch.empty((M, R), dtype=torch.bfloat16, device=dev) if du is None else du
     _check(dx, "dx", torch.float32, (M, K)); _check(da, "da", torch.float32, (R, K))
     _check(db, "db", torch.float32, (N, R)); _check(du, "du", torch.bfloat16, (M, R))
-    need = lora_delta_bwd_workspace_size(M, K, N, R)
+    need = (lora_delta_bwd_f32dy_workspace_size if dy_f32 else lora_delta_bwd_workspace_size)(M, K, N, R)
     if workspace is None:
         workspace = new_workspace(need, dev)
-    rc = _lib().lora_delta_bwd(_ptr(dy), _ptr(x), _ptr(a), _ptr(b), _ptr(u), float(alpha), M, K, N, R, _ptr(dx),
+    name = "lora_delta_bwd_f32dy" if dy_f32 else "lora_delta_bwd"
+    rc = getattr(_lib(), name)(_ptr(dy), _ptr(x), _ptr(a), _ptr(b), _ptr(u), float(alpha), M, K, N, R, _ptr(dx),
                                _ptr(da), _ptr(db), _ptr(du), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != LORA_OK:
-        raise LoraDeltaError(rc, "lora_delta_bwd")
+        raise LoraDeltaError(rc, name)
     return dx, da, db, du
 
 

@@ -98,6 +98,22 @@ lora_status lora_delta_fwd_bf16(const void *x, const void *a, const void *b, flo
                                 void *stream);
 
 /*
+ * Backward pass with a binary32 dY (the FP32-dY input variant; its BF16-output
+ * counterpart is asked for in the review thread of page "[DSv4][P5-3]
+ * shared_grouped_lora_delta: CUDA + Triton, both batch-invariant").
+ *   dy       [M][N] fp32   upstream gradient; dV = bf16(fp32(dy * alpha))
+ * Every other argument, output and error is that of lora_delta_bwd; the
+ * workspace (lora_delta_bwd_f32dy_workspace_size) also holds dV, written by a
+ * first launch and read by the backward kernels as their dY with alpha = 1.
+ * When every dy value is representable in BF16 the outputs are bit for bit
+ * those of lora_delta_bwd on that BF16 dY.
+ */
+size_t lora_delta_bwd_f32dy_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
+lora_status lora_delta_bwd_f32dy(const float *dy, const void *x, const void *a, const void *b, const void *u,
+                                 float alpha, int64_t M, int64_t K, int64_t N, int64_t R, float *dx, float *da,
+                                 float *db, void *du, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Grouped calls: up to 4 independent sites (LoRA insertion points, e.g. the
  * fc1 and fc2 adapters of one MLP, page "[DSv4][P5-3] shared_grouped_lora_delta:
  * CUDA + Triton, both batch-invariant", section "Summary": one operator for a

@@ -258,6 +258,27 @@ int ora_dv(const uint16_t *dy, float alpha, int64_t M, int64_t N, uint16_t *dv)
 }
 
 /*
+ * The FP32-dY input variant (SURVEY's "FP32-dY input", the input counterpart of
+ * the BF16 output asked for in the review thread of page "[DSv4][P5-3]
+ * shared_grouped_lora_delta: CUDA + Triton, both batch-invariant"):
+ * dv[m][n] = rnbf(rn32(dy[m][n] * alpha)) with dy read as binary32 (the product
+ * of two binary32 values is exact in binary64; it is rounded to binary32, then
+ * to bfloat16: two roundings, as for BF16 dY).
+ */
+int ora_dv_f32(const float *dy, float alpha, int64_t M, int64_t N, uint16_t *dv)
+{
+    for (int64_t e = 0; e < M * N; ++e) {
+#if ORACLE_MUTANT == 11  /* planted: the binary32 product truncated to bfloat16 */
+        float f = rn32((double)dy[e] * (double)alpha);
+        uint32_t bits; memcpy(&bits, &f, 4); dv[e] = (uint16_t)(bits >> 16);
+#else
+        dv[e] = rnbf(rn32((double)dy[e] * (double)alpha));
+#endif
+    }
+    return 0;
+}
+
+/*
  * du[m][r] = rnbf(rn32(sum_n dv[m][n] * b[n][r]))  ("dU = dV @ B", rounded to
  * BF16 between the GEMMs, section "Summary"). f32_du (optional) = the rn32 value.
  */

@@ -71,6 +71,7 @@ class Oracle:
             "ora_delta_y": [_u16p, _u16p, ctypes.c_float, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
             "ora_delta_y_bf16": [_u16p, _u16p, ctypes.c_float, _i64, _i64, _i64, _u16p, ctypes.c_int],
             "ora_dv": [_u16p, ctypes.c_float, _i64, _i64, _u16p],
+            "ora_dv_f32": [_f32p, ctypes.c_float, _i64, _i64, _u16p],
             "ora_du": [_u16p, _u16p, _i64, _i64, _i64, _u16p, _f32p, _f64p, ctypes.c_int],
             "ora_db": [_u16p, _u16p, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
             "ora_dx": [_u16p, _u16p, _i64, _i64, _i64, _f32p, _f64p, ctypes.c_int],
@@ -138,6 +139,14 @@ class Oracle:
         M, N = dy.shape
         dv = np.empty((M, N), np.uint16)
         assert self.lib.ora_dv(_p(dy, _u16p), float(alpha), M, N, _p(dv, _u16p)) == 0
+        return dv
+
+    def dv_f32(self, dy, alpha):
+        """dV (bf16 bits) of the FP32-dY input variant: rnbf(rn32(dy * alpha))."""
+        dy = self._c(dy, np.float32)
+        M, N = dy.shape
+        dv = np.empty((M, N), np.uint16)
+        assert self.lib.ora_dv_f32(_p(dy, _f32p), float(alpha), M, N, _p(dv, _u16p)) == 0
         return dv
 
     def du(self, dv, b, want_s=False, want_f32=False):

@@ -13,7 +13,9 @@ when the oracle disagrees with:
 * ``pin_invariants``        B = 0, A = 0, linearity in alpha;
 * ``pin_finite_differences`` the gradients against central differences of the scalar loss;
 * ``pin_bf16_output``       the BF16 dY_lora variant: exact rationals rounded at its extra
-                            rounding point, and constructed ties of round-to-nearest-even.
+                            rounding point, and constructed ties of round-to-nearest-even;
+* ``pin_f32_dy``            the FP32-dY input variant's dV: exact rationals, and a value that
+                            only two roundings (binary32, then bfloat16) send to the even side.
 
 The test suite also runs every pin against builds of the oracle with a planted
 mistake and requires that some pin fails for each.
@@ -255,5 +257,30 @@ def pin_bf16_output(o, seed=13):
                                                    -(1.0 + 2.0 ** -6), 1.0 - 2.0 ** -8]]))
 
 
+# ------------------------------------------------------ FP32-dY input variant
+def pin_f32_dy(o, seed=17):
+    # (1) exact rationals: dV = rnbf(rn32(dy * alpha)) for binary32 dy of every magnitude
+    rng = np.random.default_rng(seed)
+    dy = (rng.standard_normal((6, 40)) * np.exp2(rng.integers(-30, 30, (6, 40)))).astype(np.float32)
+    for alpha in (0.3, 2.0, -1.5):
+        a32 = np.float32(alpha)
+        got = o.dv_f32(dy, float(a32))
+        exp = np.empty(dy.shape, np.uint16)
+        for idx, v in np.ndenumerate(dy):
+            q32 = ex.rn32(Fraction(float(v)) * Fraction(float(a32)))
+            q = ex.rnbf_of_f32(Fraction(float(ex.to_f32(q32))) if not isinstance(q32, float) else q32)
+            exp[idx] = (0x7F80 if q > 0 else 0xFF80) if isinstance(q, float) else ex.bf16_bits(q)
+        _eq_bits(f"f32_dy:alpha={alpha}", got, exp)
+    # (2) two roundings, not one: (1 + 2^-8 + 2^-23) * (1 - 2^-24) lies just above the BF16
+    # midpoint 1 + 2^-8 but rounds to it in binary32, so the BF16 result is the even 1;
+    # 1 + 3 * 2^-8 is a midpoint already and goes up; a value past the binary32 range is infinite
+    dy2 = np.array([[1 + 2.0 ** -8 + 2.0 ** -23, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3.0e38]], np.float32)
+    got = o.dv_f32(dy2[:, :3], float(np.float32(1 - 2.0 ** -24)))
+    _eq_bits("f32_dy:double rounding", got[:, :1], _bits([[1.0]]))
+    got = o.dv_f32(dy2, 1.0)
+    assert got[0, 1] == _bits([[1 + 2.0 ** -6]])[0, 0] and got[0, 2] == _bits([[-1.0]])[0, 0], got
+    assert o.dv_f32(dy2[:, 3:], 2.0)[0, 0] == 0x7F80
+
+
 ALL_PINS = [pin_golden, pin_rounding, pin_rational, pin_headroom_integers, pin_permutation,
-            pin_library_matmul, pin_invariants, pin_finite_differences, pin_bf16_output]
+            pin_library_matmul, pin_invariants, pin_finite_differences, pin_bf16_output, pin_f32_dy]

@@ -190,3 +190,32 @@ def test_grouped_calls_host_checks(lib):
         # valid arguments reach the device check and fail there: never a CPU computation
         assert f(two, 2, 8, 0, FAKE, big, None) in (6, 7)
         assert g(btwo, 2, 16, FAKE, big, None) in (6, 7)
+
+
+def test_f32dy_backward_host_checks(lib):
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    f = lib.lora_delta_bwd_f32dy
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_float] + [ctypes.c_int64] * 4 + [ctypes.c_void_p] * 5 + \
+                 [ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    need = ld.lora_delta_bwd_f32dy_workspace_size(64, 128, 96, 16)
+    # the backward's workspace plus the BF16 dV (M x N x 2 bytes, 256-byte rounded)
+    assert need == ld.lora_delta_bwd_workspace_size(64, 128, 96, 16) + 64 * 96 * 2
+    assert ld.lora_delta_bwd_f32dy_workspace_size(64, 100, 96, 16) == 0
+    ok = [FAKE] * 10
+
+    def call(p=ok, M=64, K=128, N=96, R=16, ws=need):
+        dy, x, a, b, u, dx, da, db, du, w = p
+        return f(dy, x, a, b, u, 2.0, M, K, N, R, dx, da, db, du, w, ws, None)
+
+    assert call(M=0) == 0
+    assert call([None] + ok[1:]) == 1
+    assert call(K=100) == 2
+    assert call(R=12) == 4
+    assert call([FAKE + 8] + ok[1:]) == 3
+    assert call(ws=need - 256) == 5
+    import torch
+
+    if not torch.cuda.is_available():
+        assert call() in (6, 7)

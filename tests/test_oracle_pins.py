@@ -8,7 +8,7 @@ import pytest
 import pins
 from oracle import oracle as oracle_mod
 
-N_MUTANTS = 10
+N_MUTANTS = 11
 
 
 @pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
