@@ -258,9 +258,9 @@ int ora_dv(const uint16_t *dy, float alpha, int64_t M, int64_t N, uint16_t *dv)
 }
 
 /*
- * The FP32-dY input variant (SURVEY's "FP32-dY input", the input counterpart of
- * the BF16 output asked for in the review thread of page "[DSv4][P5-3]
- * shared_grouped_lora_delta: CUDA + Triton, both batch-invariant"):
+ * The FP32-dY input variant (the input counterpart of the BF16 output asked
+ * for in the review thread of page "[DSv4][P5-3] shared_grouped_lora_delta:
+ * CUDA + Triton, both batch-invariant"):
  * dv[m][n] = rnbf(rn32(dy[m][n] * alpha)) with dy read as binary32 (the product
  * of two binary32 values is exact in binary64; it is rounded to binary32, then
  * to bfloat16: two roundings, as for BF16 dY).
