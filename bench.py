@@ -324,6 +324,39 @@ def bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
     return out
 
 
+def exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, reps=5):
+    """Exact mode of dA and dB (lora_delta_grads_exact: integer long-accumulator digits, one
+    rounding) on the step's inputs, event-timed per launch pair (digits + reduce) through the
+    library's profiling hook, inputs rotated like the main step."""
+    import torch
+
+    U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    DU = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+    wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
+    ld.lora_delta_fwd(Xs[0], A, B, alpha, u=U, workspace=wf)
+    ld.lora_delta_bwd(DYs[0], Xs[0], A, B, U, alpha, du=DU, workspace=wb)
+    we = ld.new_workspace(ld.lora_delta_grads_exact_workspace_size(M, K, N, R), dev)
+    da = torch.empty((R, K), dtype=torch.float32, device=dev)
+    db = torch.empty((N, R), dtype=torch.float32, device=dev)
+    for i in range(2):
+        ld.lora_delta_grads_exact(DYs[i % N_ROTATE], Xs[i % N_ROTATE], U, DU, alpha, da=da, db=db, workspace=we)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for i in range(reps):
+        ld.lora_delta_set_profile_events(ev[i])
+        ld.lora_delta_grads_exact(DYs[i % N_ROTATE], Xs[i % N_ROTATE], U, DU, alpha, da=da, db=db, workspace=we)
+    ld.lora_delta_set_profile_events([])
+    torch.cuda.synchronize()
+    t_da = sorted(e[0].elapsed_time(e[1]) for e in ev)[reps // 2]
+    t_db = sorted(e[1].elapsed_time(e[2]) for e in ev)[reps // 2]
+    prod = M * R * (K + N)
+    ms = t_da + t_db
+    return {"grads_exact": {"ms": round(ms, 4), "ms_da": round(t_da, 4), "ms_db": round(t_db, 4),
+                            "products": prod, "gproducts_per_s": round(prod / (ms * 1e-3) / 1e9, 1),
+                            "launches_per_step": 4, "median_of": reps}}
+
+
 def grouped_variants(ld, dev, steps=10, reps=20):
     """The MLP insertion points of the pages (fc1 K5120 -> N17408, fc2 K17408 -> N5120,
     M4096, R16, alpha 1; random BF16 inputs drawn on the device), forward + backward of
@@ -534,6 +567,7 @@ def run_ours(args, world, rank, local):
         variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev)
         variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(grouped_variants(ld, dev))
+        variants.update(exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
 
     # ----------------------------------------------------------- end to end
     e2e = None

@@ -50,7 +50,7 @@ lora_status device_ready(int* num_sms) {
     d.usable = (major == 10 && minor == 3);
     if (d.usable) {
       if (prepare_down() != cudaSuccess || prepare_up() != cudaSuccess || prepare_wgrad() != cudaSuccess ||
-          prepare_dy() != cudaSuccess) {
+          prepare_dy() != cudaSuccess || prepare_exact() != cudaSuccess) {
         d.probed = false;
         return LORA_ERR_CUDA;
       }
@@ -505,6 +505,77 @@ lora_status lora_delta_bwd_grouped(const lora_bwd_site* sites, int count, int64_
     in[i] = BwdIn{sites[i].dy, sites[i].x, sites[i].a, sites[i].b, sites[i].u, sites[i].alpha, sites[i].M,
                   sites[i].K, sites[i].N, sites[i].dx, sites[i].da, sites[i].db, sites[i].du};
   return bwd_group(in, count, R, workspace, workspace_bytes, stream);
+}
+
+int lora_delta_exact_slots(void) { return kExactSlots; }
+
+size_t lora_delta_grads_exact_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
+  if (check_shape(M, K, N, R) != LORA_OK || M >= (int64_t(1) << 30) || R * K >= (int64_t(1) << 31) ||
+      R * N >= (int64_t(1) << 31))
+    return 0;
+  return round256(std::max(exact_part_bytes(M, R, K), exact_part_bytes(M, R, N)));
+}
+
+lora_status lora_delta_grads_exact(const void* dy, const void* x, const void* u, const void* du, float alpha,
+                                   int64_t M, int64_t K, int64_t N, int64_t R, float* da, float* db,
+                                   int64_t* da_digits, int64_t* db_digits, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  lora_status s = check_shape(M, K, N, R);
+  if (s != LORA_OK) return s;
+  if (M >= (int64_t(1) << 30) || R * K >= (int64_t(1) << 31) || R * N >= (int64_t(1) << 31)) return LORA_ERR_SHAPE;
+  const bool want_a = da || da_digits, want_b = db || db_digits;
+  if (!want_a && !want_b) return LORA_OK;
+  // inputs are read only when M > 0 (an empty batch gives zero gradients)
+  if (!workspace || (M > 0 && ((want_a && (!x || !du)) || (want_b && (!dy || !u))))) return LORA_ERR_NULL;
+  for (const void* p : {dy, x, u, du, static_cast<const void*>(da), static_cast<const void*>(db),
+                        static_cast<const void*>(da_digits), static_cast<const void*>(db_digits),
+                        static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return LORA_ERR_ALIGN;
+  if (workspace_bytes < lora_delta_grads_exact_workspace_size(M, K, N, R)) return LORA_ERR_WORKSPACE;
+  int nsm = 0;
+  if ((s = device_ready(&nsm)) != LORA_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  long long* part = static_cast<long long*>(workspace);
+  Recorder rec(st);
+  rec.mark();
+  // dA = du^T x: left du [M][R], right x [M][K], out [R][K]
+  if (want_a && launch_exact(du, int(R), x, int(K), false, 1.0f, int(M), int(R), int(K), part, false,
+                             reinterpret_cast<long long*>(da_digits), da, nsm, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  rec.mark();
+  // dB = dv^T u: left u [M][R], right dv from dy [M][N], out transposed to [N][R]
+  if (want_b && launch_exact(u, int(R), dy, int(N), true, alpha, int(M), int(R), int(N), part, true,
+                             reinterpret_cast<long long*>(db_digits), db, nsm, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  rec.mark();
+  return LORA_OK;
+}
+
+lora_status lora_delta_exact_combine(const int64_t* a, const int64_t* b, int64_t n, int64_t* out_digits, void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 40)) return LORA_ERR_SHAPE;
+  if (n == 0) return LORA_OK;
+  if (!a || !b || !out_digits) return LORA_ERR_NULL;
+  int nsm = 0;
+  lora_status s = device_ready(&nsm);
+  if (s != LORA_OK) return s;
+  return launch_exact_combine(reinterpret_cast<const long long*>(a), reinterpret_cast<const long long*>(b), n,
+                              reinterpret_cast<long long*>(out_digits), nullptr,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
+}
+
+lora_status lora_delta_exact_finalize(const int64_t* digits, int64_t n, float* out, void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 40)) return LORA_ERR_SHAPE;
+  if (n == 0) return LORA_OK;
+  if (!digits || !out) return LORA_ERR_NULL;
+  int nsm = 0;
+  lora_status s = device_ready(&nsm);
+  if (s != LORA_OK) return s;
+  return launch_exact_combine(reinterpret_cast<const long long*>(digits), nullptr, n, nullptr, out,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
 }
 
 lora_status lora_delta_device_status(const void* workspace, int* code) {

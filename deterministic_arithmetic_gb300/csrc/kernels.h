@@ -169,6 +169,23 @@ cudaError_t launch_combine(const CombineJobs& jobs, cudaStream_t st);
 // dV = bf16(fp32(dy * alpha)) from a binary32 dY of n values (n a multiple of 8), into dv.
 cudaError_t launch_dv_from_f32(const float* dy, float alpha, int64_t n, void* dv, int nsm, cudaStream_t st);
 
+// Exact mode of the weight gradients (exact.cu): per output, kDigits signed 64-bit digits in radix
+// 2^32 (digit i weighs 2^(32 i - 266)) and three counters (+inf, -inf, NaN products): kExactSlots.
+constexpr int kDigits = 18, kExactSlots = kDigits + 3;
+// The digit kernel runs at most kMaxExactGrid persistent CTAs; exact_part_bytes is its scratch
+// (segment records and digit arrays) for a P x Q output.
+constexpr int kMaxExactGrid = 512;
+size_t exact_part_bytes(int64_t M, int64_t P, int64_t Q);
+// sum_m left[m][p] * right[m][q] (right = bf16(fp32(dy * alpha)) with dv) for p < P, q < Q, exactly:
+// the normalised digit arrays to out_digits and / or the FP32 values to out, both in the order
+// [p][q], or [q][p] with transpose (either may be null). nsm: SMs of the device.
+cudaError_t launch_exact(const void* left, int ldl, const void* right, int ldr, bool dv, float alpha, int M, int P, int Q,
+                         long long* part, bool transpose, long long* out_digits, float* out, int nsm, cudaStream_t st);
+// n digit arrays: out_digits = normalised (a + b), out = the FP32 values (b, out_digits or out may be null)
+cudaError_t launch_exact_combine(const long long* a, const long long* b, int64_t n, long long* out_digits, float* out,
+                                 cudaStream_t st);
+cudaError_t prepare_exact();
+
 // Raise the dynamic shared-memory limit of every kernel instance in a
 // translation unit (once per device, with that device current).
 cudaError_t prepare_down();

@@ -83,6 +83,18 @@ def _lib() -> ctypes.CDLL:
             lib.lora_delta_bwd_grouped.argtypes = [ctypes.POINTER(BwdSite), ctypes.c_int, _i64, _vp, ctypes.c_size_t,
                                                    _vp]
             lib.lora_delta_bwd_grouped.restype = ctypes.c_int
+        if hasattr(lib, "lora_delta_grads_exact"):
+            lib.lora_delta_exact_slots.argtypes = []
+            lib.lora_delta_exact_slots.restype = ctypes.c_int
+            lib.lora_delta_grads_exact_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
+            lib.lora_delta_grads_exact_workspace_size.restype = ctypes.c_size_t
+            lib.lora_delta_grads_exact.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp,
+                                                   _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            lib.lora_delta_grads_exact.restype = ctypes.c_int
+            lib.lora_delta_exact_combine.argtypes = [_vp, _vp, _i64, _vp, _vp]
+            lib.lora_delta_exact_combine.restype = ctypes.c_int
+            lib.lora_delta_exact_finalize.argtypes = [_vp, _i64, _vp, _vp]
+            lib.lora_delta_exact_finalize.restype = ctypes.c_int
         lib.lora_status_str.argtypes = [ctypes.c_int]
         lib.lora_status_str.restype = ctypes.c_char_p
         lib.lora_delta_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
@@ -187,6 +199,85 @@ def lora_delta_bwd(dy, x, a, b, u, alpha: float, *, dx=None, da=None, db=None, d
     if rc != LORA_OK:
         raise LoraDeltaError(rc, name)
     return dx, da, db, du
+
+
+def lora_delta_exact_slots() -> int:
+    """int64 slots of one exact-mode digit array (18 digits, then +inf, -inf and NaN counts)."""
+    return int(_lib().lora_delta_exact_slots())
+
+
+def lora_delta_grads_exact_workspace_size(M: int, K: int, N: int, R: int) -> int:
+    return int(_lib().lora_delta_grads_exact_workspace_size(M, K, N, R))
+
+
+def lora_delta_grads_exact(dy, x, u, du, alpha: float, *, da=None, db=None, da_digits=None,
+                           db_digits=None, want=("da", "db"), workspace=None, stream=None):
+    """Exact mode of the weight gradients (page "det-train", section "Method"):
+    dA = rn32(exact sum du^T x), dB = rn32(exact sum dv^T u), dv = bf16(fp32(dy * alpha)).
+
+    ``want`` names the outputs to allocate when not given: any of "da", "db",
+    "da_digits" ([R][K][slots] int64), "db_digits" ([N][R][slots] int64). Returns
+    the dict of outputs written. ``dy`` or ``x`` may be None when its gradient
+    is not wanted."""
+    M, R = (u if u is not None else du).shape
+    K = x.shape[1] if x is not None else 8
+    N = dy.shape[1] if dy is not None else 8
+    dev = (u if u is not None else du).device
+    slots = lora_delta_exact_slots()
+    shapes = {"da": ((R, K), torch.float32), "db": ((N, R), torch.float32),
+              "da_digits": ((R, K, slots), torch.int64), "db_digits": ((N, R, slots), torch.int64)}
+    outs = {"da": da, "db": db, "da_digits": da_digits, "db_digits": db_digits}
+    for k in want:
+        if outs[k] is None:
+            outs[k] = torch.empty(shapes[k][0], dtype=shapes[k][1], device=dev)
+    for k, v in outs.items():
+        if v is not None:
+            _check(v, k, shapes[k][1], shapes[k][0])
+    if x is not None:
+        _check(x, "x", torch.bfloat16, (M, K))
+    if dy is not None:
+        _check(dy, "dy", torch.bfloat16, (M, N))
+    if u is not None:
+        _check(u, "u", torch.bfloat16, (M, R))
+    if du is not None:
+        _check(du, "du", torch.bfloat16, (M, R))
+    if workspace is None:
+        workspace = new_workspace(lora_delta_grads_exact_workspace_size(M, K, N, R), dev)
+    rc = _lib().lora_delta_grads_exact(_ptr(dy), _ptr(x), _ptr(u), _ptr(du), float(alpha), M, K, N, R,
+                                       _ptr(outs["da"]), _ptr(outs["db"]), _ptr(outs["da_digits"]),
+                                       _ptr(outs["db_digits"]), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_grads_exact")
+    return {k: v for k, v in outs.items() if v is not None}
+
+
+def lora_delta_exact_combine(a, b, *, out=None, stream=None):
+    """Digit arrays of the sums: a + b (same shape [..., slots] int64), normalised; out may be a or b."""
+    if a.shape != b.shape or a.dtype != torch.int64 or b.dtype != torch.int64:
+        raise ValueError("digit arrays must be int64 tensors of one shape")
+    slots = lora_delta_exact_slots()
+    if a.shape[-1] != slots or not a.is_contiguous() or not b.is_contiguous():
+        raise ValueError(f"digit arrays: contiguous [..., {slots}] int64")
+    out = torch.empty_like(a) if out is None else out
+    _check(out, "out", torch.int64, tuple(a.shape))
+    rc = _lib().lora_delta_exact_combine(_ptr(a), _ptr(b), a.numel() // slots, _ptr(out), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_exact_combine")
+    return out
+
+
+def lora_delta_exact_finalize(digits, *, out=None, stream=None):
+    """FP32 values of digit arrays [..., slots] (rounded to nearest even, once)."""
+    slots = lora_delta_exact_slots()
+    if digits.dtype != torch.int64 or digits.shape[-1] != slots or not digits.is_contiguous():
+        raise ValueError(f"digit arrays: contiguous [..., {slots}] int64")
+    out = torch.empty(tuple(digits.shape[:-1]), dtype=torch.float32, device=digits.device) if out is None else out
+    _check(out, "out", torch.float32, tuple(digits.shape[:-1]))
+    rc = _lib().lora_delta_exact_finalize(_ptr(digits), digits.numel() // slots, _ptr(out), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_exact_finalize")
+    return out
 
 
 def lora_delta_device_status(workspace: torch.Tensor) -> int:

@@ -226,6 +226,65 @@ size_t lora_delta_describe(char *buf, size_t len);
 lora_status lora_delta_fwd_noalloc(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K,
                                    int64_t N, int64_t R, float *delta_y, void *u, void *stream);
 
+/*
+ * Exact mode of the weight gradients (page "det-train", sections "Method",
+ * "API" and "Correctness": a Kulisch long accumulator per output, partials
+ * composed by adding digit arrays, one rounding to FP32 at the end).
+ *
+ *   dA[r][k] = rn32( sum_m du[m][r] * x[m][k] )
+ *   dB[n][r] = rn32( sum_m dv[m][n] * u[m][r] ),  dv = bf16(fp32(dy[m][n] * alpha))
+ *
+ * where the sums are exact (every BF16 product is exact; the products are
+ * added as integers) and rn32 rounds to nearest even once. So dA and dB do not
+ * depend on the order of the rows, on the chunking or on how the rows are
+ * split between calls: the digit arrays of row shards, added with
+ * lora_delta_exact_combine (in any grouping), give the digit arrays of the
+ * whole, and lora_delta_exact_finalize rounds those to the same bits. Special
+ * values: a NaN product (a NaN factor, or inf * 0), or both an infinite
+ * positive and an infinite negative product, gives NaN; otherwise an infinite
+ * product gives that infinity; a sum beyond the FP32 range rounds to infinity;
+ * an exact zero sum is +0.
+ *
+ * Digit array: lora_delta_exact_slots() (= 21) int64 per output: 18 digits in
+ * radix 2^32, digit i weighing 2^(32 i - 266) (the bottom of the BF16 product
+ * range), then the counts of +inf, -inf and NaN products. The library writes
+ * them normalised (digits 0..16 in [0, 2^32), digit 17 signed), so equal sums
+ * give equal arrays, byte for byte.
+ *
+ * lora_delta_grads_exact: inputs as in lora_delta_bwd (du is the du output of
+ * the backward pass). Outputs, each optional (NULL: not written):
+ *   da        [R][K] fp32      da_digits [R][K][21] int64
+ *   db        [N][R] fp32      db_digits [N][R][21] int64
+ * dA is computed when da or da_digits is given, dB when db or db_digits is;
+ * the inputs it reads must then be non-NULL (x, du for dA; dy, u for dB) unless
+ * M = 0, which writes zero gradients (+0, and all-zero digit arrays).
+ * M < 2^30 (digit headroom); R * K and R * N below 2^31. workspace: >= lora_delta_grads_exact_workspace_size
+ * bytes of scratch (no status block: no kernel of this call waits).
+ * Kernels: per gradient, the digit kernel (integer accumulation over row
+ * chunks) and the reduce kernel (adds the chunks' digits, normalises, rounds).
+ * The call is much slower than lora_delta_bwd's dA and dB: integer units, not
+ * tensor cores.
+ */
+int lora_delta_exact_slots(void);
+size_t lora_delta_grads_exact_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
+lora_status lora_delta_grads_exact(const void *dy, const void *x, const void *u, const void *du, float alpha,
+                                   int64_t M, int64_t K, int64_t N, int64_t R, float *da, float *db,
+                                   int64_t *da_digits, int64_t *db_digits, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+/*
+ * out_digits = a + b over n digit arrays (n outputs, 21 int64 each), written
+ * normalised; out_digits may be a or b (in place). Inputs may be normalised
+ * or not, as long as every sum of a digit stays within int64 (digit arrays of
+ * fewer than 2^30 rows in all). Returns LORA_ERR_SHAPE for n < 0; n = 0 is a
+ * no-op.
+ */
+lora_status lora_delta_exact_combine(const int64_t *a, const int64_t *b, int64_t n, int64_t *out_digits,
+                                     void *stream);
+
+/* out[i] = FP32 value of digit array i (rounded to nearest even, once), i < n. */
+lora_status lora_delta_exact_finalize(const int64_t *digits, int64_t n, float *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -219,3 +219,44 @@ def test_f32dy_backward_host_checks(lib):
 
     if not torch.cuda.is_available():
         assert call() in (6, 7)
+
+
+def test_exact_mode_host_checks(lib):
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    assert ld.lora_delta_exact_slots() == 21
+    need = ld.lora_delta_grads_exact_workspace_size(300, 136, 72, 16)
+    # segments of the digit kernel: units (64 rows of a 16 x 64 output tile) 3 tiles x 5 = 15 for
+    # dA (K = 136), so at most 15 CTAs and 15 + 3 segments; per segment and tile output a 16-byte
+    # record and a 21-int64 digit array; the larger gradient's, 256-byte rounded
+    assert need == ((18 * 1024 * (16 + 21 * 8) + 255) // 256) * 256
+    assert ld.lora_delta_grads_exact_workspace_size(1 << 30, 128, 96, 16) == 0   # M below 2^30
+    assert ld.lora_delta_grads_exact_workspace_size(64, 100, 96, 16) == 0
+    f = lib.lora_delta_grads_exact
+    ok = [FAKE] * 9
+
+    def call(p=ok, M=64, K=128, N=96, R=16, ws=1 << 30):
+        dy, x, u, du, da, db, dad, dbd, w = p
+        return f(dy, x, u, du, 2.0, M, K, N, R, da, db, dad, dbd, w, ws, None)
+
+    assert call([FAKE] * 4 + [None] * 4 + [FAKE]) == 0          # nothing asked for: a no-op
+    assert call([None] + ok[1:]) == 1                            # dB asked for without dy
+    assert call(ok[:3] + [None] + ok[4:]) == 1                   # dA asked for without du
+    assert call([None, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE]) != 1   # dA alone needs no dy
+    assert call(ok[:8] + [None]) == 1                            # workspace
+    assert call(K=100) == 2
+    assert call(M=1 << 30) == 2
+    assert call(R=12) == 4
+    assert call(ok[:4] + [FAKE + 4] + ok[5:]) == 3
+    assert call(ws=ld.lora_delta_grads_exact_workspace_size(64, 128, 96, 16) - 8) == 5
+    assert lib.lora_delta_exact_combine(FAKE, FAKE, -1, FAKE, None) == 2
+    assert lib.lora_delta_exact_combine(FAKE, FAKE, 0, FAKE, None) == 0
+    assert lib.lora_delta_exact_combine(FAKE, None, 4, FAKE, None) == 1
+    assert lib.lora_delta_exact_finalize(FAKE, -1, FAKE, None) == 2
+    assert lib.lora_delta_exact_finalize(None, 4, FAKE, None) == 1
+    import torch
+
+    if not torch.cuda.is_available():
+        assert call() in (6, 7)
+        assert call(M=0) in (6, 7)                                # M = 0 still writes zero gradients
+        assert lib.lora_delta_exact_finalize(FAKE, 4, FAKE, None) in (6, 7)
