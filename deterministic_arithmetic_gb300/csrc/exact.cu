@@ -21,21 +21,27 @@
 // exact_digits_kernel: persistent CTAs (two per SM) over work units, a unit being
 // 64 rows of one 16 x 64 output tile (units numbered tile by tile); CTA c takes
 // the units [c U / G, (c + 1) U / G) and handles each run of them that lies in
-// one tile as a segment, numbered c + t (t the tile). The rows are decoded 64 at
-// a time into (m, s) pairs in shared memory. Each thread owns two outputs and
-// keeps, for each, a window accumulator in registers: a signed 64-bit sum of
-// m1 m2 2^(pos - anc) over the products whose position lies in [anc, anc + 30]
-// (one IMAD.WIDE per product; at most 2^16 rows per window keep it below
-// 2^62, so a longer segment adds its window to the digits every 2^16 rows).
-// Before each 64 rows the window is anchored (or moved up, after adding it to the
-// digits) so that the largest product the rows can hold -- at the position of
-// the sum of the column maxima of s -- lies 24 bits above the anchor; the
-// products below the window (none for data of ordinary range), and the
-// infinite and NaN ones,
-// and the infinite and NaN ones, are added straight into the output's digit
-// array of the segment in global memory (owned by the thread; zeroed at its
-// first use). Each segment leaves one record per output: the window (acc, anc)
-// and whether its digit array was used.
+// one tile as a segment, numbered c + t (t the tile). The raw rows of the next
+// unit are copied into shared memory (cp.async) while the current one computes.
+//
+// Per unit, every factor is written as a fixed-point integer scaled to its
+// column: with E the biased exponent and C the largest E over the column's
+// non-zero finite values in the 64 rows, the factor +-mag 2^(E' - 134) (mag the
+// significand with its leading bit, E' = max(E, 1)) becomes
+// f = +-mag 2^(E' - C + 20), an integer below 2^28 whenever E' >= C - 20. Then
+// each product is one IMAD.WIDE, f_l f_r < 2^56, and a thread's 64-row sum S
+// (below 2^62) of an output is exact at the unit position C_l + C_r - 42
+// (counted from 2^-266). S is added, shifted, into a 128-bit window in
+// registers (anchor set 20 bits below the first S's position, which leaves 41
+// bits of room above it), or -- out of the window's range -- straight into the
+// output's digit array of the segment in global memory (owned by the thread;
+// zeroed at its first use). Factors more than 20 bits below their column's
+// largest ("small"; none in data of ordinary range) are written as 0 and their
+// products are added exactly one by one from the raw values; so are all the
+// products of 64 rows holding an infinite or NaN value (whose products go to
+// the counters), or more small factors than the list of them holds. Each
+// segment leaves one record per output: the window and whether its digit array
+// was used.
 // exact_reduce_kernel adds, per output, the windows and digit arrays of the
 // segments of its tile, and writes the normalised digits or rounds them.
 #include <algorithm>
@@ -47,47 +53,30 @@ namespace lora {
 
 namespace {
 
-constexpr int kTP = 16, kTQ = 64;                      // output tile [p][q]
-constexpr int kRows = 64;                              // rows decoded per step
-constexpr int kThreads = 512;                          // two outputs (p, p + 1) per thread
-// Exponent codes s of the factors that are not finite non-zero values, and the ranges of e = s1 + s2
-// they give: finite * finite in [-266, 240]; finite * 0 in [-20133, -19880]; 0 * 0 = -40000;
-// inf * finite in [867, 1120]; inf * 0 = -19000; inf * inf = 2000; NaN * finite in [3867, 4120];
-// NaN * 0 = -16000; NaN * inf = 5000; NaN * NaN = 8000.
-constexpr int kZero = -20000, kInf = 1000, kNaN = 4000;
-constexpr int kWindow = 30;                            // highest position above the anchor
-constexpr int kBelowTop = 24;                          // anchor = the largest possible product's position - this
-constexpr int kNone = -100000;                         // column maximum of a column with no non-zero finite value
-constexpr int kNoneMin = 100000;                       // its column minimum
-constexpr int kUnset = -100000;                        // window offset before its anchor is set
-constexpr int kFlushBlocks = (1 << 16) / kRows;         // window headroom: 2^16 products below 2^46 each
-constexpr int kOut = kTP * kTQ;                        // outputs per tile
+constexpr int kTP = 16, kTQ = 64;                // output tile [p][q]
+constexpr int kOut = kTP * kTQ;                  // outputs per tile
+constexpr int kRows = 64;                        // rows per unit
+constexpr int kThreads = 512;                    // two outputs (p, p + 1) per thread
+constexpr int kScale = 20;                       // fixed-point bits below a column's largest exponent
+constexpr int kWinBelow = 20;                    // window anchor: this far below the first step sum's position
+constexpr int kWinAbove = 41;                    // highest step-sum shift the 128-bit window takes
+constexpr int kMaxSmall = 256;                   // small factors listed per unit
+constexpr int kFlushUnits = 1 << 16;             // window headroom (2^24 step sums below 2^103 each)
 
-// BF16 -> (m, s), value = m * 2^s; zero: (0, kZero); inf: (+-1, kInf); NaN: (0, kNaN)
-__device__ __forceinline__ int2 decode_bf16(uint32_t h) {
-  const int e = int(h >> 7) & 0xFF, f = int(h) & 0x7F;
-  const bool neg = (h & 0x8000u) != 0u;
-  if (e == 0xFF) return f ? make_int2(0, kNaN) : make_int2(neg ? -1 : 1, kInf);
-  const int mag = e ? (f | 0x80) : f;
-  return make_int2(neg ? -mag : mag, mag ? (e ? e : 1) - 134 : kZero);
-}
-
-__device__ __forceinline__ bool special_product(int e) { return e > 600 || (e > -19500 && e < -1000); }
-
-// 2^sh for sh in [0, 31), 0 for sh < 0 or sh >= 32 (PTX clamps the shift amount, read unsigned)
-__device__ __forceinline__ int pow2_or_zero(int sh) {
-  int r;
-  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(1), "r"(sh));
-  return r;
-}
-
-// The window of one output: acc * 2^(anc - 266), anc = 266 - off (off = kUnset: no anchor yet),
-// and whether the output's digit array for the segment has been used.
-struct Win {
-  long long acc;
-  int off;
-  int used;
+// 128-bit two's complement accumulator
+struct I128 {
+  unsigned long long lo;
+  long long hi;
 };
+
+// v * 2^sh (0 <= sh < 64) added into a
+__device__ __forceinline__ void add_shifted(I128& a, long long v, int sh) {
+  const unsigned long long lo = (unsigned long long)v << sh;
+  const long long hi = sh ? (v >> (64 - sh)) : (v >> 63);
+  const unsigned long long s = a.lo + lo;
+  a.hi += hi + (s < lo ? 1 : 0);
+  a.lo = s;
+}
 
 // The digit array of one output for one segment: dig[slot * kOut] (global memory, owned by
 // one thread), zeroed at its first use.
@@ -98,90 +87,138 @@ __device__ __forceinline__ void touch(long long* dig, int& used) {
   }
 }
 
-// the window's value into the digit array (the window keeps its anchor, emptied)
-__device__ __forceinline__ void spill_window(Win& w, long long* dig) {
-  if (w.off == kUnset || w.acc == 0) return;
-  touch(dig, w.used);
-  const int anc = 266 - w.off, d = anc >> 5, sa = anc & 31;
-  const unsigned long long lo = (unsigned long long)w.acc << sa;
-  const long long hi = sa ? (w.acc >> (64 - sa)) : (w.acc >> 63);   // acc * 2^sa = hi * 2^64 + lo
+// (hi : lo) * 2^(pos - 266) into the digits, pos in [0, 446] (window anchors): words d .. d + 4
+// of v * 2^(pos & 31)
+__device__ __forceinline__ void digits_add128(long long* dig, int& used, I128 v, int pos) {
+  touch(dig, used);
+  const int d = pos >> 5, sa = pos & 31;
+  const unsigned long long lo = v.lo << sa;
+  const unsigned long long mid = sa ? (v.lo >> (64 - sa)) | ((unsigned long long)v.hi << sa) : (unsigned long long)v.hi;
+  const long long top = sa ? (v.hi >> (64 - sa)) : (v.hi >> 63);
+  dig[d * kOut] += (long long)(lo & 0xFFFFFFFFull);
+  dig[(d + 1) * kOut] += (long long)(lo >> 32);
+  dig[(d + 2) * kOut] += (long long)(mid & 0xFFFFFFFFull);
+  dig[(d + 3) * kOut] += (long long)(mid >> 32);
+  dig[(d + 4) * kOut] += top;
+}
+
+// v * 2^(pos - 266) into the digits, pos <= 506 (a negative pos: v is then a multiple of
+// 2^-pos, every product's unit lying at position >= 0): words d, d + 1 of v * 2^(pos & 31)
+// and the signed rest in d + 2
+__device__ __forceinline__ void digits_add64(long long* dig, int& used, long long v, int pos) {
+  if (v == 0) return;
+  if (pos < 0) {
+    v >>= -pos;
+    pos = 0;
+  }
+  touch(dig, used);
+  const int d = pos >> 5, sa = pos & 31;
+  const unsigned long long lo = (unsigned long long)v << sa;
+  const long long hi = sa ? (v >> (64 - sa)) : (v >> 63);
   dig[d * kOut] += (long long)(lo & 0xFFFFFFFFull);
   dig[(d + 1) * kOut] += (long long)(lo >> 32);
   dig[(d + 2) * kOut] += hi;
-  w.acc = 0;
 }
 
-// a product the window did not take: mm * 2^e (e = s1 + s2); returns the new window
-__device__ __forceinline__ Win slow_product(Win w, long long* dig, int mm, int e) {
-  if (special_product(e)) {   // an infinite or NaN factor
-    touch(dig, w.used);
-    const bool nan = e > 3000 || e < 0;   // a NaN factor, or inf * 0
-    dig[(nan ? kDigits + 2 : (mm < 0 ? kDigits + 1 : kDigits)) * kOut] += 1;
-    return w;
+// one product of raw BF16 values a * b into the digits or the special counters
+__device__ __forceinline__ void digits_product(long long* dig, int& used, uint32_t a, uint32_t b) {
+  const int ea = int(a >> 7) & 0xFF, eb = int(b >> 7) & 0xFF;
+  const bool za = (a & 0x7FFFu) == 0u, zb = (b & 0x7FFFu) == 0u;
+  const bool nega = (a & 0x8000u) != 0u, negb = (b & 0x8000u) != 0u;
+  if (ea == 0xFF || eb == 0xFF) {   // inf or NaN: NaN for a NaN factor or inf * 0
+    const bool nan = (ea == 0xFF && (a & 0x7Fu)) || (eb == 0xFF && (b & 0x7Fu)) || za || zb;
+    touch(dig, used);
+    dig[(nan ? kDigits + 2 : (nega != negb ? kDigits + 1 : kDigits)) * kOut] += 1;
+    return;
   }
-  if (e < -1000) return w;                             // a zero factor
-  const int pos = e + 266;                             // in [0, 506]; mm != 0
-  if (w.off != kUnset && pos < 266 - w.off) {          // below the window: straight into the digits
-    touch(dig, w.used);
-    const long long v = (long long)mm << (pos & 31);   // |v| < 2^47
-    const int d = pos >> 5;
-    dig[d * kOut] += (long long)(uint32_t)v;           // low word, unsigned
-    dig[(d + 1) * kOut] += v >> 32;                    // the rest, signed
-    return w;
-  }
-  // above the window, or no window yet: not reached when the window is anchored under the
-  // rows' largest possible product, but kept exact all the same -- a new window, this
-  // product near its top
-  spill_window(w, dig);
-  const int anc = max(pos - kBelowTop, 0);
-  w.off = 266 - anc;
-  w.acc = (long long)mm << (pos - anc);
-  return w;
+  if (za || zb) return;
+  const int ma = (ea ? 0x80 : 0) | int(a & 0x7Fu), mb = (eb ? 0x80 : 0) | int(b & 0x7Fu);
+  const long long v = (long long)(nega != negb ? -(ma * mb) : ma * mb);
+  digits_add64(dig, used, v, max(ea, 1) + max(eb, 1) - 268 + 266);
 }
 
-__device__ __forceinline__ long long record_tag(const Win& w) {
-  return (long long)(uint32_t)(w.off == kUnset ? -1 : 266 - w.off) | ((long long)w.used << 32);
+// 16-byte asynchronous copy global -> shared; bytes = 0 fills the 16 bytes with zeros
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(uint32_t(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// shared memory of the digit kernel
+struct ExactSmem {
+  uint16_t raw_l[2][kRows][kTP];   // raw BF16 rows (dV for the right rows of dB), double-buffered
+  uint16_t raw_r[2][kRows][kTQ];
+  int fl[kRows][kTP];              // fixed-point factors
+  int fr[kRows][kTQ];
+  int cl_part[kRows / 2][kTP];     // column maxima of E' per decoding thread
+  int cr_part[kRows / 8][kTQ];
+  int cl[kTP], cr[kTQ];            // column maxima of E' over the 64 rows (0: no non-zero finite value)
+  uint32_t small[kMaxSmall];       // small factors: right << 31 | row << 16 | column
+  int n_small;
+};
+
+// Start the copies of unit u's raw rows into buffer b (one 16-byte chunk of the right rows per
+// thread, one of the left rows for the first 128 threads; zeros past M, P and Q).
+__device__ __forceinline__ void fetch_unit(ExactSmem& sm, int b, int64_t u, int B, int n_tq, const uint16_t* left,
+                                           int ldl, const uint16_t* right, int ldr, int M, int P, int Q) {
+  const int tile = int(u / B);
+  const int m0 = int(u - int64_t(tile) * B) * kRows;
+  const int q0 = (tile % n_tq) * kTQ, p0 = (tile / n_tq) * kTP;
+  const int tid = threadIdx.x;
+  {
+    const int r = tid / (kTQ / 8), c8 = (tid % (kTQ / 8)) * 8;   // 512 chunks: 64 rows x 8
+    const bool ok = m0 + r < M && q0 + c8 < Q;
+    cp_async16(&sm.raw_r[b][r][c8], ok ? right + size_t(m0 + r) * ldr + q0 + c8 : right, ok ? 16 : 0);
+  }
+  if (tid < kRows * (kTP / 8)) {
+    const int r = tid / (kTP / 8), c8 = (tid % (kTP / 8)) * 8;   // 128 chunks: 64 rows x 2
+    const bool ok = m0 + r < M && p0 + c8 < P;
+    cp_async16(&sm.raw_l[b][r][c8], ok ? left + size_t(m0 + r) * ldl + p0 + c8 : left, ok ? 16 : 0);
+  }
 }
 
-// How the rows' products are checked: kFree -- every non-zero product lies in the window (known
-// from the column extremes): no check; kBelow -- finite values, some products may lie below the
-// window; kSpecial -- infinite or NaN values among the rows.
-enum RowMode { kFree, kBelow, kSpecial };
+// E' of a non-zero finite BF16 value, 0 for zeros, -1 for inf and NaN
+__device__ __forceinline__ int eff_exp(uint32_t h) {
+  const int e = int(h >> 7) & 0xFF;
+  return e == 0xFF ? -1 : ((h & 0x7FFFu) ? max(e, 1) : 0);
+}
 
-// The products of rows [0, nr) of the decoded tile for this thread's two outputs (2 pg, q) and
-// (2 pg + 1, q): each adds m1 m2 2^sh to the window when sh = e + off is in [0, 30] (and 0
-// otherwise: below the window, or a zero, infinite or NaN factor, whose e lies far outside),
-// and the ones the window does not take go to slow_product.
-template <int MODE>
-__device__ __forceinline__ void window_rows(const int4 (*lft)[kTP / 2], const int2 (*rgt)[kTQ], int nr, int q, int pg,
-                                            Win& wa, Win& wb, long long* dig_a, long long* dig_b) {
-  for (int r0 = 0; r0 < nr; r0 += 4) {
-    int2 rv[4];
-    int4 lv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      rv[j] = rgt[r0 + j][q];
-      lv[j] = lft[r0 + j][pg];
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int mm0 = lv[j].x * rv[j].x, mm1 = lv[j].z * rv[j].x;
-      const int sh0 = lv[j].y + rv[j].y + wa.off, sh1 = lv[j].w + rv[j].y + wb.off;
-      wa.acc += (long long)mm0 * pow2_or_zero(sh0);
-      wb.acc += (long long)mm1 * pow2_or_zero(sh1);
-      if (MODE != kFree) {
-        const int e0 = lv[j].y + rv[j].y, e1 = lv[j].w + rv[j].y;
-        const bool out0 = MODE == kBelow ? (sh0 < 0 && e0 > -1000)
-                                         : (special_product(e0) || (e0 > -1000 && unsigned(sh0) > unsigned(kWindow)));
-        const bool out1 = MODE == kBelow ? (sh1 < 0 && e1 > -1000)
-                                         : (special_product(e1) || (e1 > -1000 && unsigned(sh1) > unsigned(kWindow)));
-        if (out0 | out1) {
-          if (out0) wa = slow_product(wa, dig_a, mm0, e0);
-          if (out1) wb = slow_product(wb, dig_b, mm1, e1);
-        }
-      }
-    }
+// the fixed-point factor of h in a column whose largest E' is c; small: set when h needs
+// more than kScale bits below c (the factor is then 0)
+__device__ __forceinline__ int fixed_factor(uint32_t h, int c, bool& small) {
+  const int e = int(h >> 7) & 0xFF;
+  if ((h & 0x7FFFu) == 0u || e == 0xFF) return 0;
+  const int sh = max(e, 1) - c + kScale;
+  if (sh < 0) {
+    small = true;
+    return 0;
   }
+  const int v = ((e ? 0x80 : 0) | int(h & 0x7Fu)) << sh;
+  return (h & 0x8000u) ? -v : v;
+}
+
+// The window of one output: a 128-bit sum at anchor anc (-1: none yet) and whether the
+// output's digit array for the segment has been used.
+struct Win {
+  I128 acc;
+  int anc;
+  int used;
+};
+
+// the 64-row sum s at unit position pos added to the window (or, outside its range, to the digits)
+__device__ __forceinline__ void window_fold(Win& w, long long* dig, long long s, int pos) {
+  if (s == 0) return;
+  if (w.anc < 0) w.anc = max(pos - kWinBelow, 0);
+  const int sh = pos - w.anc;
+  if (sh >= 0 && sh <= kWinAbove) add_shifted(w.acc, s, sh);
+  else digits_add64(dig, w.used, s, pos);
+}
+
+__device__ __forceinline__ void window_spill(Win& w, long long* dig) {
+  if (w.anc >= 0 && (w.acc.lo != 0 || w.acc.hi != 0)) digits_add128(dig, w.used, w.acc, w.anc);
+  w.acc = I128{0, 0};
 }
 
 // CTA of unit u when U units are split among G CTAs as [c U / G, (c + 1) U / G)
@@ -189,122 +226,162 @@ __host__ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int G)
   return int(((u + 1) * G - 1) / U);
 }
 
+// Segment record of one output: the window (lo, hi) and anc | used << 32 (anc = -1: none)
+struct ExactRec {
+  unsigned long long lo;
+  long long hi;
+  long long tag;
+  long long pad;
+};
+
 // DV: the right operand is dV = bf16(fp32(dy * alpha)), formed from dY.
 // Tiles: t = tp * n_tq + tq (16 rows of P by 64 columns of Q); B row blocks of 64 per tile.
-// rec[seg][o]: (window acc, anchor (-1: none) | digits-used << 32); spill[seg][slot][o],
-// o = (p - p0) * 64 + (q - q0), seg = c + t.
+// rec[seg][o], spill[seg][slot][o] with o = (p - p0) * 64 + (q - q0), seg = c + t.
+// Left and right rows are 16-byte aligned (P, Q, ldl, ldr multiples of 8).
 template <bool DV>
 __global__ void __launch_bounds__(kThreads, 2)
     exact_digits_kernel(const uint16_t* __restrict__ left, int ldl, const uint16_t* __restrict__ right, int ldr,
-                        int M, int P, int Q, int n_tq, int B, int64_t U, float alpha, longlong2* __restrict__ rec,
+                        int M, int P, int Q, int n_tq, int B, int64_t U, float alpha, ExactRec* __restrict__ rec,
                         long long* __restrict__ spill) {
   grid_dependency_wait();
   grid_dependents_launch();
-  __shared__ int4 lft[kRows][kTP / 2];   // (m, s) of left columns 2i and 2i + 1
-  __shared__ int2 rgt[kRows][kTQ];
-  __shared__ int2 wl[kRows / 2][kTP], wr[kRows / 8][kTQ];   // column (max, min) of s per staging thread
-  __shared__ int2 ext_l[kTP], ext_r[kTQ];                     // column (max, min) of s over the 64 rows
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  ExactSmem& sm = *reinterpret_cast<ExactSmem*>(smem_raw);
   const int tid = threadIdx.x, q = tid % kTQ, pg = tid / kTQ;   // outputs (2 pg, q) and (2 pg + 1, q)
   const int oa = 2 * pg * kTQ + q, ob = oa + kTQ;               // their indexes in the tile
   const int G = gridDim.x, c = blockIdx.x;
-  int2* l2 = reinterpret_cast<int2*>(&lft[0][0]);
-  const int64_t u_end = (int64_t(c) + 1) * U / G;
-  for (int64_t u = int64_t(c) * U / G; u < u_end;) {
-    const int tile = int(u / B);
-    const int64_t seg_end = std::min<int64_t>(u_end, (int64_t(tile) + 1) * B);
-    const int q0 = (tile % n_tq) * kTQ, p0 = (tile / n_tq) * kTP;
-    const size_t seg = size_t(c) + tile;
-    long long* dig_a = spill + seg * kExactSlots * kOut + oa;
-    long long* dig_b = spill + seg * kExactSlots * kOut + ob;
-    Win wa{0, kUnset, 0}, wb{0, kUnset, 0};
-    int blocks = 0;
-    for (; u < seg_end; ++u) {
-      const int m0 = int(u - int64_t(tile) * B) * kRows, m_end = min(M, m0 + kRows);
-      __syncthreads();   // previous rows consumed
-      // decode the rows: left column tid % 16, rows 2 (tid / 16) and the next; right column
-      // tid % 64, rows 8 (tid / 64) .. + 7; zeros past M, P and Q. special: an infinite or NaN
-      // value among them; the column extremes of s over non-zero finite values.
-      int special = 0;
-      {
-        const int p = tid % kTP, rp = tid / kTP;
-        int mx = kNone, mn = kNoneMin;
+  const int dl_p = tid % kTP, dl_r = 2 * (tid / kTP);           // decoding: left column, first of two rows
+  const int dr_r = 8 * (tid / kTQ);                             // right column q, first of eight rows
+  const int64_t u_begin = int64_t(c) * U / G, u_end = (int64_t(c) + 1) * U / G;
+  if (u_begin < u_end) fetch_unit(sm, 0, u_begin, B, n_tq, left, ldl, right, ldr, M, P, Q);
+  cp_async_commit();
+  int tile = -1, units = 0;
+  size_t seg = 0;
+  long long *dig_a = spill, *dig_b = spill;
+  Win wa{{0, 0}, -1, 0}, wb{{0, 0}, -1, 0};
+  for (int64_t u = u_begin; u < u_end; ++u) {
+    const int buf = int((u - u_begin) & 1);
+    if (u / B != tile) {   // a new segment
+      tile = int(u / B);
+      seg = size_t(c) + tile;
+      dig_a = spill + seg * kExactSlots * kOut + oa;
+      dig_b = spill + seg * kExactSlots * kOut + ob;
+      wa = Win{{0, 0}, -1, 0};
+      wb = Win{{0, 0}, -1, 0};
+      units = 0;
+    }
+    cp_async_wait_all();   // this thread's copies of unit u have landed
+    __syncthreads();       // everyone's; the previous unit's factors consumed; buffer buf ^ 1 free
+    if (u + 1 < u_end) fetch_unit(sm, buf ^ 1, u + 1, B, n_tq, left, ldl, right, ldr, M, P, Q);
+    cp_async_commit();
+    if (tid == 0) sm.n_small = 0;
+    // pass 1: dV (dB), column maxima of E', inf / NaN
+    int special = 0;
+    {
+      int mx = 0;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int r = 2 * rp + k, m = m0 + r;
-          const uint32_t h = (m < m_end && p0 + p < P) ? left[size_t(m) * ldl + p0 + p] : 0u;
-          special |= (h & 0x7F80u) == 0x7F80u;
-          const int2 d = decode_bf16(h);
-          l2[r * kTP + p] = d;
-          if (d.x != 0 && d.y < 600) mx = max(mx, d.y), mn = min(mn, d.y);
-        }
-        wl[rp][p] = make_int2(mx, mn);
+      for (int k = 0; k < 2; ++k) {
+        const int e = eff_exp(sm.raw_l[buf][dl_r + k][dl_p]);
+        special |= e < 0;
+        mx = max(mx, e);
       }
-      {
-        const int rg = tid / kTQ;
-        const bool qin = q0 + q < Q;
-        int mx = kNone, mn = kNoneMin;
+      sm.cl_part[dl_r / 2][dl_p] = mx;
+      mx = 0;
 #pragma unroll
-        for (int k = 0; k < kRows / 8; ++k) {
-          const int r = 8 * rg + k, m = m0 + r;
-          uint32_t h = (m < m_end && qin) ? right[size_t(m) * ldr + q0 + q] : 0u;
-          if (DV) h = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__uint_as_float(h << 16), alpha)));
-          special |= (h & 0x7F80u) == 0x7F80u;
-          const int2 d = decode_bf16(h);
-          rgt[r][q] = d;
-          if (d.x != 0 && d.y < 600) mx = max(mx, d.y), mn = min(mn, d.y);
+      for (int k = 0; k < 8; ++k) {
+        uint32_t h = sm.raw_r[buf][dr_r + k][q];
+        if (DV) {
+          h = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__uint_as_float(h << 16), alpha)));
+          sm.raw_r[buf][dr_r + k][q] = uint16_t(h);
         }
-        wr[rg][q] = make_int2(mx, mn);
+        const int e = eff_exp(h);
+        special |= e < 0;
+        mx = max(mx, e);
       }
-      const bool any_special = __syncthreads_or(special);
-      if (tid < kTP) {
-        int2 x = make_int2(kNone, kNoneMin);
-        for (int i = 0; i < kRows / 2; ++i) x = make_int2(max(x.x, wl[i][tid].x), min(x.y, wl[i][tid].y));
-        ext_l[tid] = x;
-      } else if (tid >= 2 * kTQ && tid < 3 * kTQ) {
-        int2 x = make_int2(kNone, kNoneMin);
-        for (int i = 0; i < kRows / 8; ++i)
-          x = make_int2(max(x.x, wr[i][tid - 2 * kTQ].x), min(x.y, wr[i][tid - 2 * kTQ].y));
-        ext_r[tid - 2 * kTQ] = x;
-      }
-      __syncthreads();
-      // windows: anchored (or moved up, after adding them to the digits) so that the largest
-      // product these rows can hold sits kBelowTop bits above the anchor; free: the smallest
-      // non-zero one lies in the window too
-      bool free = true;
-      {
-        const int2 er = ext_r[q], ea = ext_l[2 * pg], eb = ext_l[2 * pg + 1];
-        if (er.x != kNone && ea.x != kNone) {
-          const int top = ea.x + er.x + 266;
-          if (wa.off == kUnset || top > 266 - wa.off + kWindow) {
-            spill_window(wa, dig_a);
-            wa.off = 266 - max(top - kBelowTop, 0);
-          }
-          free = free && ea.y + er.y + wa.off >= 0;
-        }
-        if (er.x != kNone && eb.x != kNone) {
-          const int top = eb.x + er.x + 266;
-          if (wb.off == kUnset || top > 266 - wb.off + kWindow) {
-            spill_window(wb, dig_b);
-            wb.off = 266 - max(top - kBelowTop, 0);
-          }
-          free = free && eb.y + er.y + wb.off >= 0;
+      sm.cr_part[dr_r / 8][q] = mx;
+    }
+    const bool any_special = __syncthreads_or(special);
+    if (tid < kTP) {
+      int mx = 0;
+      for (int i = 0; i < kRows / 2; ++i) mx = max(mx, sm.cl_part[i][tid]);
+      sm.cl[tid] = mx;
+    } else if (tid >= 2 * kTQ && tid < 3 * kTQ) {
+      int mx = 0;
+      for (int i = 0; i < kRows / 8; ++i) mx = max(mx, sm.cr_part[i][tid - 2 * kTQ]);
+      sm.cr[tid - 2 * kTQ] = mx;
+    }
+    __syncthreads();
+    // pass 2: the fixed-point factors; small ones listed
+    {
+      const int c_l = sm.cl[dl_p];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        bool s = false;
+        sm.fl[dl_r + k][dl_p] = fixed_factor(sm.raw_l[buf][dl_r + k][dl_p], c_l, s);
+        if (s) {
+          const int i = atomicAdd(&sm.n_small, 1);
+          if (i < kMaxSmall) sm.small[i] = uint32_t((dl_r + k) << 16 | dl_p);
         }
       }
-      const int nr = m_end - m0;   // rows past nr hold zeros: adding them changes nothing
-      if (any_special)
-        window_rows<kSpecial>(lft, rgt, nr, q, pg, wa, wb, dig_a, dig_b);
-      else if (__all_sync(0xFFFFFFFFu, free))
-        window_rows<kFree>(lft, rgt, nr, q, pg, wa, wb, dig_a, dig_b);
-      else
-        window_rows<kBelow>(lft, rgt, nr, q, pg, wa, wb, dig_a, dig_b);
-      if (++blocks == kFlushBlocks) {   // 2^16 rows in the window: empty it into the digits
-        spill_window(wa, dig_a);
-        spill_window(wb, dig_b);
-        blocks = 0;
+      const int c_r = sm.cr[q];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        bool s = false;
+        sm.fr[dr_r + k][q] = fixed_factor(sm.raw_r[buf][dr_r + k][q], c_r, s);
+        if (s) {
+          const int i = atomicAdd(&sm.n_small, 1);
+          if (i < kMaxSmall) sm.small[i] = 0x80000000u | uint32_t((dr_r + k) << 16 | q);
+        }
       }
     }
-    rec[seg * kOut + oa] = make_longlong2(wa.acc, record_tag(wa));
-    rec[seg * kOut + ob] = make_longlong2(wb.acc, record_tag(wb));
+    __syncthreads();
+    const int n_small = sm.n_small;
+    if (any_special || n_small > kMaxSmall) {
+      // every product of these rows, one by one from the raw values
+      for (int r = 0; r < kRows; ++r) {
+        const uint32_t hr = sm.raw_r[buf][r][q];
+        digits_product(dig_a, wa.used, sm.raw_l[buf][r][2 * pg], hr);
+        digits_product(dig_b, wb.used, sm.raw_l[buf][r][2 * pg + 1], hr);
+      }
+    } else {
+      long long sa = 0, sb = 0;
+#pragma unroll 8
+      for (int r = 0; r < kRows; ++r) {
+        const int fr = sm.fr[r][q];
+        const int2 fl = *reinterpret_cast<const int2*>(&sm.fl[r][2 * pg]);
+        sa += (long long)fl.x * fr;
+        sb += (long long)fl.y * fr;
+      }
+      const int crq = sm.cr[q];
+      window_fold(wa, dig_a, sa, sm.cl[2 * pg] + crq - 2 * kScale - 2);
+      window_fold(wb, dig_b, sb, sm.cl[2 * pg + 1] + crq - 2 * kScale - 2);
+      // the small factors' products, exactly (a product of two small factors once: with the
+      // left one's entry)
+      for (int i = 0; i < n_small; ++i) {
+        const uint32_t e = sm.small[i];
+        const int r = int(e >> 16) & 0x7FFF, col = int(e & 0xFFFFu);
+        if (e >> 31) {   // right factor (r, col): with every left factor of row r that is not small
+          if (col != q) continue;
+          const uint32_t hr = sm.raw_r[buf][r][q];
+          const uint32_t la = sm.raw_l[buf][r][2 * pg], lb = sm.raw_l[buf][r][2 * pg + 1];
+          if (sm.fl[r][2 * pg] != 0) digits_product(dig_a, wa.used, la, hr);
+          if (sm.fl[r][2 * pg + 1] != 0) digits_product(dig_b, wb.used, lb, hr);
+        } else {         // left factor (r, col): with every right factor of row r
+          if ((col >> 1) != pg) continue;
+          if (col & 1) digits_product(dig_b, wb.used, sm.raw_l[buf][r][col], sm.raw_r[buf][r][q]);
+          else digits_product(dig_a, wa.used, sm.raw_l[buf][r][col], sm.raw_r[buf][r][q]);
+        }
+      }
+    }
+    if (++units == kFlushUnits) {   // window headroom
+      window_spill(wa, dig_a);
+      window_spill(wb, dig_b);
+      units = 0;
+    }
+    if (u + 1 == u_end || (u + 1) / B != tile) {   // the segment ends: its records
+      rec[seg * kOut + oa] = ExactRec{wa.acc.lo, wa.acc.hi, (long long)(uint32_t)wa.anc | ((long long)wa.used << 32), 0};
+      rec[seg * kOut + ob] = ExactRec{wb.acc.lo, wb.acc.hi, (long long)(uint32_t)wb.anc | ((long long)wb.used << 32), 0};
+    }
   }
 }
 
@@ -387,7 +464,7 @@ __device__ __forceinline__ size_t out_index(int p, int q, int P, int Q, int tran
 // the windows and digit arrays of the segments of each output's tile added; written
 // normalised to out_digits ([outputs][kExactSlots], outputs in out_index order) and/or
 // rounded to out
-__global__ void __launch_bounds__(256) exact_reduce_kernel(const longlong2* __restrict__ rec,
+__global__ void __launch_bounds__(256) exact_reduce_kernel(const ExactRec* __restrict__ rec,
                                                            const long long* __restrict__ spill, int P, int Q,
                                                            int n_tq, int B, int64_t U, int G, int transpose,
                                                            long long* __restrict__ out_digits,
@@ -405,17 +482,24 @@ __global__ void __launch_bounds__(256) exact_reduce_kernel(const longlong2* __re
     const int c0 = cta_of_unit(int64_t(tile) * B, U, G), c1 = cta_of_unit((int64_t(tile) + 1) * B - 1, U, G);
     for (int cta = c0; cta <= c1; ++cta) {
       const size_t seg = size_t(cta) + tile;
-      const longlong2 r = rec[seg * kOut + o];
-      const int anc = int(r.y & 0xFFFFFFFF);
-      if (anc >= 0) {   // window acc * 2^(anc - 266): words d, d + 1 (unsigned) and d + 2 (signed)
+      const ExactRec r = rec[seg * kOut + o];
+      const int anc = int(r.tag & 0xFFFFFFFF);
+      if (anc >= 0) {   // window (hi : lo) * 2^(anc - 266): words d .. d + 4 of it * 2^(anc & 31)
         const int d = anc >> 5, sa = anc & 31;
-        const unsigned long long lo = (unsigned long long)r.x << sa;
-        const long long hi = sa ? (r.x >> (64 - sa)) : (r.x >> 63);
-        const long long w0 = (long long)(lo & 0xFFFFFFFFull), w1 = (long long)(lo >> 32);
+        const unsigned long long lo = r.lo << sa;
+        const unsigned long long mid = sa ? (r.lo >> (64 - sa)) | ((unsigned long long)r.hi << sa) : (unsigned long long)r.hi;
+        const long long top = sa ? (r.hi >> (64 - sa)) : (r.hi >> 63);
+        const long long w[5] = {(long long)(lo & 0xFFFFFFFFull), (long long)(lo >> 32), (long long)(mid & 0xFFFFFFFFull),
+                                (long long)(mid >> 32), top};
 #pragma unroll
-        for (int s = 0; s < kDigits; ++s) c[s] += s == d ? w0 : (s == d + 1 ? w1 : (s == d + 2 ? hi : 0));
+        for (int s = 0; s < kDigits; ++s) {
+          long long v = 0;
+#pragma unroll
+          for (int j = 0; j < 5; ++j) v = s == d + j ? w[j] : v;
+          c[s] += v;
+        }
       }
-      if ((r.y >> 32) & 1) {
+      if ((r.tag >> 32) & 1) {
 #pragma unroll
         for (int s = 0; s < kExactSlots; ++s) c[s] += spill[(seg * kExactSlots + s) * kOut + o];
       }
@@ -460,9 +544,9 @@ size_t exact_segments(int64_t M, int64_t P, int64_t Q) {
 }
 
 size_t exact_part_bytes(int64_t M, int64_t P, int64_t Q) {
-  // records (16 bytes) and digit arrays (kExactSlots int64) per segment and output
+  // records and digit arrays (kExactSlots int64) per segment and output
   const size_t segs = exact_segments(M, P, Q);
-  return segs * kOut * (sizeof(longlong2) + kExactSlots * sizeof(long long));
+  return segs * kOut * (sizeof(ExactRec) + kExactSlots * sizeof(long long));
 }
 
 cudaError_t launch_exact(const void* left, int ldl, const void* right, int ldr, bool dv, float alpha, int M, int P, int Q,
@@ -476,18 +560,18 @@ cudaError_t launch_exact(const void* left, int ldl, const void* right, int ldr, 
   const size_t segs = exact_segments(M, P, Q);
   const uint16_t* l = static_cast<const uint16_t*>(left);
   const uint16_t* r = static_cast<const uint16_t*>(right);
-  longlong2* rec = reinterpret_cast<longlong2*>(part);
-  long long* spill = part + segs * kOut * 2;
+  ExactRec* rec = reinterpret_cast<ExactRec*>(part);
+  long long* spill = part + segs * kOut * (sizeof(ExactRec) / sizeof(long long));
   if (U > 0) {
     const cudaError_t e =
-        dv ? launch_pdl(exact_digits_kernel<true>, dim3(unsigned(G)), dim3(kThreads), 0, st, l, ldl, r, ldr, M, P, Q,
+        dv ? launch_pdl(exact_digits_kernel<true>, dim3(unsigned(G)), dim3(kThreads), sizeof(ExactSmem), st, l, ldl, r, ldr, M, P, Q,
                         n_tq, B, U, alpha, rec, spill)
-           : launch_pdl(exact_digits_kernel<false>, dim3(unsigned(G)), dim3(kThreads), 0, st, l, ldl, r, ldr, M, P,
+           : launch_pdl(exact_digits_kernel<false>, dim3(unsigned(G)), dim3(kThreads), sizeof(ExactSmem), st, l, ldl, r, ldr, M, P,
                         Q, n_tq, B, U, alpha, rec, spill);
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(exact_reduce_kernel, dim3(unsigned(ceil_div(int64_t(P) * Q, 256))), dim3(256), 0, st,
-                    static_cast<const longlong2*>(rec), static_cast<const long long*>(spill), P, Q, n_tq, B, U, G,
+                    static_cast<const ExactRec*>(rec), static_cast<const long long*>(spill), P, Q, n_tq, B, U, G,
                     transpose ? 1 : 0, out_digits, out);
 }
 
@@ -497,6 +581,12 @@ cudaError_t launch_exact_combine(const long long* a, const long long* b, int64_t
                     out);
 }
 
-cudaError_t prepare_exact() { return cudaSuccess; }
+cudaError_t prepare_exact() {
+  cudaError_t e = cudaFuncSetAttribute(exact_digits_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(sizeof(ExactSmem)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(exact_digits_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(sizeof(ExactSmem)));
+}
 
 }  // namespace lora

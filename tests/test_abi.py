@@ -227,9 +227,9 @@ def test_exact_mode_host_checks(lib):
     assert ld.lora_delta_exact_slots() == 21
     need = ld.lora_delta_grads_exact_workspace_size(300, 136, 72, 16)
     # segments of the digit kernel: units (64 rows of a 16 x 64 output tile) 3 tiles x 5 = 15 for
-    # dA (K = 136), so at most 15 CTAs and 15 + 3 segments; per segment and tile output a 16-byte
+    # dA (K = 136), so at most 15 CTAs and 15 + 3 segments; per segment and tile output a 32-byte
     # record and a 21-int64 digit array; the larger gradient's, 256-byte rounded
-    assert need == ((18 * 1024 * (16 + 21 * 8) + 255) // 256) * 256
+    assert need == ((18 * 1024 * (32 + 21 * 8) + 255) // 256) * 256
     assert ld.lora_delta_grads_exact_workspace_size(1 << 30, 128, 96, 16) == 0   # M below 2^30
     assert ld.lora_delta_grads_exact_workspace_size(64, 100, 96, 16) == 0
     f = lib.lora_delta_grads_exact
