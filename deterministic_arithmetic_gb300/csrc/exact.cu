@@ -137,6 +137,13 @@ __device__ __forceinline__ void digits_product(long long* dig, int& used, uint32
   digits_add64(dig, used, v, max(ea, 1) + max(eb, 1) - 268 + 266);
 }
 
+// a * b + c with a 64-bit product and addend (one multiply-add)
+__device__ __forceinline__ long long mad_wide(int a, int b, long long c) {
+  long long d;
+  asm("mad.wide.s32 %0, %1, %2, %3;" : "=l"(d) : "r"(a), "r"(b), "l"(c));
+  return d;
+}
+
 // 16-byte asynchronous copy global -> shared; bytes = 0 fills the 16 bytes with zeros
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(uint32_t(__cvta_generic_to_shared(dst))),
@@ -146,26 +153,23 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// shared memory of the digit kernel
+// shared memory of the digit kernel (row pitches padded against bank conflicts)
+constexpr int kRawLP = 24, kRawRP = 72, kFrP = 68;
 struct ExactSmem {
-  uint16_t raw_l[2][kRows][kTP];   // raw BF16 rows (dV for the right rows of dB), double-buffered
-  uint16_t raw_r[2][kRows][kTQ];
-  int fl[kRows][kTP];              // fixed-point factors
-  int fr[kRows][kTQ];
-  int cl_part[kRows / 2][kTP];     // column maxima of E' per decoding thread
-  int cr_part[kRows / 8][kTQ];
-  int cl[kTP], cr[kTQ];            // column maxima of E' over the 64 rows (0: no non-zero finite value)
-  uint32_t small[kMaxSmall];       // small factors: right << 31 | row << 16 | column
-  int n_small;
+  uint16_t raw_l[2][kRows][kRawLP];   // raw BF16 rows (dV for the right rows of dB), double-buffered
+  uint16_t raw_r[2][kRows][kRawRP];
+  int frT[kTQ][kFrP];                 // right fixed-point factors, column-major
+  int flT[kTP / 2][kRows][2];         // left fixed-point factors, column pairs
+  int cl[kTP], cr[kTQ];               // column maxima of E' over the 64 rows (0: no non-zero finite value)
+  uint32_t small[kMaxSmall];          // small factors: right << 31 | row << 16 | column
+  int n_small[2];                     // their count (by unit parity)
 };
 
-// Start the copies of unit u's raw rows into buffer b (one 16-byte chunk of the right rows per
+// Start the copies of the raw rows of unit (tile at p0, q0; row block blk) into buffer b (one 16-byte chunk of the right rows per
 // thread, one of the left rows for the first 128 threads; zeros past M, P and Q).
-__device__ __forceinline__ void fetch_unit(ExactSmem& sm, int b, int64_t u, int B, int n_tq, const uint16_t* left,
+__device__ __forceinline__ void fetch_unit(ExactSmem& sm, int b, int p0, int q0, int blk, const uint16_t* left,
                                            int ldl, const uint16_t* right, int ldr, int M, int P, int Q) {
-  const int tile = int(u / B);
-  const int m0 = int(u - int64_t(tile) * B) * kRows;
-  const int q0 = (tile % n_tq) * kTQ, p0 = (tile / n_tq) * kTP;
+  const int m0 = blk * kRows;
   const int tid = threadIdx.x;
   {
     const int r = tid / (kTQ / 8), c8 = (tid % (kTQ / 8)) * 8;   // 512 chunks: 64 rows x 8
@@ -179,24 +183,23 @@ __device__ __forceinline__ void fetch_unit(ExactSmem& sm, int b, int64_t u, int 
   }
 }
 
-// E' of a non-zero finite BF16 value, 0 for zeros, -1 for inf and NaN
-__device__ __forceinline__ int eff_exp(uint32_t h) {
-  const int e = int(h >> 7) & 0xFF;
-  return e == 0xFF ? -1 : ((h & 0x7FFFu) ? max(e, 1) : 0);
-}
-
-// the fixed-point factor of h in a column whose largest E' is c; small: set when h needs
-// more than kScale bits below c (the factor is then 0)
-__device__ __forceinline__ int fixed_factor(uint32_t h, int c, bool& small) {
-  const int e = int(h >> 7) & 0xFF;
-  if ((h & 0x7FFFu) == 0u || e == 0xFF) return 0;
-  const int sh = max(e, 1) - c + kScale;
-  if (sh < 0) {
-    small = true;
-    return 0;
-  }
-  const int v = ((e ? 0x80 : 0) | int(h & 0x7Fu)) << sh;
-  return (h & 0x8000u) ? -v : v;
+// The fixed-point factor +-mag 2^(E - c + kScale) of a BF16 value h (E its biased exponent,
+// mag its significand with the leading bit) in a column whose largest E is c: adding
+// (154 - c) << 23 to the exponent field of h as binary32 gives exactly that integer (below
+// 2^28) whenever E >= max(c - kScale, 1), and the conversion to int is then exact. Otherwise
+// the factor is 0, and small is set when h is non-zero (a subnormal, or more than kScale bits
+// below c). Not for inf or NaN (rows holding one take another path).
+struct ColScale {
+  uint32_t adj;   // (154 - c) << 23
+  int lo;         // max(c - kScale, 1)
+};
+__device__ __forceinline__ ColScale col_scale(int c) { return ColScale{uint32_t(154 - c) << 23, max(c - kScale, 1)}; }
+__device__ __forceinline__ int fixed_factor(uint32_t h, ColScale cs, bool& small) {
+  const uint32_t x = h << 16;
+  const int e = int(x >> 23) & 0xFF;
+  const bool ok = e >= cs.lo;
+  small = !ok && (x & 0x7FFF0000u) != 0u;
+  return ok ? __float2int_rz(__uint_as_float(x + cs.adj)) : 0;
 }
 
 // The window of one output: a 128-bit sum at anchor anc (-1: none yet) and whether the
@@ -247,22 +250,35 @@ __global__ void __launch_bounds__(kThreads, 2)
   grid_dependents_launch();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ExactSmem& sm = *reinterpret_cast<ExactSmem*>(smem_raw);
-  const int tid = threadIdx.x, q = tid % kTQ, pg = tid / kTQ;   // outputs (2 pg, q) and (2 pg + 1, q)
-  const int oa = 2 * pg * kTQ + q, ob = oa + kTQ;               // their indexes in the tile
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int q = tid % kTQ, pg = tid / kTQ;            // outputs (2 pg, q) and (2 pg + 1, q)
+  const int oa = 2 * pg * kTQ + q, ob = oa + kTQ;     // their indexes in the tile
+  const int dr_c = tid / 8, dr_i = tid % 8;           // decoding: right column, rows dr_i + 8 k
   const int G = gridDim.x, c = blockIdx.x;
-  const int dl_p = tid % kTP, dl_r = 2 * (tid / kTP);           // decoding: left column, first of two rows
-  const int dr_r = 8 * (tid / kTQ);                             // right column q, first of eight rows
   const int64_t u_begin = int64_t(c) * U / G, u_end = (int64_t(c) + 1) * U / G;
-  if (u_begin < u_end) fetch_unit(sm, 0, u_begin, B, n_tq, left, ldl, right, ldr, M, P, Q);
+  if (tid < 2) sm.n_small[tid] = 0;
+  // the unit (tile, row block) now and next, advanced without divisions; the next tile's corner
+  int tile = u_begin < u_end ? int(u_begin / B) : 0, blk = int(u_begin - int64_t(tile) * B);
+  int next_tile = tile, next_blk = blk, next_q0 = (tile % n_tq) * kTQ, next_p0 = (tile / n_tq) * kTP;
+  if (u_begin < u_end) fetch_unit(sm, 0, next_p0, next_q0, blk, left, ldl, right, ldr, M, P, Q);
   cp_async_commit();
-  int tile = -1, units = 0;
+  int units = 0;
   size_t seg = 0;
   long long *dig_a = spill, *dig_b = spill;
   Win wa{{0, 0}, -1, 0}, wb{{0, 0}, -1, 0};
   for (int64_t u = u_begin; u < u_end; ++u) {
     const int buf = int((u - u_begin) & 1);
-    if (u / B != tile) {   // a new segment
-      tile = int(u / B);
+    tile = next_tile;
+    blk = next_blk;
+    if (++next_blk == B) {
+      next_blk = 0;
+      ++next_tile;
+      if ((next_q0 += kTQ) >= n_tq * kTQ) {
+        next_q0 = 0;
+        next_p0 += kTP;
+      }
+    }
+    if (u == u_begin || blk == 0) {   // a new segment
       seg = size_t(c) + tile;
       dig_a = spill + seg * kExactSlots * kOut + oa;
       dig_b = spill + seg * kExactSlots * kOut + ob;
@@ -271,71 +287,63 @@ __global__ void __launch_bounds__(kThreads, 2)
       units = 0;
     }
     cp_async_wait_all();   // this thread's copies of unit u have landed
-    __syncthreads();       // everyone's; the previous unit's factors consumed; buffer buf ^ 1 free
-    if (u + 1 < u_end) fetch_unit(sm, buf ^ 1, u + 1, B, n_tq, left, ldl, right, ldr, M, P, Q);
+    __syncthreads();       // everyone's; the previous unit consumed; buffer buf ^ 1 free
+    if (u + 1 < u_end) fetch_unit(sm, buf ^ 1, next_p0, next_q0, next_blk, left, ldl, right, ldr, M, P, Q);
     cp_async_commit();
-    if (tid == 0) sm.n_small = 0;
-    // pass 1: dV (dB), column maxima of E', inf / NaN
+    if (tid == 0) sm.n_small[buf ^ 1] = 0;
+    // decode: each group of 8 lanes takes one right column (rows dr_i + 8 k), each warp one left
+    // column (rows lane and lane + 32); the column's largest E' by shuffles, then the fixed-point
+    // factors; small ones listed; inf / NaN noted
     int special = 0;
     {
+      uint32_t h[8];
       int mx = 0;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int e = eff_exp(sm.raw_l[buf][dl_r + k][dl_p]);
-        special |= e < 0;
-        mx = max(mx, e);
+      for (int k = 0; k < 8; ++k) {
+        h[k] = sm.raw_r[buf][dr_i + 8 * k][dr_c];
+        if (DV) {
+          h[k] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__uint_as_float(h[k] << 16), alpha)));
+          sm.raw_r[buf][dr_i + 8 * k][dr_c] = uint16_t(h[k]);
+        }
+        mx = max(mx, int(h[k] >> 7) & 0xFF);
       }
-      sm.cl_part[dl_r / 2][dl_p] = mx;
-      mx = 0;
+#pragma unroll
+      for (int s = 1; s < 8; s <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, s));
+      special |= mx == 0xFF;
+      if (dr_i == 0) sm.cr[dr_c] = mx;
+      const ColScale cs = col_scale(mx);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        uint32_t h = sm.raw_r[buf][dr_r + k][q];
-        if (DV) {
-          h = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__uint_as_float(h << 16), alpha)));
-          sm.raw_r[buf][dr_r + k][q] = uint16_t(h);
+        bool s = false;
+        sm.frT[dr_c][dr_i + 8 * k] = fixed_factor(h[k], cs, s);
+        if (s) {
+          const int i = atomicAdd(&sm.n_small[buf], 1);
+          if (i < kMaxSmall) sm.small[i] = 0x80000000u | uint32_t((dr_i + 8 * k) << 16 | dr_c);
         }
-        const int e = eff_exp(h);
-        special |= e < 0;
-        mx = max(mx, e);
       }
-      sm.cr_part[dr_r / 8][q] = mx;
+    }
+    {
+      const uint32_t h0 = sm.raw_l[buf][lane][warp], h1 = sm.raw_l[buf][lane + 32][warp];
+      int mx = max(int(h0 >> 7) & 0xFF, int(h1 >> 7) & 0xFF);
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, s));
+      special |= mx == 0xFF;
+      if (lane == 0) sm.cl[warp] = mx;
+      const ColScale cs = col_scale(mx);
+      bool s0 = false, s1 = false;
+      sm.flT[warp / 2][lane][warp % 2] = fixed_factor(h0, cs, s0);
+      sm.flT[warp / 2][lane + 32][warp % 2] = fixed_factor(h1, cs, s1);
+      if (s0) {
+        const int i = atomicAdd(&sm.n_small[buf], 1);
+        if (i < kMaxSmall) sm.small[i] = uint32_t(lane << 16 | warp);
+      }
+      if (s1) {
+        const int i = atomicAdd(&sm.n_small[buf], 1);
+        if (i < kMaxSmall) sm.small[i] = uint32_t((lane + 32) << 16 | warp);
+      }
     }
     const bool any_special = __syncthreads_or(special);
-    if (tid < kTP) {
-      int mx = 0;
-      for (int i = 0; i < kRows / 2; ++i) mx = max(mx, sm.cl_part[i][tid]);
-      sm.cl[tid] = mx;
-    } else if (tid >= 2 * kTQ && tid < 3 * kTQ) {
-      int mx = 0;
-      for (int i = 0; i < kRows / 8; ++i) mx = max(mx, sm.cr_part[i][tid - 2 * kTQ]);
-      sm.cr[tid - 2 * kTQ] = mx;
-    }
-    __syncthreads();
-    // pass 2: the fixed-point factors; small ones listed
-    {
-      const int c_l = sm.cl[dl_p];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        bool s = false;
-        sm.fl[dl_r + k][dl_p] = fixed_factor(sm.raw_l[buf][dl_r + k][dl_p], c_l, s);
-        if (s) {
-          const int i = atomicAdd(&sm.n_small, 1);
-          if (i < kMaxSmall) sm.small[i] = uint32_t((dl_r + k) << 16 | dl_p);
-        }
-      }
-      const int c_r = sm.cr[q];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        bool s = false;
-        sm.fr[dr_r + k][q] = fixed_factor(sm.raw_r[buf][dr_r + k][q], c_r, s);
-        if (s) {
-          const int i = atomicAdd(&sm.n_small, 1);
-          if (i < kMaxSmall) sm.small[i] = 0x80000000u | uint32_t((dr_r + k) << 16 | q);
-        }
-      }
-    }
-    __syncthreads();
-    const int n_small = sm.n_small;
+    const int n_small = sm.n_small[buf];
     if (any_special || n_small > kMaxSmall) {
       // every product of these rows, one by one from the raw values
       for (int r = 0; r < kRows; ++r) {
@@ -345,12 +353,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     } else {
       long long sa = 0, sb = 0;
-#pragma unroll 8
-      for (int r = 0; r < kRows; ++r) {
-        const int fr = sm.fr[r][q];
-        const int2 fl = *reinterpret_cast<const int2*>(&sm.fl[r][2 * pg]);
-        sa += (long long)fl.x * fr;
-        sb += (long long)fl.y * fr;
+#pragma unroll 4
+      for (int r = 0; r < kRows; r += 4) {
+        const int4 fr = *reinterpret_cast<const int4*>(&sm.frT[q][r]);
+        const int4 f01 = *reinterpret_cast<const int4*>(&sm.flT[pg][r][0]);      // rows r, r + 1
+        const int4 f23 = *reinterpret_cast<const int4*>(&sm.flT[pg][r + 2][0]);  // rows r + 2, r + 3
+        sa = mad_wide(f01.x, fr.x, sa);
+        sb = mad_wide(f01.y, fr.x, sb);
+        sa = mad_wide(f01.z, fr.y, sa);
+        sb = mad_wide(f01.w, fr.y, sb);
+        sa = mad_wide(f23.x, fr.z, sa);
+        sb = mad_wide(f23.y, fr.z, sb);
+        sa = mad_wide(f23.z, fr.w, sa);
+        sb = mad_wide(f23.w, fr.w, sb);
       }
       const int crq = sm.cr[q];
       window_fold(wa, dig_a, sa, sm.cl[2 * pg] + crq - 2 * kScale - 2);
@@ -363,9 +378,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (e >> 31) {   // right factor (r, col): with every left factor of row r that is not small
           if (col != q) continue;
           const uint32_t hr = sm.raw_r[buf][r][q];
-          const uint32_t la = sm.raw_l[buf][r][2 * pg], lb = sm.raw_l[buf][r][2 * pg + 1];
-          if (sm.fl[r][2 * pg] != 0) digits_product(dig_a, wa.used, la, hr);
-          if (sm.fl[r][2 * pg + 1] != 0) digits_product(dig_b, wb.used, lb, hr);
+          if (sm.flT[pg][r][0] != 0) digits_product(dig_a, wa.used, sm.raw_l[buf][r][2 * pg], hr);
+          if (sm.flT[pg][r][1] != 0) digits_product(dig_b, wb.used, sm.raw_l[buf][r][2 * pg + 1], hr);
         } else {         // left factor (r, col): with every right factor of row r
           if ((col >> 1) != pg) continue;
           if (col & 1) digits_product(dig_b, wb.used, sm.raw_l[buf][r][col], sm.raw_r[buf][r][q]);
@@ -378,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       window_spill(wb, dig_b);
       units = 0;
     }
-    if (u + 1 == u_end || (u + 1) / B != tile) {   // the segment ends: its records
+    if (u + 1 == u_end || next_tile != tile) {   // the segment ends: its records
       rec[seg * kOut + oa] = ExactRec{wa.acc.lo, wa.acc.hi, (long long)(uint32_t)wa.anc | ((long long)wa.used << 32), 0};
       rec[seg * kOut + ob] = ExactRec{wb.acc.lo, wb.acc.hi, (long long)(uint32_t)wb.anc | ((long long)wb.used << 32), 0};
     }
