@@ -72,12 +72,12 @@ def measured_peaks():
 # dram__bytes_write.sum), keyed by kernel, with the hash of the kernel source
 # the counters were taken on; a kernel changed since then reports null.
 NCU_TRAFFIC = {   # ncu, training step, warm caches (--cache-control none), per launch
-    "down U": {"bytes": 71600000, "src_hash": "e57e2cb6ea3afff6"},
-    "up dY_lora": {"bytes": 125100000, "src_hash": "ef3ff4a0da20658b"},
-    "dy dU+dB": {"bytes": 79700000, "src_hash": "87a5fe328aafbc61"},
-    "up dX": {"bytes": 127400000, "src_hash": "ef3ff4a0da20658b"},
-    "wgrad dA": {"bytes": 75500000, "src_hash": "e3813b8b0870e8f6"},
-    "combine dA+dB": {"bytes": 860000, "src_hash": "337f1bac5b0e1c32"},
+    "down U": {"bytes": 71610000, "src_hash": "2a4b5ad0158cc814"},
+    "up dY_lora": {"bytes": 124820000, "src_hash": "094f138f10a9f88e"},
+    "dy dU+dB": {"bytes": 79910000, "src_hash": "7971a7838ffbc72d"},
+    "up dX": {"bytes": 126770000, "src_hash": "094f138f10a9f88e"},
+    "wgrad dA": {"bytes": 76030000, "src_hash": "086a1ed9dabedcad"},
+    "combine dA+dB": {"bytes": 1040000, "src_hash": "b45fe2f879bdf9ea"},
 }
 
 
@@ -352,8 +352,16 @@ def exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, reps=5):
     t_db = sorted(e[1].elapsed_time(e[2]) for e in ev)[reps // 2]
     prod = M * R * (K + N)
     ms = t_da + t_db
+    rate = prod / (ms * 1e-3) / 1e12
+    # integer-issue roofline: one wide multiply-add per product, 32 per SM per cycle (8 lanes per
+    # scheduler per cycle, inferred from the FMA-heavy pipe counters), at the 2070 MHz SM maximum
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * 32 * 2.07e9 / 1e12
     return {"grads_exact": {"ms": round(ms, 4), "ms_da": round(t_da, 4), "ms_db": round(t_db, 4),
-                            "products": prod, "gproducts_per_s": round(prod / (ms * 1e-3) / 1e9, 1),
+                            "products": prod, "gproducts_per_s": round(rate * 1e3, 1),
+                            "roofline": {"bound": "alu", "achieved": round(rate, 3), "peak": round(peak, 2),
+                                         "unit": "Tproducts/s", "frac": round(rate / peak, 4),
+                                         "peak_kind": "derived: 32 wide integer multiply-adds per SM per cycle at 2070 MHz"},
                             "launches_per_step": 4, "median_of": reps}}
 
 
