@@ -252,19 +252,32 @@ def lora_delta_grads_exact(dy, x, u, du, alpha: float, *, da=None, db=None, da_d
     return {k: v for k, v in outs.items() if v is not None}
 
 
-def lora_delta_exact_combine(a, b, *, out=None, stream=None):
-    """Digit arrays of the sums: a + b (same shape [..., slots] int64), normalised; out may be a or b."""
-    if a.shape != b.shape or a.dtype != torch.int64 or b.dtype != torch.int64:
-        raise ValueError("digit arrays must be int64 tensors of one shape")
+def lora_delta_exact_combine(a, b=None, *, out=None, stream=None):
+    """Digit arrays of the sums a + b (same shape [..., slots] int64), normalised; out may be a or
+    b. b None: a normalised."""
     slots = lora_delta_exact_slots()
-    if a.shape[-1] != slots or not a.is_contiguous() or not b.is_contiguous():
-        raise ValueError(f"digit arrays: contiguous [..., {slots}] int64")
+    for t, name in ((a, "a"), (b, "b")):
+        if t is None and name == "b":
+            continue
+        if t.dtype != torch.int64 or t.shape != a.shape or t.shape[-1] != slots or not t.is_contiguous():
+            raise ValueError(f"digit arrays: contiguous [..., {slots}] int64 tensors of one shape")
     out = torch.empty_like(a) if out is None else out
     _check(out, "out", torch.int64, tuple(a.shape))
     rc = _lib().lora_delta_exact_combine(_ptr(a), _ptr(b), a.numel() // slots, _ptr(out), _stream(stream))
     if rc != LORA_OK:
         raise LoraDeltaError(rc, "lora_delta_exact_combine")
     return out
+
+
+def lora_delta_exact_all_reduce(digits, *, group=None, stream=None):
+    """The digit arrays of the sum over the ranks of ``group`` (torch.distributed), in place:
+    one int64 sum all-reduce -- exact and order-free, so the result is the same at any world
+    size and rank order -- then normalised by the library (page "det-train", "API":
+    det_all_reduce). Run by every rank of the group on its own digits."""
+    import torch.distributed as dist
+
+    dist.all_reduce(digits, op=dist.ReduceOp.SUM, group=group)
+    return lora_delta_exact_combine(digits, None, out=digits, stream=stream)
 
 
 def lora_delta_exact_finalize(digits, *, out=None, stream=None):

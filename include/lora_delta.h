@@ -274,10 +274,11 @@ lora_status lora_delta_grads_exact(const void *dy, const void *x, const void *u,
 
 /*
  * out_digits = a + b over n digit arrays (n outputs, 21 int64 each), written
- * normalised; out_digits may be a or b (in place). Inputs may be normalised
- * or not, as long as every sum of a digit stays within int64 (digit arrays of
- * fewer than 2^30 rows in all). Returns LORA_ERR_SHAPE for n < 0; n = 0 is a
- * no-op.
+ * normalised; out_digits may be a or b (in place). b NULL: out_digits = a,
+ * normalised (e.g. after an int64 sum all-reduce of digit arrays across ranks,
+ * the det-train page's det_all_reduce). Inputs may be normalised or not, as
+ * long as every sum of a digit stays within int64 (digit arrays of fewer than
+ * 2^30 rows in all). Returns LORA_ERR_SHAPE for n < 0; n = 0 is a no-op.
  */
 lora_status lora_delta_exact_combine(const int64_t *a, const int64_t *b, int64_t n, int64_t *out_digits,
                                      void *stream);

@@ -251,7 +251,8 @@ def test_exact_mode_host_checks(lib):
     assert call(ws=ld.lora_delta_grads_exact_workspace_size(64, 128, 96, 16) - 8) == 5
     assert lib.lora_delta_exact_combine(FAKE, FAKE, -1, FAKE, None) == 2
     assert lib.lora_delta_exact_combine(FAKE, FAKE, 0, FAKE, None) == 0
-    assert lib.lora_delta_exact_combine(FAKE, None, 4, FAKE, None) == 1
+    assert lib.lora_delta_exact_combine(None, FAKE, 4, FAKE, None) == 1
+    assert lib.lora_delta_exact_combine(FAKE, FAKE, 4, None, None) == 1
     assert lib.lora_delta_exact_finalize(FAKE, -1, FAKE, None) == 2
     assert lib.lora_delta_exact_finalize(None, 4, FAKE, None) == 1
     import torch

@@ -8,7 +8,8 @@ section "Method") against the exact-mode oracle: bitwise, everywhere.
 * The closed-form sums of the oracle's pins (cancellation, ties, overflow,
   subnormals, IEEE specials) come out exact on the GPU.
 * Row shards' digit arrays, added with lora_delta_exact_combine in any grouping,
-  equal the whole batch's; finalize gives the same FP32 bits; any row order gives
+  equal the whole batch's; so does their plain int64 sum (what an all-reduce
+  leaves) once normalised; finalize gives the same FP32 bits; any row order gives
   the same bits; reruns are bitwise.
 * The full training shape (M=8192, K=N=4096, R=16): sampled columns against the
   oracle, and every output equal to the correctly rounded binary64 sum where that
@@ -199,3 +200,19 @@ def test_training_shape_sampled(oracle):
         half_ulp = np.spacing(np.abs(got).astype(np.float32)).astype(np.float64) / 2
         assert np.all(np.abs(g - ref) <= half_ulp + bound + 2.0 ** -149), f"{name}: not the rounded exact sum"
         assert math.isfinite(float(np.abs(g).max()))
+
+
+def test_raw_digit_sums_normalise_to_the_whole():
+    """What an int64 sum all-reduce of the ranks' digit arrays leaves (a plain sum, not
+    normalised), normalised by lora_delta_exact_combine(a, None): the whole batch's digits."""
+    M, K, N, R, alpha = 300, 72, 64, 16, 0.5
+    d = _inputs(M, K, N, R, seed=12, wide=True)
+    whole = _gpu(d, alpha, want=("da_digits", "db_digits"))
+    cuts = [0, 100, 101, M]
+    parts = [_gpu({k: v[a:b] for k, v in d.items()}, alpha, want=("da_digits", "db_digits"))
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    for key in ("da_digits", "db_digits"):
+        raw = sum(torch.from_numpy(p[key]) for p in parts).cuda()
+        norm = ld.lora_delta_exact_combine(raw, None, out=raw)
+        torch.cuda.synchronize()
+        _bits_equal(f"{key}: summed and normalised", norm.cpu().numpy(), whole[key])
