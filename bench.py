@@ -365,6 +365,84 @@ def exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, reps=5):
                             "launches_per_step": 4, "median_of": reps}}
 
 
+def decode_variants(ld, dev, steps=50, reps=20, copies=8):
+    """The decode batches of the pages' MLP width (M = 1, 8, 64; K5120 -> N17408; R64; alpha 1;
+    random BF16 operands drawn on the device): the forward, and at M = 64 the backward too,
+    CUDA-graph timed over `copies` rotated sets of every operand (weights included). The
+    working set stays in L2 at these sizes, so the figures are latencies, not HBM rates."""
+    import torch
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    K, N, R, alpha = 5120, 17408, 64, 1.0
+    bf, f4 = 2, 4
+
+    def rnd(*shape, s=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * s).to(torch.bfloat16)
+
+    def graph_ms(call):
+        for i in range(3):
+            call(i, torch.cuda.current_stream(dev))
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                gst = torch.cuda.current_stream(dev)
+                for i in range(steps):
+                    call(i, gst)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * steps)
+
+    out = {}
+    for M in (1, 8, 64):
+        As = [rnd(R, K, s=K ** -0.5) for _ in range(copies)]
+        Bs = [rnd(N, R, s=R ** -0.5) for _ in range(copies)]
+        Xs = [rnd(M, K) for _ in range(copies)]
+        Ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(copies)]
+        Us = [torch.empty((M, R), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+        wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+
+        def fwd(i, st):
+            j = i % copies
+            ld.lora_delta_fwd(Xs[j], As[j], Bs[j], alpha, delta_y=Ys[j], u=Us[j], workspace=wf, stream=st)
+
+        ms = graph_ms(fwd)
+        nbytes = M * K * bf + R * K * bf + 2 * M * R * bf + N * R * bf + M * N * f4
+        out[f"decode_fwd_M{M}"] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes,
+                                   "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 2}
+        assert ld.lora_delta_device_status(wf) == 0
+        if M == 64:
+            DYs = [rnd(M, N) for _ in range(copies)]
+            wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
+            dx = torch.empty((M, K), dtype=torch.float32, device=dev)
+            da = torch.empty((R, K), dtype=torch.float32, device=dev)
+            db = torch.empty((N, R), dtype=torch.float32, device=dev)
+            du = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+
+            def bwd(i, st):
+                j = i % copies
+                ld.lora_delta_bwd(DYs[j], Xs[j], As[j], Bs[j], Us[j], alpha, dx=dx, da=da, db=db, du=du,
+                                  workspace=wb, stream=st)
+
+            ms = graph_ms(bwd)
+            nbytes = M * N * bf + N * R * bf + M * R * bf + M * K * bf + R * K * bf + M * K * f4 + 2 * M * R * bf \
+                + R * K * f4 + N * R * f4
+            out["decode_bwd_M64"] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes,
+                                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 5}
+            assert ld.lora_delta_device_status(wb) == 0
+    return out
+
+
 def grouped_variants(ld, dev, steps=10, reps=20):
     """The MLP insertion points of the pages (fc1 K5120 -> N17408, fc2 K17408 -> N5120,
     M4096, R16, alpha 1; random BF16 inputs drawn on the device), forward + backward of
@@ -576,6 +654,7 @@ def run_ours(args, world, rank, local):
         variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(grouped_variants(ld, dev))
         variants.update(exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
+        variants.update(decode_variants(ld, dev))
 
     # ----------------------------------------------------------- end to end
     e2e = None
