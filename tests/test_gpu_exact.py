@@ -7,6 +7,8 @@ section "Method") against the exact-mode oracle: bitwise, everywhere.
   the kernel's direct path as well as its register window).
 * The closed-form sums of the oracle's pins (cancellation, ties, overflow,
   subnormals, IEEE specials) come out exact on the GPU.
+* Factors far below their column's largest, subnormal ones and zeros, few or many
+  per 64 rows, take the kernel's exact side paths with the same bits.
 * Row shards' digit arrays, added with lora_delta_exact_combine in any grouping,
   equal the whole batch's; so does their plain int64 sum (what an all-reduce
   leaves) once normalised; finalize gives the same FP32 bits; any row order gives
@@ -216,3 +218,28 @@ def test_raw_digit_sums_normalise_to_the_whole():
         norm = ld.lora_delta_exact_combine(raw, None, out=raw)
         torch.cuda.synchronize()
         _bits_equal(f"{key}: summed and normalised", norm.cpu().numpy(), whole[key])
+
+
+@pytest.mark.parametrize("frac", [0.002, 0.02, 0.1], ids=["few-small", "more-small", "past-the-list"])
+def test_small_factors_take_the_exact_side_path(oracle, frac):
+    """The training distributions with a sprinkling of factors far below their column's
+    largest (2^-24 .. 2^-60 of it), subnormal ones, and exact zeros: a few of them per 64 rows
+    go through the listed one-by-one path, more than the list holds through the general one.
+    Bitwise equal to the oracle either way."""
+    M, K, N, R, alpha = 640, 136, 200, 16, 0.75
+    rng = np.random.default_rng(int(frac * 1e4))
+    d = _inputs(M, K, N, R, seed=33)
+    for key in ("x", "dy", "u", "du"):
+        v = S.bf16_bits_to_f64(d[key])
+        pick = rng.random(v.shape) < frac
+        v[pick] *= np.exp2(-rng.integers(24, 60, v.shape))[pick]
+        v[rng.random(v.shape) < frac / 4] = 2.0 ** -130 * rng.integers(-100, 100)   # subnormal (or zero)
+        v[rng.random(v.shape) < frac] = 0.0
+        d[key] = S.to_bf16_bits(v)
+    out = _gpu(d, alpha)
+    dv = oracle.dv(d["dy"], alpha)
+    _bits_equal("dA digits", out["da_digits"], EO.digits(d["du"], d["x"]))
+    _bits_equal("dB digits", out["db_digits"], EO.digits(d["u"], dv, transpose=True))
+    da, db = EO.grads(dv, d["x"], d["u"], d["du"])
+    _bits_equal("dA", out["da"], da)
+    _bits_equal("dB", out["db"], db)
