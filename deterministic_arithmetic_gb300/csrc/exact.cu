@@ -25,18 +25,19 @@
 // unit are copied into shared memory (cp.async) while the current one computes.
 //
 // Per unit, every factor is written as a fixed-point integer scaled to its
-// column: with E the biased exponent and C the largest E over the column's
-// non-zero finite values in the 64 rows, the factor +-mag 2^(E' - 134) (mag the
-// significand with its leading bit, E' = max(E, 1)) becomes
-// f = +-mag 2^(E' - C + 20), an integer below 2^28 whenever E' >= C - 20. Then
-// each product is one IMAD.WIDE, f_l f_r < 2^56, and a thread's 64-row sum S
-// (below 2^62) of an output is exact at the unit position C_l + C_r - 42
-// (counted from 2^-266). S is added, shifted, into a 128-bit window in
-// registers (anchor set 20 bits below the first S's position, which leaves 41
-// bits of room above it), or -- out of the window's range -- straight into the
-// output's digit array of the segment in global memory (owned by the thread;
-// zeroed at its first use). Factors more than 20 bits below their column's
-// largest ("small"; none in data of ordinary range) are written as 0 and their
+// column: with E the biased exponent and C the largest E in the column over the
+// 64 rows (found by warp shuffles), a normal factor +-mag 2^(E - 134) (mag the
+// significand with its leading bit) becomes f = +-mag 2^(E - C + 20) -- its
+// binary32 exponent field raised by 154 - C, then converted exactly to int --
+// an integer below 2^28 whenever E >= C - 20. Then each product is one wide
+// multiply-add, f_l f_r < 2^56, and a thread's 64-row sum S (below 2^62) of an
+// output is exact at the unit position C_l + C_r - 42 (counted from 2^-266). S
+// is added, shifted, into a 128-bit window in registers (anchor set 20 bits
+// below the first S's position, which leaves 41 bits of room above it), or --
+// out of the window's range -- straight into the output's digit array of the
+// segment in global memory (owned by the thread; zeroed at its first use).
+// Factors more than 20 bits below their column's largest, and subnormal ones
+// ("small"; none in data of ordinary range), are written as 0 and their
 // products are added exactly one by one from the raw values; so are all the
 // products of 64 rows holding an infinite or NaN value (whose products go to
 // the counters), or more small factors than the list of them holds. Each
@@ -61,7 +62,7 @@ constexpr int kScale = 20;                       // fixed-point bits below a col
 constexpr int kWinBelow = 20;                    // window anchor: this far below the first step sum's position
 constexpr int kWinAbove = 41;                    // highest step-sum shift the 128-bit window takes
 constexpr int kMaxSmall = 256;                   // small factors listed per unit
-constexpr int kFlushUnits = 1 << 16;             // window headroom (2^24 step sums below 2^103 each)
+constexpr int kFlushUnits = 1 << 16;             // a window holds 2^24 step sums below 2^103; spilled sooner
 
 // 128-bit two's complement accumulator
 struct I128 {
@@ -160,13 +161,14 @@ struct ExactSmem {
   uint16_t raw_r[2][kRows][kRawRP];
   int frT[kTQ][kFrP];                 // right fixed-point factors, column-major
   int flT[kTP / 2][kRows][2];         // left fixed-point factors, column pairs
-  int cl[kTP], cr[kTQ];               // column maxima of E' over the 64 rows (0: no non-zero finite value)
+  int cl[kTP], cr[kTQ];               // column maxima of the biased exponent over the 64 rows
   uint32_t small[kMaxSmall];          // small factors: right << 31 | row << 16 | column
   int n_small[2];                     // their count (by unit parity)
 };
 
-// Start the copies of the raw rows of unit (tile at p0, q0; row block blk) into buffer b (one 16-byte chunk of the right rows per
-// thread, one of the left rows for the first 128 threads; zeros past M, P and Q).
+// Start the copies of the raw rows of unit (tile at p0, q0; row block blk) into buffer b (one
+// 16-byte chunk of the right rows per thread, one of the left rows for the first 128 threads;
+// zeros past M, P and Q).
 __device__ __forceinline__ void fetch_unit(ExactSmem& sm, int b, int p0, int q0, int blk, const uint16_t* left,
                                            int ldl, const uint16_t* right, int ldr, int M, int P, int Q) {
   const int m0 = blk * kRows;
