@@ -552,7 +552,7 @@ lora_status lora_delta_grads_exact(const void* dy, const void* x, const void* u,
 }
 
 lora_status lora_delta_exact_combine(const int64_t* a, const int64_t* b, int64_t n, int64_t* out_digits, void* stream) {
-  if (n < 0 || n >= (int64_t(1) << 40)) return LORA_ERR_SHAPE;
+  if (n < 0 || n >= (int64_t(1) << 38)) return LORA_ERR_SHAPE;   // grid of n / 256 blocks
   if (n == 0) return LORA_OK;
   if (!a || !out_digits) return LORA_ERR_NULL;
   int nsm = 0;
@@ -566,7 +566,7 @@ lora_status lora_delta_exact_combine(const int64_t* a, const int64_t* b, int64_t
 }
 
 lora_status lora_delta_exact_finalize(const int64_t* digits, int64_t n, float* out, void* stream) {
-  if (n < 0 || n >= (int64_t(1) << 40)) return LORA_ERR_SHAPE;
+  if (n < 0 || n >= (int64_t(1) << 38)) return LORA_ERR_SHAPE;   // grid of n / 256 blocks
   if (n == 0) return LORA_OK;
   if (!digits || !out) return LORA_ERR_NULL;
   int nsm = 0;

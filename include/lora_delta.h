@@ -278,12 +278,14 @@ lora_status lora_delta_grads_exact(const void *dy, const void *x, const void *u,
  * normalised (e.g. after an int64 sum all-reduce of digit arrays across ranks,
  * the det-train page's det_all_reduce). Inputs may be normalised or not, as
  * long as every sum of a digit stays within int64 (digit arrays of fewer than
- * 2^30 rows in all). Returns LORA_ERR_SHAPE for n < 0; n = 0 is a no-op.
+ * 2^30 rows in all). Returns LORA_ERR_SHAPE for n < 0 or n >= 2^38; n = 0 is a
+ * no-op.
  */
 lora_status lora_delta_exact_combine(const int64_t *a, const int64_t *b, int64_t n, int64_t *out_digits,
                                      void *stream);
 
-/* out[i] = FP32 value of digit array i (rounded to nearest even, once), i < n. */
+/* out[i] = FP32 value of digit array i (rounded to nearest even, once), i < n;
+ * n as for lora_delta_exact_combine. */
 lora_status lora_delta_exact_finalize(const int64_t *digits, int64_t n, float *out, void *stream);
 
 #ifdef __cplusplus
