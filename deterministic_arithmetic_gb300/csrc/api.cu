@@ -551,6 +551,37 @@ lora_status lora_delta_grads_exact(const void* dy, const void* x, const void* u,
   return LORA_OK;
 }
 
+size_t lora_delta_grads_exact_f32dy_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
+  const size_t e = lora_delta_grads_exact_workspace_size(M, K, N, R);
+  return e ? e + round256(size_t(M) * size_t(N) * 2) : 0;
+}
+
+lora_status lora_delta_grads_exact_f32dy(const float* dy, const void* x, const void* u, const void* du, float alpha,
+                                         int64_t M, int64_t K, int64_t N, int64_t R, float* da, float* db,
+                                         int64_t* da_digits, int64_t* db_digits, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  lora_status s = check_shape(M, K, N, R);
+  if (s != LORA_OK) return s;
+  const size_t exact_bytes = lora_delta_grads_exact_workspace_size(M, K, N, R);
+  if (!exact_bytes) return LORA_ERR_SHAPE;
+  const bool want_b = db || db_digits;
+  if (!workspace) return LORA_ERR_NULL;
+  if (M > 0 && want_b && !dy) return LORA_ERR_NULL;
+  if ((dy && !aligned16(dy)) || !aligned16(workspace)) return LORA_ERR_ALIGN;
+  if (workspace_bytes < lora_delta_grads_exact_f32dy_workspace_size(M, K, N, R)) return LORA_ERR_WORKSPACE;
+  // dV = bf16(fp32(dy * alpha)) into the workspace after the digit kernel's scratch; the exact
+  // pass then reads it as its dY with alpha = 1 (bf16(fp32(dv * 1)) = dv)
+  void* dv = static_cast<uint8_t*>(workspace) + exact_bytes;
+  if (M > 0 && want_b) {
+    int nsm = 0;
+    if ((s = device_ready(&nsm)) != LORA_OK) return s;
+    if (launch_dv_from_f32(dy, alpha, M * N, dv, nsm, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return LORA_ERR_CUDA;
+  }
+  return lora_delta_grads_exact(want_b ? dv : nullptr, x, u, du, 1.0f, M, K, N, R, da, db, da_digits, db_digits,
+                                workspace, exact_bytes, stream);
+}
+
 lora_status lora_delta_exact_combine(const int64_t* a, const int64_t* b, int64_t n, int64_t* out_digits, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 38)) return LORA_ERR_SHAPE;   // grid of n / 256 blocks
   if (n == 0) return LORA_OK;

@@ -91,6 +91,10 @@ def _lib() -> ctypes.CDLL:
             lib.lora_delta_grads_exact.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp,
                                                    _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
             lib.lora_delta_grads_exact.restype = ctypes.c_int
+            lib.lora_delta_grads_exact_f32dy.argtypes = lib.lora_delta_grads_exact.argtypes
+            lib.lora_delta_grads_exact_f32dy.restype = ctypes.c_int
+            lib.lora_delta_grads_exact_f32dy_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
+            lib.lora_delta_grads_exact_f32dy_workspace_size.restype = ctypes.c_size_t
             lib.lora_delta_exact_combine.argtypes = [_vp, _vp, _i64, _vp, _vp]
             lib.lora_delta_exact_combine.restype = ctypes.c_int
             lib.lora_delta_exact_finalize.argtypes = [_vp, _i64, _vp, _vp]
@@ -218,7 +222,8 @@ def lora_delta_grads_exact(dy, x, u, du, alpha: float, *, da=None, db=None, da_d
     ``want`` names the outputs to allocate when not given: any of "da", "db",
     "da_digits" ([R][K][slots] int64), "db_digits" ([N][R][slots] int64). Returns
     the dict of outputs written. ``dy`` or ``x`` may be None when its gradient
-    is not wanted."""
+    is not wanted. An FP32 ``dy`` selects ``lora_delta_grads_exact_f32dy``
+    (dV = bf16(fp32(dy * alpha)))."""
     M, R = (u if u is not None else du).shape
     K = x.shape[1] if x is not None else 8
     N = dy.shape[1] if dy is not None else 8
@@ -235,20 +240,22 @@ def lora_delta_grads_exact(dy, x, u, du, alpha: float, *, da=None, db=None, da_d
             _check(v, k, shapes[k][1], shapes[k][0])
     if x is not None:
         _check(x, "x", torch.bfloat16, (M, K))
+    dy_f32 = dy is not None and dy.dtype == torch.float32
     if dy is not None:
-        _check(dy, "dy", torch.bfloat16, (M, N))
+        _check(dy, "dy", torch.float32 if dy_f32 else torch.bfloat16, (M, N))
     if u is not None:
         _check(u, "u", torch.bfloat16, (M, R))
     if du is not None:
         _check(du, "du", torch.bfloat16, (M, R))
+    name = "lora_delta_grads_exact_f32dy" if dy_f32 else "lora_delta_grads_exact"
     if workspace is None:
-        workspace = new_workspace(lora_delta_grads_exact_workspace_size(M, K, N, R), dev)
-    rc = _lib().lora_delta_grads_exact(_ptr(dy), _ptr(x), _ptr(u), _ptr(du), float(alpha), M, K, N, R,
-                                       _ptr(outs["da"]), _ptr(outs["db"]), _ptr(outs["da_digits"]),
-                                       _ptr(outs["db_digits"]), _ptr(workspace),
-                                       workspace.numel() * workspace.element_size(), _stream(stream))
+        workspace = new_workspace(int(getattr(_lib(), name + "_workspace_size")(M, K, N, R)), dev)
+    rc = getattr(_lib(), name)(_ptr(dy), _ptr(x), _ptr(u), _ptr(du), float(alpha), M, K, N, R,
+                               _ptr(outs["da"]), _ptr(outs["db"]), _ptr(outs["da_digits"]),
+                               _ptr(outs["db_digits"]), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != LORA_OK:
-        raise LoraDeltaError(rc, "lora_delta_grads_exact")
+        raise LoraDeltaError(rc, name)
     return {k: v for k, v in outs.items() if v is not None}
 
 

@@ -273,6 +273,18 @@ lora_status lora_delta_grads_exact(const void *dy, const void *x, const void *u,
                                    void *stream);
 
 /*
+ * The exact mode with a binary32 dY (as lora_delta_bwd_f32dy): dV = bf16(fp32(dy * alpha))
+ * is formed by a first launch into the workspace (after the digit kernel's scratch), and
+ * the exact pass reads it with alpha = 1. dy [M][N] fp32; everything else as for
+ * lora_delta_grads_exact; workspace >= lora_delta_grads_exact_f32dy_workspace_size bytes.
+ */
+size_t lora_delta_grads_exact_f32dy_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
+lora_status lora_delta_grads_exact_f32dy(const float *dy, const void *x, const void *u, const void *du, float alpha,
+                                         int64_t M, int64_t K, int64_t N, int64_t R, float *da, float *db,
+                                         int64_t *da_digits, int64_t *db_digits, void *workspace,
+                                         size_t workspace_bytes, void *stream);
+
+/*
  * out_digits = a + b over n digit arrays (n outputs, 21 int64 each), written
  * normalised; out_digits may be a or b (in place). b NULL: out_digits = a,
  * normalised (e.g. after an int64 sum all-reduce of digit arrays across ranks,

@@ -261,3 +261,30 @@ def test_exact_mode_host_checks(lib):
         assert call() in (6, 7)
         assert call(M=0) in (6, 7)                                # M = 0 still writes zero gradients
         assert lib.lora_delta_exact_finalize(FAKE, 4, FAKE, None) in (6, 7)
+
+
+def test_exact_f32dy_host_checks(lib):
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    f = lib.lora_delta_grads_exact_f32dy
+    g = lib.lora_delta_grads_exact_f32dy_workspace_size
+    need = int(g(64, 128, 96, 16))
+    # the exact pass's scratch plus the BF16 dV (M x N x 2 bytes, 256-byte rounded)
+    assert need == ld.lora_delta_grads_exact_workspace_size(64, 128, 96, 16) + 64 * 96 * 2
+    assert int(g(64, 100, 96, 16)) == 0
+    ok = [FAKE] * 9
+
+    def call(p=ok, M=64, K=128, N=96, R=16, ws=need):
+        dy, x, u, du, da, db, dad, dbd, w = p
+        return f(dy, x, u, du, 2.0, M, K, N, R, da, db, dad, dbd, w, ws, None)
+
+    assert call([None] + ok[1:]) == 1          # dB asked for without dy
+    assert call(ok[:8] + [None]) == 1          # workspace
+    assert call(K=100) == 2
+    assert call(R=12) == 4
+    assert call([FAKE + 4] + ok[1:]) == 3
+    assert call(ws=need - 256) == 5
+    import torch
+
+    if not torch.cuda.is_available():
+        assert call() in (6, 7)

@@ -243,3 +243,27 @@ def test_small_factors_take_the_exact_side_path(oracle, frac):
     da, db = EO.grads(dv, d["x"], d["u"], d["du"])
     _bits_equal("dA", out["da"], da)
     _bits_equal("dB", out["db"], db)
+
+
+def test_f32_dy(oracle):
+    """lora_delta_grads_exact with a binary32 dY: dB is the exact oracle's on
+    dV = bf16(fp32(dy * alpha)) (the FP32-dY backward's dV), bit for bit; dY values BF16 holds
+    exactly give the BF16-dY call's bits."""
+    M, K, N, R, alpha = 300, 64, 136, 16, 0.3
+    d = _inputs(M, K, N, R, seed=21)
+    rng = np.random.default_rng(5)
+    dy32 = (rng.standard_normal((M, N)) * np.exp2(rng.integers(-20, 20, (M, N)))).astype(np.float32)
+    t = {k: G.dev_bf16(v) for k, v in d.items()}
+    out = ld.lora_delta_grads_exact(torch.from_numpy(dy32).cuda(), t["x"], t["u"], t["du"], alpha,
+                                    want=("da", "db", "db_digits"))
+    torch.cuda.synchronize()
+    dv = oracle.dv_f32(dy32, alpha)
+    _bits_equal("dB digits (f32 dy)", out["db_digits"].cpu().numpy(), EO.digits(d["u"], dv, transpose=True))
+    _bits_equal("dB (f32 dy)", out["db"].cpu().numpy(), EO.exact_matmul(d["u"], dv, transpose=True))
+    _bits_equal("dA (f32 dy call)", out["da"].cpu().numpy(), EO.exact_matmul(d["du"], d["x"]))
+    # BF16-representable binary32 dY: the same bits as the BF16-dY call
+    dyb = S.bf16_bits_to_f64(d["dy"]).astype(np.float32)
+    a = ld.lora_delta_grads_exact(torch.from_numpy(dyb).cuda(), t["x"], t["u"], t["du"], alpha, want=("db",))
+    b = ld.lora_delta_grads_exact(t["dy"], t["x"], t["u"], t["du"], alpha, want=("db",))
+    torch.cuda.synchronize()
+    _bits_equal("dB: f32 dy holding BF16 values", a["db"].cpu().numpy(), b["db"].cpu().numpy())
