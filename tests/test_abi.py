@@ -288,3 +288,25 @@ def test_exact_f32dy_host_checks(lib):
 
     if not torch.cuda.is_available():
         assert call() in (6, 7)
+
+
+def test_no_base_weight_in_the_signatures():
+    """The operator never receives the frozen base weight, so it can neither read nor return a
+    gradient for it (page "[DSv4][P5-3] shared_grouped_lora_delta ...", "Acceptance criteria",
+    items 2 and 3): the parameters of every compute entry point are the LoRA operands, their
+    gradients, shapes, scale, scratch and stream only."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    allowed = {"x", "a", "b", "dy", "u", "du", "alpha", "M", "K", "N", "R", "delta_y", "dx", "da", "db",
+               "da_digits", "db_digits", "workspace", "workspace_bytes", "stream", "y_bf16", "sites", "count"}
+    for name in ("lora_delta_fwd", "lora_delta_fwd_bf16", "lora_delta_bwd", "lora_delta_bwd_f32dy",
+                 "lora_delta_grads_exact", "lora_delta_grads_exact_f32dy", "lora_delta_fwd_noalloc",
+                 "lora_delta_fwd_grouped", "lora_delta_bwd_grouped"):
+        m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", text)
+        assert m, name
+        params = [re.split(r"[\s*]+", p.strip())[-1] for p in m.group(1).split(",")]
+        assert set(params) <= allowed, f"{name}: unexpected parameters {set(params) - allowed}"
+    for struct in ("lora_fwd_site", "lora_bwd_site"):
+        m = re.search(r"typedef struct " + struct + r"\s*\{(.*?)\}", text, flags=re.S)
+        assert m, struct
+        fields = re.findall(r"(\w+)\s*;", m.group(1).replace(",", ";"))
+        assert set(fields) <= allowed, f"{struct}: unexpected fields {set(fields) - allowed}"
