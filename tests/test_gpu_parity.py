@@ -271,6 +271,14 @@ def test_mlp_insertion_points(oracle, site):
     out = G.run(d, w.shape.alpha)
     _sampled_parity(oracle, d, w.shape.alpha, out, nrows=24, ncols=24)
     _check_subbatches(d, w.shape.alpha, out, (8,))
+    # acceptance criteria of the same page: the gradients are finite and not all zero, at both
+    # insertion points
+    for k in ("delta_y", "dx", "da", "db"):
+        v = out[k]
+        assert np.isfinite(v).all(), f"{site}: {k} has a non-finite value"
+        assert np.count_nonzero(v) > v.size // 2, f"{site}: {k} is mostly zero"
+    for k in ("u", "du"):
+        assert ((out[k] & 0x7F80) != 0x7F80).all(), f"{site}: {k} has an infinite or NaN value"
 
 
 @pytest.mark.parametrize("M", [1, 8, 64])
