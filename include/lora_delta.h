@@ -258,10 +258,12 @@ lora_status lora_delta_fwd_noalloc(const void *x, const void *a, const void *b, 
  * dA is computed when da or da_digits is given, dB when db or db_digits is;
  * the inputs it reads must then be non-NULL (x, du for dA; dy, u for dB) unless
  * M = 0, which writes zero gradients (+0, and all-zero digit arrays).
- * M < 2^30 (digit headroom); R * K and R * N below 2^31. workspace: >= lora_delta_grads_exact_workspace_size
- * bytes of scratch (no status block: no kernel of this call waits).
- * Kernels: per gradient, the digit kernel (integer accumulation over row
- * chunks) and the reduce kernel (adds the chunks' digits, normalises, rounds).
+ * M < 2^30 (digit headroom); R * K and R * N below 2^31. workspace: at least
+ * lora_delta_grads_exact_workspace_size bytes of scratch (no status block: no
+ * kernel of this call waits). Kernels: per gradient, the digit kernel (integer
+ * accumulation over 64-row units of 16 x 64 output tiles) and the reduce kernel
+ * (adds the units' windows and digits, normalises, rounds); with profile events
+ * set, events[0] is recorded before dA, events[1] after it, events[2] after dB.
  * The call is much slower than lora_delta_bwd's dA and dB: integer units, not
  * tensor cores.
  */
