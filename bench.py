@@ -38,6 +38,7 @@ METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
 KERNELS = ["down U", "up dY_lora", "dy dU+dB", "up dX", "wgrad dA", "combine dA+dB"]
 N_FWD = 2      # forward kernels; the rest are the backward's
 N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
+HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal (context beside the measured copy peak)
 PROF_EVERY = 48   # one step in this many carries per-kernel events; the rest replay a CUDA graph
 
 
@@ -757,7 +758,9 @@ def run_ours(args, world, rank, local):
             "steps_per_s": round(1e3 / ms_step, 1),
             "roofline_step": {"bound": "hbm", "achieved": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
                               "peak": peak, "unit": "GB/s", "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
-                              "peak_kind": peak_kind, "algorithmic_bytes": total_bytes},
+                              "peak_kind": peak_kind, "algorithmic_bytes": total_bytes,
+                              "frac_of_nominal": round(total_bytes / (ms_step * 1e-3) / 1e9 / HBM_NOMINAL_GBS, 4),
+                              "nominal_gbs": HBM_NOMINAL_GBS},
             "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes": alg[dominant], "peak_kind": peak_kind},
