@@ -5,9 +5,12 @@ Qwen-14B step reimplementation ...", section "Finding 2"): M=8192 tokens,
 K=N=4096, R=16, alpha=2, BF16 inputs with FP32 accumulation; X ~ N(0,1),
 A ~ N(0,1/4096), B ~ N(0,1/16), dY ~ N(0,1e-2); seeded synthetic data.
 
-One step = lora_delta_fwd + lora_delta_bwd through the C ABI (6 kernels).
+One step = lora_delta_fwd + lora_delta_bwd through the C ABI (6 kernels),
+called eagerly every step (no CUDA graph, no events inside the timed region).
 Metric: algorithmic HBM bytes of the step / step time (GB/s); ms per step and
-the fraction of the measured HBM copy peak are reported beside it.
+the fraction of the measured HBM copy peak are reported beside it. After the
+timed region, untimed passes give the same steps replayed from a CUDA graph
+(`graph_ms_per_step`) and the per-kernel CUDA-event breakdown (`kernels`).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -39,7 +42,8 @@ KERNELS = ["down U", "up dY_lora", "dy dU+dB", "up dX", "wgrad dA", "combine dA+
 N_FWD = 2      # forward kernels; the rest are the backward's
 N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
 HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal (context beside the measured copy peak)
-PROF_EVERY = 48   # one step in this many carries per-kernel events; the rest replay a CUDA graph
+GRAPH_STEPS = 48   # steps captured in the CUDA graph of the untimed graph pass
+PROF_STEPS = 16    # steps of the untimed per-kernel event pass
 
 
 def algorithmic_bytes(M, K, N, R):
@@ -172,6 +176,33 @@ def max_over_ranks(value: float, world: int) -> float:
     t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def kernel_event_pass(ld, names, n_fwd, steps, stream, fwd, bwd):
+    """Average duration of each kernel of a forward + backward step (names: the forward's n_fwd
+    kernels, then the backward's), from CUDA events the library records between its launches."""
+    import torch
+
+    n_bwd = len(names) - n_fwd
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_fwd + 1)] for _ in range(steps)]
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_bwd + 1)] for _ in range(steps)]
+    for evs in fev + bev:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ld.lora_delta_set_profile_events(fev[i])
+        fwd(i)
+        ld.lora_delta_set_profile_events(bev[i])
+        bwd(i)
+    ld.lora_delta_set_profile_events(None)
+    torch.cuda.synchronize()
+    out = {}
+    for j, name in enumerate(names[:n_fwd]):
+        out[name] = statistics.mean(f[j].elapsed_time(f[j + 1]) for f in fev)
+    for j, name in enumerate(names[n_fwd:]):
+        out[name] = statistics.mean(b[j].elapsed_time(b[j + 1]) for b in bev)
+    return out
 
 
 # ------------------------------------------------------------------ oracle
@@ -444,11 +475,12 @@ def decode_variants(ld, dev, steps=50, reps=20, copies=8):
     return out
 
 
-def grouped_variants(ld, dev, steps=10, reps=20):
+def grouped_variants(ld, dev, peak, steps=10, reps=20):
     """The MLP insertion points of the pages (fc1 K5120 -> N17408, fc2 K17408 -> N5120,
     M4096, R16, alpha 1; random BF16 inputs drawn on the device), forward + backward of
     both sites: one grouped call per pass against two single-site calls per pass, each
-    CUDA-graph timed."""
+    CUDA-graph timed; then an untimed per-kernel event pass of the single-site fc1 and fc2
+    calls and of the grouped call, each kernel against its algorithmic bytes."""
     import torch
 
     g = torch.Generator(device=dev)
@@ -511,6 +543,27 @@ def grouped_variants(ld, dev, steps=10, reps=20):
         ms = e0.elapsed_time(e1) / (reps * steps)
         out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
                      "launches_per_step": launches}
+    # per-kernel event pass (untimed): single-site fc1, single-site fc2, grouped fc1 + fc2
+    stream = torch.cuda.current_stream(dev)
+
+    def single(s):
+        return (lambda i: ld.lora_delta_fwd(s["x"], s["a"], s["b"], s["alpha"], delta_y=s["delta_y"], u=s["u"],
+                                            workspace=s["wf"], stream=stream),
+                lambda i: ld.lora_delta_bwd(s["dy"], s["x"], s["a"], s["b"], s["u"], s["alpha"], dx=s["dx"],
+                                            da=s["da"], db=s["db"], du=s["du"], workspace=s["wb"], stream=stream))
+
+    passes = (("mlp_fc1", *single(sites[0]), sites[:1]), ("mlp_fc2", *single(sites[1]), sites[1:]),
+              ("mlp_fc1_fc2_grouped", lambda i: ld.lora_delta_fwd_grouped(fw_sites, workspace=wfg, stream=stream),
+               lambda i: ld.lora_delta_bwd_grouped(bw_sites, workspace=wbg, stream=stream), sites))
+    for label, f, b, ss in passes:
+        kavg = kernel_event_pass(ld, KERNELS, N_FWD, 8, stream, f, b)
+        alg = {k: sum(algorithmic_bytes(M, s["x"].shape[1], s["b"].shape[0], R)[k] for s in ss) for k in KERNELS}
+        kern = {k: {"ms": round(kavg[k], 5), "algorithmic_bytes": alg[k],
+                    "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
+                    "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None} for k in KERNELS}
+        worst = min((k for k in KERNELS if alg[k]), key=lambda k: kern[k]["frac"])
+        out.setdefault(label, {}).update({"kernels": kern, "worst_kernel": worst,
+                                          "kernels_note": "untimed pass of 8 steps with a CUDA event between kernels"})
     for s in sites:
         assert ld.lora_delta_device_status(s["wf"]) == 0 and ld.lora_delta_device_status(s["wb"]) == 0
     assert ld.lora_delta_device_status(wfg) == 0 and ld.lora_delta_device_status(wbg) == 0
@@ -562,37 +615,7 @@ def run_ours(args, world, rank, local):
         step(i)
     torch.cuda.synchronize()
 
-    # Timed region: blocks of PROF_EVERY steps. The first step of each block runs through the API
-    # with per-kernel CUDA events (a mark before the first kernel and after each); the other
-    # PROF_EVERY - 1 steps replay one CUDA graph of those same API calls (kernel launches only,
-    # programmatic dependent launch kept between them). Steps past the last full block run
-    # through the API without events.
-    n_blocks = args.steps // PROF_EVERY
-    prof_steps = [b * PROF_EVERY for b in range(n_blocks)]
-    tail_prof = [] if n_blocks else list(range(min(args.steps, 8)))   # short runs: events on the first steps
-    n_bwd = len(KERNELS) - N_FWD
-    fev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(N_FWD + 1)] for i in prof_steps}
-    bev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(n_bwd + 1)] for i in prof_steps + tail_prof}
-    fev.update({i: [torch.cuda.Event(enable_timing=True) for _ in range(N_FWD + 1)] for i in tail_prof})
-    for evs in list(fev.values()) + list(bev.values()):
-        for e in evs:
-            e.record(stream)
-    graph = None
-    if n_blocks:
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                gst = torch.cuda.current_stream(dev)
-                for j in range(1, PROF_EVERY):
-                    x, dy = Xs[j % N_ROTATE], DYs[j % N_ROTATE]
-                    ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=gst)
-                    ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=gst)
-        stream.wait_stream(cap)
-        graph.replay()          # warm the graph
-    torch.cuda.synchronize()
-
+    # Timed region: every step calls the two API entry points eagerly, as a training loop does.
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -600,44 +623,50 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else int(
             os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])) as clocks:
         start.record(stream)
-        for i in prof_steps:
-            x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
-            ld.lora_delta_set_profile_events(fev[i])
-            ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
-            ld.lora_delta_set_profile_events(bev[i])
-            ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
-            ld.lora_delta_set_profile_events(None)
-            graph.replay()      # steps i + 1 .. i + PROF_EVERY - 1 (same rotation phase: PROF_EVERY % 3 == 0)
-        for i in range(n_blocks * PROF_EVERY, args.steps):
-            if i in tail_prof:
-                x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
-                ld.lora_delta_set_profile_events(fev[i])
-                ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=stream)
-                ld.lora_delta_set_profile_events(bev[i])
-                ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=stream)
-                ld.lora_delta_set_profile_events(None)
-            else:
-                step(i)
+        for i in range(args.steps):
+            step(i)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     elapsed_ms = start.elapsed_time(stop)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     ms_step = elapsed_ms / args.steps
-
-    # per-kernel average durations over the sampled steps
-    ktimes = {k: [] for k in KERNELS}
-    for i in prof_steps + tail_prof:
-        f, b = fev[i], bev[i]
-        for j, name in enumerate(KERNELS[:N_FWD]):
-            ktimes[name].append(f[j].elapsed_time(f[j + 1]))
-        for j, name in enumerate(KERNELS[N_FWD:]):
-            ktimes[name].append(b[j].elapsed_time(b[j + 1]))
-    kavg = {k: statistics.mean(v) for k, v in ktimes.items()}
     status = (ld.lora_delta_device_status(wf), ld.lora_delta_device_status(wb))
     if status != (0, 0):
         raise SystemExit(f"device status block reports {status}")
 
+    # Untimed: the same steps replayed from a CUDA graph (launch cost on the host and between
+    # kernels as low as it gets), for comparison with the eager steps above.
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            gst = torch.cuda.current_stream(dev)
+            for j in range(GRAPH_STEPS):
+                x, dy = Xs[j % N_ROTATE], DYs[j % N_ROTATE]
+                ld.lora_delta_fwd(x, A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=gst)
+                ld.lora_delta_bwd(dy, x, A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU, workspace=wb, stream=gst)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_rep = max(1, min(20, args.steps // GRAPH_STEPS))
+    g0.record(stream)
+    for _ in range(n_rep):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / (n_rep * GRAPH_STEPS)
+    del graph
+
+    # Untimed: per-kernel CUDA events (a mark before the first kernel of each call and after each
+    # kernel). The events sit between the kernels, so each figure includes its launch boundary.
+    kavg = kernel_event_pass(ld, KERNELS, N_FWD, PROF_STEPS, stream,
+                             lambda i: ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf,
+                                                         stream=stream),
+                             lambda i: ld.lora_delta_bwd(DYs[i % N_ROTATE], Xs[i % N_ROTATE], A, B, U, alpha, dx=DX,
+                                                         da=DA, db=DB, du=DU, workspace=wb, stream=stream))
     alg = algorithmic_bytes(M, K, N, R)
     total_bytes = sum(alg.values())
     peak, peak_kind = measured_peaks()
@@ -653,7 +682,7 @@ def run_ours(args, world, rank, local):
     if not args.no_variants:
         variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev)
         variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
-        variants.update(grouped_variants(ld, dev))
+        variants.update(grouped_variants(ld, dev, measured_peaks()[0]))
         variants.update(exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(decode_variants(ld, dev))
 
@@ -752,9 +781,10 @@ def run_ours(args, world, rank, local):
                        "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
                              "output stream per step, all larger than the 129 MB L2",
                        "parallelism": f"replicas x{world}",
-                       "timing": (f"{PROF_EVERY - 1} of every {PROF_EVERY} steps replay a CUDA graph of the API calls; "
-                                  "the other step goes through the API with per-kernel CUDA events"
-                                  if args.steps >= PROF_EVERY else "every step through the API")},
+                       "timing": "every timed step calls lora_delta_fwd and lora_delta_bwd eagerly (Python binding, "
+                                 "C ABI); CUDA events only at the two ends of the timed region"},
+            "graph_ms_per_step": round(graph_ms, 5),
+            "graph_note": f"the same steps replayed from a CUDA graph of {GRAPH_STEPS} steps (untimed pass)",
             "steps_per_s": round(1e3 / ms_step, 1),
             "roofline_step": {"bound": "hbm", "achieved": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
                               "peak": peak, "unit": "GB/s", "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
@@ -764,6 +794,8 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes": alg[dominant], "peak_kind": peak_kind},
+            "kernels_note": f"untimed pass of {PROF_STEPS} steps with a CUDA event between kernels (each figure "
+                            "includes its launch boundary; events stop the kernels' launch overlap)",
             "kernels": {k: {"ms": round(kavg[k], 5), "algorithmic_bytes": alg[k],
                             "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
                             "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None}
@@ -781,7 +813,7 @@ def run_ours(args, world, rank, local):
 def main():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)

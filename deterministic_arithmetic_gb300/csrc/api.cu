@@ -143,7 +143,7 @@ int grid_for(int64_t units, int nsm) { return int(std::max<int64_t>(1, std::min<
 
 extern "C" {
 
-const char* lora_status_str(int s) {
+const char* lora_status_str(lora_status s) {
   switch (s) {
     case LORA_OK: return "ok";
     case LORA_ERR_NULL: return "a required pointer is NULL";
@@ -166,6 +166,14 @@ size_t lora_delta_fwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R)
 size_t lora_delta_bwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
   if (check_shape(M, K, N, R) != LORA_OK) return 0;
   return bwd_layout(M, K, N, R).total;
+}
+
+size_t lora_delta_fwd_workspace(int64_t M, int64_t K, int64_t N, int64_t R) {
+  return lora_delta_fwd_workspace_size(M, K, N, R);
+}
+
+size_t lora_delta_bwd_workspace(int64_t M, int64_t K, int64_t N, int64_t R) {
+  return lora_delta_bwd_workspace_size(M, K, N, R);
 }
 
 }  // extern "C"
@@ -271,7 +279,6 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
     UpSite& q = uargs.s[j];
     if (!make_map(&d.in, p.x, false, p.M, p.K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&d.w, p.a, false, R, p.K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&q.a, p.u, false, p.M, R, RP, 128, swizzle_for_span(span)) ||
         !make_map(&q.b, p.b, false, p.N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
         !(y_bf16 ? make_map(&q.out, p.delta_y, false, p.M, p.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
                  : make_map(&q.out, p.delta_y, true, p.M, p.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
@@ -335,8 +342,7 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     const int C = int(ceil_div(p.M, kWgradChunk));
     UpSite& q = uargs.s[j];
     WgSite& wa = aargs.s[j];
-    if (!make_map(&q.a, p.du, false, M, R, RP, 128, swizzle_for_span(span)) ||
-        !make_map(&q.b, p.a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_map(&q.b, p.a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&q.out, p.dx, true, M, K, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&wa.in, p.x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&wa.g, p.du, false, M, R, RP, 64, swizzle_for_span(span)))

@@ -17,8 +17,15 @@ namespace lora {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s, for teardown waits
 
-// Status word codes (first word of the caller's workspace).
+// Status block (the first bytes of the caller's workspace), 32-bit words:
+//   word 0  status code, written by a kernel that gives up on a wait: (site << 8) | kDevTimeout;
+//           only while the word is zero, so the first code (the root cause) stays
+//   word 2  test hook: a kernel kind (kKindDown ...); the producer warp of that kernel first waits
+//           on an mbarrier that nothing completes, so the wait runs out (0: off)
+//   word 3  test hook: the wait limit in microseconds (0: kWaitLimitNs)
+// Words 2 and 3 are read, never written, by the kernels.
 constexpr uint32_t kDevTimeout = 1u;
+constexpr uint32_t kKindDown = 1u, kKindUp = 2u, kKindDy = 3u, kKindWgrad = 4u;
 
 // ------------------------------------------------------------ small utils
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -59,11 +66,22 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0u;
 }
 
-// Per-CTA abort state: a flag in shared memory and the caller's status word.
+// Per-CTA abort state: a flag in shared memory, the caller's status word and the wait limit.
 struct Abort {
   volatile uint32_t* flag;   // shared memory
   uint32_t* status;          // global (may be null)
+  uint64_t limit_ns;         // a wait gives up after this long
 };
+// The abort state of a kernel: the wait limit is kWaitLimitNs unless word 3 of the status block
+// overrides it (test hook). Call after the grid dependency wait.
+__device__ __forceinline__ Abort make_abort(volatile uint32_t* flag, uint32_t* status) {
+  const uint32_t us = status ? status[3] : 0u;
+  return Abort{flag, status, us ? uint64_t(us) * 1000ull : kWaitLimitNs};
+}
+// True when word 2 of the status block asks this kind of kernel to stall (test hook).
+__device__ __forceinline__ bool stall_requested(const uint32_t* status, uint32_t kind) {
+  return status && status[2] == kind;
+}
 
 // Slow path of a bounded wait. Returns false when the CTA is aborting: either
 // this wait ran past its limit (then it raises the abort flag and records
@@ -77,55 +95,23 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Abo
       if (honour_abort && *ab.flag) return false;
       if (global_ns() - t0 > limit_ns) {
         *ab.flag = 1u;
-        if (ab.status) *reinterpret_cast<volatile uint32_t*>(ab.status) = (site << 8) | kDevTimeout;
+        if (ab.status) atomicCAS(ab.status, 0u, (site << 8) | kDevTimeout);   // the first code stays
         return false;
       }
     }
   }
 }
 
-// ------------------------------------------------------ grid-wide barrier
-// For kernels launched cooperatively (every CTA resident at once). All
-// threads of every CTA call it; on return, every global store made by any CTA
-// before its call is visible to every thread after the call. cnt: two words,
-// zero when the launch starts (arrivals, departures); the last CTA to leave
-// puts both back to zero, so the next launch finds them at zero. The wait for
-// the last arrival gives up after kWaitLimitNs (then the CTA aborts).
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Grid-wide barrier for one thread per CTA (cooperative launches only: every
-// CTA is resident). cnt[0] counts arrivals; the wait gives up after
-// kWaitLimitNs (abort flag and status set). grid_leave then counts departures
-// in cnt[1]; the last CTA to leave zeroes both, ready for the next launch.
-static __device__ __noinline__ void grid_arrive_wait(uint32_t* cnt, uint32_t ncta, volatile uint32_t* abort_flag,
-                                                     uint32_t* status, uint32_t site) {
-  __threadfence();                                     // this CTA's stores, device-visible before arriving
-  atomicAdd(&cnt[0], 1u);
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 1; ld_acquire_gpu(&cnt[0]) < ncta; ++it) {
-    if ((it & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1u;
-      if (status) *reinterpret_cast<volatile uint32_t*>(status) = (site << 8) | kDevTimeout;
-      break;
-    }
-    __nanosleep(64);
-  }
-}
-static __device__ __forceinline__ void grid_leave(uint32_t* cnt, uint32_t ncta) {
-  if (atomicAdd(&cnt[1], 1u) == ncta - 1u) {            // every CTA has left the wait
-    atomicExch(&cnt[0], 0u);
-    atomicExch(&cnt[1], 0u);
-  }
-}
-
 // Wait for the phase of `bar` with the given parity to complete, for at most
-// kWaitLimitNs. False means "abort": skip the work, keep the control flow.
+// the abort state's limit. False means "abort": skip the work, keep the control flow.
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
   if (mbar_test(bar, parity)) return true;
-  return wait_slow(bar, parity, ab, site, kWaitLimitNs, true);
+  return wait_slow(bar, parity, ab, site, ab.limit_ns, true);
+}
+// The stall test hook: a wait on a barrier that nothing completes, given a quarter of the
+// limit so that it runs out before any wait that depends on the stalled warp.
+__device__ __forceinline__ void stall_wait(uint32_t never, Abort ab, uint32_t site) {
+  wait_slow(never, 0u, ab, site, ab.limit_ns / 4, true);
 }
 // Teardown variant: ignores the abort flag, shorter limit.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {

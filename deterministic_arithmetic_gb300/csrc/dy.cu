@@ -46,7 +46,7 @@ struct DyCfg {
   static constexpr int kEpiWarps = 8, kXfWarps = 4;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kXfWarps);
   static constexpr int kCPT = RP / 2;                      // columns of R per epilogue thread
-  static constexpr int kNumBars = 3 * kStages + 2 * kGroups + 1;
+  static constexpr int kNumBars = 3 * kStages + 2 * kGroups + 2;
   static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
   static_assert(kSliceTiles == 4 && kChunkTiles == 2, "epilogue tree shape");
   static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   auto tfull = [&](int g) { return bar0 + 8u * (3 * C::kStages + g); };
   auto tempty = [&](int g) { return bar0 + 8u * (3 * C::kStages + C::kGroups + g); };
   const uint32_t drain = bar0 + 8u * (3 * C::kStages + 2 * C::kGroups);
+  const uint32_t never = drain + 8u;   // completed by nothing (the stall test hook waits on it)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
       mbar_init(tempty(g), C::kEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0u;
     mbar_fence_init();
     for (int i = 0; i < (GR ? args.n : 1); ++i) {
@@ -144,11 +146,12 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
   }
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
-  const Abort ab{abort_flag, status};
+  const Abort ab = make_abort(abort_flag, status);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      if (stall_requested(status, kKindDy)) stall_wait(never, ab, 39);   // test hook: a wait that runs out
       const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
       Ring r;
       uint32_t issued = 0, parities = 0;

@@ -66,7 +66,7 @@ using DownArgs = Sites<DownSite, kMaxSites>;
 
 // Up-projection (dY_lora, or dX) with the U / dU combine folded in.
 struct UpSite {
-  CUtensorMap a, b, out;   // u / du rows (box 128 x RP), weight (B rows or A columns), output
+  CUtensorMap b, out;      // weight (B rows or A columns), output
   const float* part;       // [S][M][RP] slice partials of u / du
   __nv_bfloat16* out_bf16; // u / du [M][R], written here
   int S, M, Nout, n_mt, n_nt, u0;
@@ -111,27 +111,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// The same with a cooperative launch as well (every CTA resident at once): for
-// kernels with a grid-wide barrier. grid must not exceed the SM count (these
-// kernels run one CTA per SM).
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                   Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 // Work-unit counts (all launches use persistent CTAs over units).
 inline int64_t down_units(int64_t M, int64_t Kred, int RP) { return ceil_div(M, 128) * ceil_div(Kred, down_slice(RP)); }
 inline int64_t up_units(int64_t M, int64_t Nout, int RP) { return ceil_div(M, 128) * ceil_div(Nout, up_bn(RP)); }
@@ -141,9 +120,9 @@ inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil
 // word; `grid` the number of persistent CTAs.
 // args: sites filled in except n_mt, n_sl, u0 and total (set here)
 cudaError_t launch_down(int RP, bool dv, DownArgs& args, uint32_t* status, int grid, cudaStream_t st);
-// up: a = u / du rows (box 128 x RP), written by the kernel itself (prep warps); y_bf16
-// (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte swizzle. args: sites
-// filled in except n_mt, n_nt, u0 and total (set here).
+// up: the u / du rows are formed by the kernel itself from the slice partials (and written to
+// out_bf16); y_bf16 (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte
+// swizzle. args: sites filled in except n_mt, n_nt, u0 and total (set here).
 cudaError_t launch_up(int RP, bool dx, bool y_bf16, UpArgs& args, uint32_t* status, int grid, cudaStream_t st);
 // args: sites filled in except n_sl, n_ch, u0 and total (set here)
 cudaError_t launch_dy(DyArgs& args, uint32_t* status, int grid, cudaStream_t st);

@@ -46,6 +46,14 @@ lora_status scratch_address(void** out) {
   return LORA_OK;
 }
 
+// The address if a call on the current device has looked it up already, else null.
+void* known_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_scratch_ptr[dev];
+}
+
 }  // namespace
 
 extern "C" lora_status lora_delta_fwd_noalloc(const void* x, const void* a, const void* b, float alpha, int64_t M,
@@ -63,4 +71,17 @@ extern "C" lora_status lora_delta_fwd_noalloc(const void* x, const void* a, cons
   if (cudaMemsetAsync(scratch, 0, kStatusBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return LORA_ERR_CUDA;
   return lora_delta_fwd(x, a, b, alpha, M, K, N, R, delta_y, u, scratch, kScratchBytes, stream);
+}
+
+// The status block is the first word of the array; before any call on this device there is
+// nothing to report (the array starts zeroed, as every __device__ variable does).
+extern "C" lora_status lora_delta_fwd_noalloc_status(int* code) {
+  if (!code) return LORA_ERR_NULL;
+  void* scratch = known_scratch_address();
+  if (!scratch) {
+    *code = 0;
+    return LORA_OK;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
+  return lora_delta_device_status(scratch, code);
 }

@@ -8,15 +8,16 @@
 // batch-invariant", section "Summary"; the alpha scale is fused into the
 // epilogue, as that page's "Benchmark" section proposes.)
 //
-// One cooperative launch. The u / du rows are the canonical pairwise tree
-// (FP32, round to nearest) over the slice partials left by the down kernel,
-// rounded to BF16. Two prep warps per CTA form its share of the batch rows,
-// write them to u / du and meet the other CTAs at a grid-wide barrier. The
-// expansion does not wait for that barrier at first: the epilogue warps form
-// the rows of the CTA's first two units themselves, straight into those
-// units' operand stages, so the stores start at once and the barrier's wait
-// overlaps them; from the third unit on the producer loads the rows with TMA
-// after the barrier. Work unit = (128-row tile, BN-column tile), BN = 256 /
+// The u / du rows are the canonical pairwise tree (FP32, round to nearest)
+// over the slice partials left by the preceding kernel, rounded to BF16: a
+// pure function of partials that are complete when this kernel starts (stream
+// order), so every CTA forms the rows of its own units itself, straight into
+// each unit's operand stage, and no CTA ever waits for another (no grid
+// barrier, a plain launch). The epilogue warps form the rows of the CTA's
+// first two units (all 256 threads at once, so the first stores start early);
+// two row warps form those of the later units, each as soon as its stage is
+// free. The unit in column tile 0 of a row tile also writes those rows to u /
+// du (each row exactly once). Work unit = (128-row tile, BN-column tile), BN = 256 /
 // (RP / 16), units dealt out round-robin, so that at any time the CTAs write
 // one compact band of the output (consecutive units are neighbours in
 // memory), which the memory system absorbs markedly faster than each CTA
@@ -32,8 +33,9 @@
 // FP32 value rounded once more (round to nearest even), half the bytes. Each
 // 32-column box is then 32 rows x 64 bytes (64-byte swizzle).
 //
-// Warp roles: 0 = TMA producer (u / du rows, B / A weight tile), 1 = MMA
-// issuer (TMEM owner), 2..9 = epilogue, 10..11 = prep (u / du share, barrier).
+// Warp roles: 0 = TMA producer (B / A weight tile), 1 = MMA issuer (TMEM
+// owner), 2..9 = epilogue (and the rows of the first two units), 10..11 = row
+// warps (u / du rows of the later units).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -51,11 +53,11 @@ struct UpCfg {
   static constexpr int kStages = RP == 16 ? 6 : (RP == 32 ? 5 : 3);   // operand ring (weight tile from L2)
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
-  static constexpr int kEpiWarps = 8, kPrepWarps = 2;
-  static constexpr int kLocal = 2;                     // units whose u / du rows a CTA forms itself
+  static constexpr int kEpiWarps = 8, kRowWarps = 2;
+  static constexpr int kLocal = 2;                     // units whose u / du rows the epilogue warps form
   static_assert(kLocal * kBM * (RP / 8) % (32 * kEpiWarps) == 0, "whole items per epilogue thread");
   static_assert(kLocal <= kStages, "locally formed rows sit in the first stages");
-  static constexpr int kThreads = 32 * (2 + kEpiWarps + kPrepWarps);
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kRowWarps);
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
@@ -66,7 +68,7 @@ struct UpCfg {
   static constexpr int kStgBytes = 32 * kChunk * 4;    // one 32-row x 32-column FP32 box: 4 KB
   static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
   static constexpr size_t kBarOff = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 3;
+  static constexpr int kNumBars = 3 * kStages + 2 * kBufs + 3;
   static constexpr size_t kSmem = kBarOff + 1024 + kNumBars * 8 + 16;
   static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
@@ -76,7 +78,7 @@ struct UpCfg {
 // GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
 template <int RP, bool DX, bool YBF, bool GR>
 __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
-    up_kernel(const __grid_constant__ Sites<UpSite, GR ? kMaxSites : 1> args, uint32_t* status, uint32_t* sync) {
+    up_kernel(const __grid_constant__ Sites<UpSite, GR ? kMaxSites : 1> args, uint32_t* status) {
   using C = UpCfg<RP, DX>;
   // site of unit u (sites are few and ordered by first unit)
   auto site = [&](int u) -> const UpSite& {
@@ -95,13 +97,14 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   uint8_t* stg_ptr = gbase + C::kStgOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
   const uint32_t bar0 = smem_u32(bars);
-  auto full = [&](int s) { return bar0 + 8u * s; };
-  auto empty = [&](int s) { return bar0 + 8u * (C::kStages + s); };
-  auto tfull = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
-  auto tempty = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kBufs + b); };
-  const uint32_t drain = bar0 + 8u * (2 * C::kStages + 2 * C::kBufs);
-  const uint32_t ufirst = drain + 8u;   // the first kLocal units' u / du rows are in their stages
-  const uint32_t gdone = drain + 16u;   // every CTA's share of u / du is in global memory (prep warps)
+  auto full = [&](int s) { return bar0 + 8u * s; };                       // weight tile landed (TMA)
+  auto empty = [&](int s) { return bar0 + 8u * (C::kStages + s); };        // stage free (MMA done)
+  auto rows = [&](int s) { return bar0 + 8u * (2 * C::kStages + s); };     // u / du rows in the stage (row warps)
+  auto tfull = [&](int b) { return bar0 + 8u * (3 * C::kStages + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (3 * C::kStages + C::kBufs + b); };
+  const uint32_t drain = bar0 + 8u * (3 * C::kStages + 2 * C::kBufs);
+  const uint32_t ufirst = drain + 8u;   // the first kLocal units' u / du rows are in their stages (epilogue)
+  const uint32_t never = drain + 16u;   // completed by nothing (the stall test hook waits on it)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
+      mbar_init(rows(s), C::kRowWarps);
     }
     for (int b = 0; b < C::kBufs; ++b) {
       mbar_init(tfull(b), 1);
@@ -117,11 +121,10 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(ufirst, C::kEpiWarps);
-    mbar_init(gdone, 1);
+    mbar_init(never, 1);
     *abort_flag = 0u;
     mbar_fence_init();
     for (int i = 0; i < (GR ? args.n : 1); ++i) {
-      prefetch_map(&args.s[i].a);
       prefetch_map(&args.s[i].b);
       prefetch_map(&args.s[i].out);
     }
@@ -136,28 +139,23 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   grid_dependency_wait();      // predecessor done: its outputs are this kernel's inputs
   grid_dependents_launch();
-  const Abort ab{abort_flag, status};
+  const Abort ab = make_abort(abort_flag, status);
   const int total = args.total;
 
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      if (stall_requested(status, kKindUp)) stall_wait(never, ab, 10);   // test hook: a wait that runs out
       const uint64_t pol = policy_evict_last();
       Ring r;
       uint32_t issued = 0, parities = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const UpSite& P = site(u);
-        const int mt = (u - P.u0) / P.n_nt, nt = (u - P.u0) % P.n_nt;
-        const int k = (u - int(blockIdx.x)) / int(gridDim.x);     // this CTA's k-th unit
-        if (k == C::kLocal) {
-          wait(gdone, 0u, ab, 16);           // the rows of later units come from every CTA's share
-          fence_proxy_async_global();        // written by generic stores, read by TMA
-        }
+        const int nt = (u - P.u0) % P.n_nt;
         if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
           const uint32_t st = base + r.idx * C::kStageBytes;
-          mbar_expect_tx(full(r.idx), k < C::kLocal ? C::kBBytes : C::kStageBytes);
-          if (k >= C::kLocal) tma_load(st, &P.a, full(r.idx), 0, mt * C::kBM, pol);    // u / du rows of the tile
+          mbar_expect_tx(full(r.idx), C::kBBytes);
           if (DX) {
 #pragma unroll
             for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
@@ -180,7 +178,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       constexpr uint32_t lay = layout_for_span(C::kSpan);
       Ring r, b;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        bool ok = wait(full(r.idx), r.phase, ab, 13);
+        bool ok = wait(full(r.idx), r.phase, ab, 13) && wait(rows(r.idx), r.phase, ab, 16);
         if (u < int(blockIdx.x) + C::kLocal * int(gridDim.x)) ok = ok && wait(ufirst, 0u, ab, 18);
         ok = ok && wait(tempty(b.idx), b.phase ^ 1u, ab, 14);
         if (ok) {
@@ -216,9 +214,10 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     uint8_t* my_stg_ptr = stg_ptr + (warp - 2) * C::kStg * C::kStgBytes;
     {
       // the rows of u / du of this CTA's first kLocal units = bf16(tree over the S slice partials),
-      // straight into stages 0 .. kLocal-1 in the layout their TMA loads would give (rows of
-      // RP * 2 bytes, 16-byte chunks swizzled by the row's place in the 8-row swizzle atom);
-      // all loads of a thread are issued before its first store
+      // straight into stages 0 .. kLocal-1 in the layout a TMA load of the rows would give (rows
+      // of RP * 2 bytes, 16-byte chunks swizzled by the row's place in the 8-row swizzle atom);
+      // all loads of a thread are issued before its first store. A unit in column tile 0 also
+      // writes its rows to u / du.
       constexpr int kItems = C::kLocal * C::kBM * (RP / 8) / (32 * C::kEpiWarps);
       uint4 v[kItems];
 #pragma unroll
@@ -240,6 +239,13 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
         const int k = i / (C::kBM * (RP / 8)), row = (i / (RP / 8)) % C::kBM, g = i % (RP / 8);
         const uint32_t o = uint32_t(row * C::kSpan + g * 16);
         *reinterpret_cast<uint4*>(gbase + size_t(k) * C::kStageBytes + (o ^ (((o >> 7) & uint32_t(C::kSpan / 16 - 1)) << 4))) = v[j];
+        const int u = int(blockIdx.x) + k * int(gridDim.x);
+        if (u < total) {
+          const UpSite& P = site(u);
+          const int grow = ((u - P.u0) / P.n_nt) * C::kBM + row;
+          if ((u - P.u0) % P.n_nt == 0 && grow < P.M && g < R / 8)
+            *reinterpret_cast<uint4*>(P.out_bf16 + size_t(grow) * R + g * 8) = v[j];
+        }
       }
       fence_proxy_async();
       __syncwarp();
@@ -339,29 +345,34 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     }
     if (lane == 0) tma_store_wait_all<0>();
   } else {
-    // ------------------------------------------------------- prep warps
-    // This CTA's share of the batch rows of u / du = bf16(tree over the S slice partials), then
-    // the grid-wide barrier (cooperative launch: every CTA is resident); its wait overlaps the
-    // first unit, whose rows the epilogue warps formed themselves.
+    // -------------------------------------------------------- row warps
+    // The u / du rows of this CTA's units from the kLocal-th on: bf16(tree over the S slice
+    // partials) into the unit's stage once the stage is free (the producer brings only the
+    // weight tile); a unit in column tile 0 also writes its rows to u / du.
     const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
-    for (int si = 0; si < (GR ? args.n : 1); ++si) {
-      const UpSite& P = args.s[si];
-      const int r0 = int(int64_t(P.M) * blockIdx.x / gridDim.x), r1 = int(int64_t(P.M) * (blockIdx.x + 1) / gridDim.x);
-      const float* __restrict__ part = P.part;
-      __nv_bfloat16* __restrict__ out_bf16 = P.out_bf16;
-      for (int i = t; i < (r1 - r0) * (R / 8); i += 32 * C::kPrepWarps) {
-        const int row = r0 + i / (R / 8), g = i % (R / 8);
-        *reinterpret_cast<uint4*>(out_bf16 + size_t(row) * R + g * 8) =
-            slices_to_bf16x8(part + size_t(row) * RP + g * 8, size_t(P.M) * RP, P.S);
+    Ring r;
+    int k = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++k) {
+      if (k >= C::kLocal && wait(empty(r.idx), r.phase ^ 1u, ab, 19)) {
+        const UpSite& P = site(u);
+        const int mt = (u - P.u0) / P.n_nt, nt = (u - P.u0) % P.n_nt;
+        uint8_t* stage = gbase + size_t(r.idx) * C::kStageBytes;
+        for (int i = t; i < C::kBM * (RP / 8); i += 32 * C::kRowWarps) {
+          const int row = i / (RP / 8), g = i % (RP / 8);
+          const int grow = mt * C::kBM + row;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (grow < P.M && g < R / 8) {
+            v = slices_to_bf16x8(P.part + size_t(grow) * RP + g * 8, size_t(P.M) * RP, P.S);
+            if (nt == 0) *reinterpret_cast<uint4*>(P.out_bf16 + size_t(grow) * R + g * 8) = v;
+          }
+          const uint32_t o = uint32_t(row * C::kSpan + g * 16);
+          *reinterpret_cast<uint4*>(stage + (o ^ (((o >> 7) & uint32_t(C::kSpan / 16 - 1)) << 4))) = v;
+        }
+        fence_proxy_async();                 // generic writes, read by the tensor core
       }
-    }
-    __threadfence();
-    named_bar(1, 32 * C::kPrepWarps);
-    if (t == 0) {
-      grid_arrive_wait(sync, gridDim.x, abort_flag, status, 10);
-      fence_proxy_async_global();
-      mbar_arrive(gdone);
-      grid_leave(sync, gridDim.x);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rows(r.idx));
+      r.next<C::kStages>();
     }
   }
 
@@ -386,11 +397,10 @@ static cudaError_t launch_one(UpArgs& args, uint32_t* status, int grid, cudaStre
   }
   args.total = u0;
   if constexpr (GR)
-    return launch_pdl_coop(up_kernel<RP, DX, YBF, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, args, status,
-                           status + 1);
+    return launch_pdl(up_kernel<RP, DX, YBF, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, args, status);
   else
-    return launch_pdl_coop(up_kernel<RP, DX, YBF, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, first_site(args),
-                           status, status + 1);
+    return launch_pdl(up_kernel<RP, DX, YBF, GR>, dim3(grid), dim3(C::kThreads), C::kSmem, st, first_site(args),
+                      status);
 }
 
 template <int RP, bool DX, bool YBF>

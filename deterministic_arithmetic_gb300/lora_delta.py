@@ -69,9 +69,14 @@ def _lib() -> ctypes.CDLL:
             lib.lora_delta_bwd_f32dy.restype = ctypes.c_int
             lib.lora_delta_bwd_f32dy_workspace_size.argtypes = [_i64, _i64, _i64, _i64]
             lib.lora_delta_bwd_f32dy_workspace_size.restype = ctypes.c_size_t
-        for fn in (lib.lora_delta_fwd_workspace_size, lib.lora_delta_bwd_workspace_size):
+        for fn in (lib.lora_delta_fwd_workspace_size, lib.lora_delta_bwd_workspace_size,
+                   lib.lora_delta_fwd_workspace, lib.lora_delta_bwd_workspace):
             fn.argtypes = [_i64, _i64, _i64, _i64]
             fn.restype = ctypes.c_size_t
+        lib.lora_delta_fwd_noalloc.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp]
+        lib.lora_delta_fwd_noalloc.restype = ctypes.c_int
+        lib.lora_delta_fwd_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.lora_delta_fwd_noalloc_status.restype = ctypes.c_int
         if hasattr(lib, "lora_delta_fwd_grouped"):
             lib.lora_delta_fwd_grouped_workspace_size.argtypes = [ctypes.POINTER(FwdSite), ctypes.c_int, _i64]
             lib.lora_delta_fwd_grouped_workspace_size.restype = ctypes.c_size_t
@@ -139,6 +144,14 @@ def lora_delta_fwd_workspace_size(M: int, K: int, N: int, R: int) -> int:
 
 def lora_delta_bwd_workspace_size(M: int, K: int, N: int, R: int) -> int:
     return int(_lib().lora_delta_bwd_workspace_size(M, K, N, R))
+
+
+def lora_delta_fwd_workspace(M: int, K: int, N: int, R: int) -> int:
+    return int(_lib().lora_delta_fwd_workspace(M, K, N, R))
+
+
+def lora_delta_bwd_workspace(M: int, K: int, N: int, R: int) -> int:
+    return int(_lib().lora_delta_bwd_workspace(M, K, N, R))
 
 
 def new_workspace(nbytes: int, device) -> torch.Tensor:
@@ -306,6 +319,34 @@ def lora_delta_device_status(workspace: torch.Tensor) -> int:
     rc = _lib().lora_delta_device_status(_ptr(workspace), ctypes.byref(code))
     if rc not in (LORA_OK, 8):
         raise LoraDeltaError(rc, "lora_delta_device_status")
+    return int(code.value)
+
+
+def lora_delta_fwd_noalloc(x, a, b, alpha: float, *, delta_y=None, u=None, stream=None):
+    """Forward without a workspace (scratch from the library's fixed device array): for callers
+    that may not allocate device memory. Same outputs and bits as ``lora_delta_fwd``."""
+    M, K = x.shape
+    R = a.shape[0]
+    N = b.shape[0]
+    _check(x, "x", torch.bfloat16, (M, K)); _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R))
+    if delta_y is None:
+        delta_y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if u is None:
+        u = torch.empty((M, R), dtype=torch.bfloat16, device=x.device)
+    _check(delta_y, "delta_y", torch.float32, (M, N)); _check(u, "u", torch.bfloat16, (M, R))
+    rc = _lib().lora_delta_fwd_noalloc(_ptr(x), _ptr(a), _ptr(b), float(alpha), M, K, N, R, _ptr(delta_y), _ptr(u),
+                                       _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_fwd_noalloc")
+    return delta_y, u
+
+
+def lora_delta_fwd_noalloc_status() -> int:
+    """Device status code of the latest ``lora_delta_fwd_noalloc`` call on the current device."""
+    code = ctypes.c_int(0)
+    rc = _lib().lora_delta_fwd_noalloc_status(ctypes.byref(code))
+    if rc not in (LORA_OK, 8):
+        raise LoraDeltaError(rc, "lora_delta_fwd_noalloc_status")
     return int(code.value)
 
 

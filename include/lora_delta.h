@@ -36,14 +36,28 @@
  *   - Argument errors are detected on the host before anything is enqueued.
  *   - `workspace` is scratch owned by the caller, at least the size the
  *     matching *_workspace_size() query returns, 256-byte aligned. Its first
- *     256 bytes are a device status block: they must be zero before the first
- *     call that uses the workspace (for example, allocate it zeroed); a kernel
- *     that gives up on an internal wait writes a non-zero code there and
- *     returns (read it with lora_delta_device_status). The block also holds
- *     the counters of a grid-wide barrier, which every call that completes
- *     without such a code leaves at zero; after a non-zero code, zero the
- *     block again before reusing the workspace. A workspace must not be
- *     shared by calls that may run concurrently.
+ *     256 bytes are a device status block, which must be zero before the first
+ *     call that uses the workspace (for example, allocate it zeroed). Its
+ *     32-bit words:
+ *       word 0  status: a kernel that gives up on an internal wait (every wait
+ *               is bounded, 1 s by default) writes (site << 8) | 1 there, unless
+ *               the word already holds a code (the first failure stays), and
+ *               returns; the call's outputs are then undefined. The code stays
+ *               until the caller clears the word (read it with
+ *               lora_delta_device_status). No kernel waits for another CTA, and
+ *               nothing else in the block carries state from call to call, so
+ *               a call after a timed-out one needs no reset to run correctly.
+ *       word 2  test hook, 0 for normal use: a kernel kind (1 down-projection,
+ *               2 up-projection / dX, 3 fused dU + dB pass, 4 weight gradients)
+ *               whose producer warp first waits on a barrier that nothing
+ *               completes, so that the wait runs out (failure-path tests).
+ *       word 3  test hook, 0 for normal use: the wait limit in microseconds.
+ *     The library never writes words 2 and 3. A workspace must not be shared
+ *     by calls that may run concurrently.
+ *   - The library keeps per-device state for the life of the process (kernel
+ *     attributes set on first use, the device address of the no-allocation
+ *     scratch array). It does not survive cudaDeviceReset or a reset of the
+ *     device's primary context: do not call the library after either.
  */
 #ifndef LORA_DELTA_H
 #define LORA_DELTA_H
@@ -174,9 +188,13 @@ lora_status lora_delta_bwd(const void *dy, const void *x, const void *a, const v
 /* Workspace bytes the calls need (0 if the shape is invalid). */
 size_t lora_delta_fwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
 size_t lora_delta_bwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R);
+/* The same two queries under the shorter names of the boundary's first
+ * description (same results). */
+size_t lora_delta_fwd_workspace(int64_t M, int64_t K, int64_t N, int64_t R);
+size_t lora_delta_bwd_workspace(int64_t M, int64_t K, int64_t N, int64_t R);
 
-/* Static description of a status code. */
-const char *lora_status_str(int status);
+/* Static description of a status code (unknown codes give "unknown status"). */
+const char *lora_status_str(lora_status status);
 
 /*
  * Reads the device status block at the start of `workspace` (synchronous:
@@ -225,6 +243,16 @@ size_t lora_delta_describe(char *buf, size_t len);
  */
 lora_status lora_delta_fwd_noalloc(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K,
                                    int64_t N, int64_t R, float *delta_y, void *u, void *stream);
+
+/*
+ * Status block of lora_delta_fwd_noalloc on the current device (the caller has
+ * no workspace to pass to lora_delta_device_status). Synchronous: waits for the
+ * whole device, then reads the block that the latest lora_delta_fwd_noalloc call
+ * on this device used; the next call clears it again. *code and the return value
+ * as for lora_delta_device_status (0 and LORA_OK when no kernel gave up, also
+ * when no lora_delta_fwd_noalloc call has run on this device yet).
+ */
+lora_status lora_delta_fwd_noalloc_status(int *code);
 
 /*
  * Exact mode of the weight gradients (page "det-train", sections "Method",

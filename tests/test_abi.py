@@ -28,12 +28,30 @@ def declared_functions():
     return sorted(set(names))
 
 
+# The boundary as first listed for the operator: the two passes, their workspace queries
+# and the status strings (with the enum as its argument type).
+BOUNDARY = ("lora_delta_fwd", "lora_delta_bwd", "lora_delta_fwd_workspace", "lora_delta_bwd_workspace",
+            "lora_status_str")
+
+
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("lora_delta_fwd", "lora_delta_fwd_bf16", "lora_delta_bwd", "lora_delta_fwd_workspace_size",
-              "lora_delta_bwd_workspace_size",
-              "lora_status_str", "lora_delta_device_status", "lora_delta_set_profile_events", "lora_delta_describe"):
+    for n in BOUNDARY + ("lora_delta_fwd_bf16", "lora_delta_fwd_workspace_size", "lora_delta_bwd_workspace_size",
+                         "lora_delta_device_status", "lora_delta_set_profile_events", "lora_delta_describe",
+                         "lora_delta_fwd_noalloc", "lora_delta_fwd_noalloc_status"):
         assert n in names, n
+    text = open(HEADER).read()
+    assert re.search(r"const char \*lora_status_str\(lora_status status\);", text)
+
+
+def test_boundary_workspace_queries_agree(lib):
+    for q in ("lora_delta_fwd_workspace", "lora_delta_bwd_workspace", "lora_delta_fwd_workspace_size",
+              "lora_delta_bwd_workspace_size"):
+        getattr(lib, q).argtypes = [ctypes.c_int64] * 4
+        getattr(lib, q).restype = ctypes.c_size_t
+    for shape in ((8192, 4096, 4096, 16), (300, 1032, 520, 40), (0, 128, 96, 8), (8, 100, 96, 8)):
+        assert lib.lora_delta_fwd_workspace(*shape) == lib.lora_delta_fwd_workspace_size(*shape)
+        assert lib.lora_delta_bwd_workspace(*shape) == lib.lora_delta_bwd_workspace_size(*shape)
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -35,7 +35,15 @@ def lib():
     f = lib.lora_delta_fwd_noalloc
     f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float] + [ctypes.c_int64] * 4 + [ctypes.c_void_p] * 3
     f.restype = ctypes.c_int
+    lib.lora_delta_fwd_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.lora_delta_fwd_noalloc_status.restype = ctypes.c_int
     return lib
+
+
+def _noalloc_status(lib):
+    code = ctypes.c_int(-1)
+    rc = lib.lora_delta_fwd_noalloc_status(ctypes.byref(code))
+    return rc, code.value
 
 
 def _noalloc_fwd(lib, X, A, B, alpha):
@@ -58,6 +66,7 @@ def test_noalloc_forward_matches_the_workspace_forward_twice_in_a_row(lib):
         d = w.generate(seed, only=("x", "a", "b"))
         X, A, B = (G.dev_bf16(d[k]) for k in ("x", "a", "b"))
         y_na, u_na = _noalloc_fwd(lib, X, A, B, w.shape.alpha)
+        assert _noalloc_status(lib) == (0, 0)   # no kernel of the call gave up on a wait
         y_ref, u_ref = ld.lora_delta_fwd(X, A, B, w.shape.alpha)
         torch.cuda.synchronize()
         G.assert_bitwise(f"{w.name} delta_y", G.host_f32(y_na), G.host_f32(y_ref))
