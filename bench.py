@@ -5,7 +5,7 @@ Qwen-14B step reimplementation ...", section "Finding 2"): M=8192 tokens,
 K=N=4096, R=16, alpha=2, BF16 inputs with FP32 accumulation; X ~ N(0,1),
 A ~ N(0,1/4096), B ~ N(0,1/16), dY ~ N(0,1e-2); seeded synthetic data.
 
-One step = lora_delta_fwd + lora_delta_bwd through the C ABI (6 kernels),
+One step = lora_delta_fwd + lora_delta_bwd through the C ABI (8 kernels),
 called eagerly every step (no CUDA graph, no events inside the timed region).
 Metric: algorithmic HBM bytes of the step / step time (GB/s); ms per step and
 the fraction of the measured HBM copy peak are reported beside it. After the
@@ -38,8 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
-KERNELS = ["down U", "up dY_lora", "dy dU+dB", "up dX", "wgrad dA", "combine dA+dB"]
-N_FWD = 2      # forward kernels; the rest are the backward's
+KERNELS = ["down U", "rows U", "up dY_lora", "dy dU+dB", "rows dU", "up dX", "wgrad dA", "combine dA+dB"]
+N_FWD = 3      # forward kernels; the rest are the backward's
 N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
 HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal (context beside the measured copy peak)
 GRAPH_STEPS = 48   # steps captured in the CUDA graph of the untimed graph pass
@@ -49,17 +49,20 @@ PROF_STEPS = 16    # steps of the untimed per-kernel event pass
 def algorithmic_bytes(M, K, N, R):
     """Minimum bytes each step of the operator must move (each streamed operand
     read once per consuming kernel, each output written once, small operands
-    counted once; dY is read once for both dU and dB). The U and dU combines
-    run inside the up kernels; the final combine of the dA/dB chunk partials
-    adds no algorithmic bytes."""
+    counted once; dY is read once for both dU and dB), split by the kernel that
+    moves them. The rows kernels write U and dU; the slice and chunk partial
+    sums they and the final combine read are scratch (L2), not algorithmic
+    bytes."""
     bf, f4 = 2, 4
     return {
-        "down U": M * K * bf + R * K * bf + M * R * bf,             # X, A -> U
+        "down U": M * K * bf + R * K * bf,                          # X, A -> U partials
+        "rows U": M * R * bf,                                       # -> U
         "up dY_lora": M * R * bf + N * R * bf + M * N * f4,         # U, B -> dY_lora
-        "dy dU+dB": M * N * bf + N * R * bf + M * R * bf            # dY (read once), B, U -> dU, dB
-                    + M * R * bf + N * R * f4,
+        "dy dU+dB": M * N * bf + N * R * bf + M * R * bf            # dY (read once), B, U -> dU, dB partials
+                    + N * R * f4,                                   # (dB written by the combine)
+        "rows dU": M * R * bf,                                      # -> dU
         "up dX": M * R * bf + R * K * bf + M * K * f4,              # dU, A -> dX
-        "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA
+        "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA partials (dA written by the combine)
         "combine dA+dB": 0,
     }
 
@@ -303,7 +306,7 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
         ms = e0.elapsed_time(e1) / (reps * steps)
         nbytes = M * K * bf + R * K * bf + 2 * M * R * bf + N * R * bf + M * N * ysz
         out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                     "launches_per_step": 2}
+                     "launches_per_step": 3}
         assert ld.lora_delta_device_status(wf) == 0
     return out
 
@@ -351,7 +354,7 @@ def bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
         nbytes = M * N * dsz + N * R * bf + M * R * bf + M * K * bf + R * K * bf + M * K * f4 + 2 * M * R * bf \
             + R * K * f4 + N * R * f4
         out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                     "launches_per_step": 4 if dsz == bf else 5}
+                     "launches_per_step": 5 if dsz == bf else 6}
         assert ld.lora_delta_device_status(wb) == 0
     return out
 
@@ -451,7 +454,7 @@ def decode_variants(ld, dev, steps=50, reps=20, copies=8):
         ms = graph_ms(fwd)
         nbytes = M * K * bf + R * K * bf + 2 * M * R * bf + N * R * bf + M * N * f4
         out[f"decode_fwd_M{M}"] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes,
-                                   "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 2}
+                                   "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 3}
         assert ld.lora_delta_device_status(wf) == 0
         if M == 64:
             DYs = [rnd(M, N) for _ in range(copies)]
@@ -470,7 +473,7 @@ def decode_variants(ld, dev, steps=50, reps=20, copies=8):
             nbytes = M * N * bf + N * R * bf + M * R * bf + M * K * bf + R * K * bf + M * K * f4 + 2 * M * R * bf \
                 + R * K * f4 + N * R * f4
             out["decode_bwd_M64"] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes,
-                                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 5}
+                                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 6}
             assert ld.lora_delta_device_status(wb) == 0
     return out
 
@@ -520,7 +523,7 @@ def grouped_variants(ld, dev, peak, steps=10, reps=20):
 
     out = {}
     nbytes = sum(sum(algorithmic_bytes(M, s["x"].shape[1], s["b"].shape[0], R).values()) for s in sites)
-    for name, fn, launches in (("mlp_fc1_fc2_separate", separate, 2 * (2 + 4)), ("mlp_fc1_fc2_grouped", grouped, 2 + 4)):
+    for name, fn, launches in (("mlp_fc1_fc2_separate", separate, 2 * (3 + 5)), ("mlp_fc1_fc2_grouped", grouped, 3 + 5)):
         for _ in range(3):
             fn(torch.cuda.current_stream(dev))
         torch.cuda.synchronize()

@@ -266,9 +266,11 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   DownArgs dargs{};
+  RowsArgs rargs{};
   UpArgs uargs{};
-  dargs.n = uargs.n = m;
-  uargs.R = int(R);
+  dargs.n = rargs.n = uargs.n = m;
+  rargs.R = uargs.R = int(R);
+  rargs.RP = RP;
   size_t off = kStatusBytes;
   int64_t n_down = 0, n_up = 0;
   for (int j = 0; j < m; ++j) {
@@ -279,6 +281,7 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
     UpSite& q = uargs.s[j];
     if (!make_map(&d.in, p.x, false, p.M, p.K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&d.w, p.a, false, R, p.K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&q.a, p.u, false, p.M, R, RP, 128, swizzle_for_span(span)) ||
         !make_map(&q.b, p.b, false, p.N, R, RP, up_bn(RP), swizzle_for_span(span)) ||
         !(y_bf16 ? make_map(&q.out, p.delta_y, false, p.M, p.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)
                  : make_map(&q.out, p.delta_y, true, p.M, p.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
@@ -287,9 +290,7 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
     d.M = int(p.M);
     d.Kred = int(p.K);
     d.alpha = 1.0f;
-    q.part = upart;
-    q.out_bf16 = static_cast<__nv_bfloat16*>(p.u);
-    q.S = int(ceil_div(p.K, down_slice(RP)));
+    rargs.s[j] = RowsSite{upart, static_cast<__nv_bfloat16*>(p.u), int(p.M), int(ceil_div(p.K, down_slice(RP))), 0};
     q.M = int(p.M);
     q.Nout = int(p.N);
     q.alpha = p.alpha;
@@ -300,7 +301,9 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   rec.mark();
   if (launch_down(RP, false, dargs, status, grid_for(n_down, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
-  // U = bf16(tree over the K-slice partials), built inside the up-projection, which also writes u
+  // U = bf16(tree over the K-slice partials), written to u
+  if (launch_rows(rargs, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
+  rec.mark();
   if (launch_up(RP, false, y_bf16, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   return LORA_OK;
@@ -325,9 +328,11 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   DownArgs dargs{};
   WgArgs bargs{}, aargs{};
   UpArgs uargs{};
+  RowsArgs rargs{};
   CombineJobs jobs{};
-  yargs.n = dargs.n = bargs.n = aargs.n = uargs.n = m;
-  uargs.R = int(R);
+  yargs.n = dargs.n = bargs.n = aargs.n = uargs.n = rargs.n = m;
+  uargs.R = rargs.R = int(R);
+  rargs.RP = RP;
   jobs.n = 2 * m;
   size_t off = kStatusBytes;
   int64_t n_dy = 0, n_du = 0, n_db = 0, n_up = 0, n_da = 0;
@@ -342,7 +347,8 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     const int C = int(ceil_div(p.M, kWgradChunk));
     UpSite& q = uargs.s[j];
     WgSite& wa = aargs.s[j];
-    if (!make_map(&q.b, p.a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_map(&q.a, p.du, false, M, R, RP, 128, swizzle_for_span(span)) ||
+        !make_map(&q.b, p.a, false, R, K, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&q.out, p.dx, true, M, K, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&wa.in, p.x, false, M, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&wa.g, p.du, false, M, R, RP, 64, swizzle_for_span(span)))
@@ -378,9 +384,7 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
       n_du += down_units(M, N, RP);
       n_db += wgrad_units(M, N, RP);
     }
-    q.part = dupart;
-    q.out_bf16 = static_cast<__nv_bfloat16*>(p.du);
-    q.S = int(ceil_div(N, du_slice(RP)));
+    rargs.s[j] = RowsSite{dupart, static_cast<__nv_bfloat16*>(p.du), M, int(ceil_div(N, du_slice(RP))), 0};
     q.M = M;
     q.Nout = K;
     q.alpha = 1.0f;
@@ -407,7 +411,9 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     if (launch_wgrad(RP, true, bargs, status, grid_for(n_db, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
   }
-  // dU = bf16(tree over the N-slice partials), built inside the dX expansion, which also writes du
+  // dU = bf16(tree over the N-slice partials), written to du
+  if (launch_rows(rargs, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
+  rec.mark();
   if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;

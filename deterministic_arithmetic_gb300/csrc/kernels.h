@@ -64,12 +64,10 @@ struct DownSite {
 };
 using DownArgs = Sites<DownSite, kMaxSites>;
 
-// Up-projection (dY_lora, or dX) with the U / dU combine folded in.
+// Up-projection (dY_lora, or dX) from the finished u / du rows.
 struct UpSite {
-  CUtensorMap b, out;      // weight (B rows or A columns), output
-  const float* part;       // [S][M][RP] slice partials of u / du
-  __nv_bfloat16* out_bf16; // u / du [M][R], written here
-  int S, M, Nout, n_mt, n_nt, u0;
+  CUtensorMap a, b, out;   // u / du rows (box 128 x RP), weight (B rows or A columns), output
+  int M, Nout, n_mt, n_nt, u0;
   float alpha;             // forward scale (1 for dX)
 };
 using UpArgs = Sites<UpSite, kMaxSites>;
@@ -120,14 +118,30 @@ inline int64_t wgrad_units(int64_t M, int64_t C, int RP) { (void)RP; return ceil
 // word; `grid` the number of persistent CTAs.
 // args: sites filled in except n_mt, n_sl, u0 and total (set here)
 cudaError_t launch_down(int RP, bool dv, DownArgs& args, uint32_t* status, int grid, cudaStream_t st);
-// up: the u / du rows are formed by the kernel itself from the slice partials (and written to
-// out_bf16); y_bf16 (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte
+// up: a = u / du rows (box 128 x RP), complete when the launch starts (written by the preceding
+// rows kernel); y_bf16 (forward only): `out` is a BF16 dY_lora map with 32 x 32 boxes, 64-byte
 // swizzle. args: sites filled in except n_mt, n_nt, u0 and total (set here).
 cudaError_t launch_up(int RP, bool dx, bool y_bf16, UpArgs& args, uint32_t* status, int grid, cudaStream_t st);
 // args: sites filled in except n_sl, n_ch, u0 and total (set here)
 cudaError_t launch_dy(DyArgs& args, uint32_t* status, int grid, cudaStream_t st);
 // args: sites filled in except n_ct, n_ch, u0 and total (set here)
 cudaError_t launch_wgrad(int RP, bool dv, WgArgs& args, uint32_t* status, int grid, cudaStream_t st);
+
+// The BF16 rows of U (or dU) from the slice partials of the down (or dy) kernel: for every row
+// and every group of 8 columns, the canonical pairwise tree over the S slice partials, rounded
+// to BF16. One thread per group of 8 values, all sites of a call in one launch.
+struct RowsSite {
+  const float* part;       // [S][M][RP]
+  __nv_bfloat16* out;      // [M][R]
+  int M, S;
+  int64_t item0;           // first item of this site (M * R / 8 items per site)
+};
+struct RowsArgs {
+  RowsSite s[kMaxSites];
+  int64_t total;
+  int n, R, RP;
+};
+cudaError_t launch_rows(RowsArgs& args, int nsm, cudaStream_t st);
 
 // Final combine of the weight-gradient chunk partials: canonical tree over
 // the C chunks, FP32 out. part is [C][RP][cols] (cols = K for dA, N for dB).

@@ -1,23 +1,14 @@
-// up.cu -- the rank-R expansions (write-bound), each with the combine of its
-// BF16 operand folded in:
-//   forward : U = bf16(tree over K-slices of the U partials)          (written to u)
-//             dY_lora[m][n] = fp32(sum_r u[m][r] * b[n][r]) * alpha    ("(U @ B^T) * alpha")
-//   backward: dU = bf16(tree over N-slices of the dU partials)         (written to du)
-//             dX[m][k] = fp32(sum_r du[m][r] * a[r][k])                ("dX = dU @ A")
+// up.cu -- the rank-R expansions (write-bound):
+//   forward : dY_lora[m][n] = fp32(sum_r u[m][r] * b[n][r]) * alpha    ("(U @ B^T) * alpha")
+//   backward: dX[m][k] = fp32(sum_r du[m][r] * a[r][k])                ("dX = dU @ A")
 // (page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA + Triton, both
 // batch-invariant", section "Summary"; the alpha scale is fused into the
 // epilogue, as that page's "Benchmark" section proposes.)
 //
-// The u / du rows are the canonical pairwise tree (FP32, round to nearest)
-// over the slice partials left by the preceding kernel, rounded to BF16: a
-// pure function of partials that are complete when this kernel starts (stream
-// order), so every CTA forms the rows of its own units itself, straight into
-// each unit's operand stage, and no CTA ever waits for another (no grid
-// barrier, a plain launch). The epilogue warps form the rows of the CTA's
-// first two units (all 256 threads at once, so the first stores start early);
-// two row warps form those of the later units, each as soon as its stage is
-// free. The unit in column tile 0 of a row tile also writes those rows to u /
-// du (each row exactly once). Work unit = (128-row tile, BN-column tile), BN = 256 /
+// The u / du rows are complete when the kernel starts: the preceding down (or
+// dy) kernel forms each 128-row tile's BF16 rows as soon as the tile's last
+// slice partial is written. So no CTA waits for another (no grid barrier, a
+// plain launch). Work unit = (128-row tile, BN-column tile), BN = 256 /
 // (RP / 16), units dealt out round-robin, so that at any time the CTAs write
 // one compact band of the output (consecutive units are neighbours in
 // memory), which the memory system absorbs markedly faster than each CTA
@@ -33,9 +24,8 @@
 // FP32 value rounded once more (round to nearest even), half the bytes. Each
 // 32-column box is then 32 rows x 64 bytes (64-byte swizzle).
 //
-// Warp roles: 0 = TMA producer (B / A weight tile), 1 = MMA issuer (TMEM
-// owner), 2..9 = epilogue (and the rows of the first two units), 10..11 = row
-// warps (u / du rows of the later units).
+// Warp roles: 0 = TMA producer (u / du rows, B / A weight tile), 1 = MMA
+// issuer (TMEM owner), 2..9 = epilogue.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,11 +43,8 @@ struct UpCfg {
   static constexpr int kStages = RP == 16 ? 6 : (RP == 32 ? 5 : 3);   // operand ring (weight tile from L2)
   static constexpr int kBufCols = kLeaves * kBN;       // 256 TMEM columns per buffer
   static constexpr int kBufs = 512 / kBufCols;
-  static constexpr int kEpiWarps = 8, kRowWarps = 2;
-  static constexpr int kLocal = 2;                     // units whose u / du rows the epilogue warps form
-  static_assert(kLocal * kBM * (RP / 8) % (32 * kEpiWarps) == 0, "whole items per epilogue thread");
-  static_assert(kLocal <= kStages, "locally formed rows sit in the first stages");
-  static constexpr int kThreads = 32 * (2 + kEpiWarps + kRowWarps);
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kHalfCols = kBN / 2;
   static constexpr int kChunk = 32;                    // FP32 columns per TMA store box (128 bytes)
   static constexpr int kChunks = kHalfCols / kChunk;
@@ -68,7 +55,7 @@ struct UpCfg {
   static constexpr int kStgBytes = 32 * kChunk * 4;    // one 32-row x 32-column FP32 box: 4 KB
   static constexpr size_t kStgOff = size_t(kStages) * kStageBytes;
   static constexpr size_t kBarOff = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
-  static constexpr int kNumBars = 3 * kStages + 2 * kBufs + 3;
+  static constexpr int kNumBars = 2 * kStages + 2 * kBufs + 2;
   static constexpr size_t kSmem = kBarOff + 1024 + kNumBars * 8 + 16;
   static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
@@ -87,7 +74,6 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     while (i + 1 < args.n && u >= args.s[i + 1].u0) ++i;
     return args.s[i];
   };
-  const int R = args.R;
   static_assert(!(DX && YBF), "BF16 output is the forward's");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -97,14 +83,12 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
   uint8_t* stg_ptr = gbase + C::kStgOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
   const uint32_t bar0 = smem_u32(bars);
-  auto full = [&](int s) { return bar0 + 8u * s; };                       // weight tile landed (TMA)
+  auto full = [&](int s) { return bar0 + 8u * s; };                       // rows and weight tile landed (TMA)
   auto empty = [&](int s) { return bar0 + 8u * (C::kStages + s); };        // stage free (MMA done)
-  auto rows = [&](int s) { return bar0 + 8u * (2 * C::kStages + s); };     // u / du rows in the stage (row warps)
-  auto tfull = [&](int b) { return bar0 + 8u * (3 * C::kStages + b); };
-  auto tempty = [&](int b) { return bar0 + 8u * (3 * C::kStages + C::kBufs + b); };
-  const uint32_t drain = bar0 + 8u * (3 * C::kStages + 2 * C::kBufs);
-  const uint32_t ufirst = drain + 8u;   // the first kLocal units' u / du rows are in their stages (epilogue)
-  const uint32_t never = drain + 16u;   // completed by nothing (the stall test hook waits on it)
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kBufs + b); };
+  const uint32_t drain = bar0 + 8u * (2 * C::kStages + 2 * C::kBufs);
+  const uint32_t never = drain + 8u;    // completed by nothing (the stall test hook waits on it)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -113,18 +97,17 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
-      mbar_init(rows(s), C::kRowWarps);
     }
     for (int b = 0; b < C::kBufs; ++b) {
       mbar_init(tfull(b), 1);
       mbar_init(tempty(b), C::kEpiWarps);
     }
     mbar_init(drain, 1);
-    mbar_init(ufirst, C::kEpiWarps);
     mbar_init(never, 1);
     *abort_flag = 0u;
     mbar_fence_init();
     for (int i = 0; i < (GR ? args.n : 1); ++i) {
+      prefetch_map(&args.s[i].a);
       prefetch_map(&args.s[i].b);
       prefetch_map(&args.s[i].out);
     }
@@ -152,10 +135,11 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       uint32_t issued = 0, parities = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const UpSite& P = site(u);
-        const int nt = (u - P.u0) % P.n_nt;
+        const int mt = (u - P.u0) / P.n_nt, nt = (u - P.u0) % P.n_nt;
         if (wait(empty(r.idx), r.phase ^ 1u, ab, 11)) {
           const uint32_t st = base + r.idx * C::kStageBytes;
-          mbar_expect_tx(full(r.idx), C::kBBytes);
+          mbar_expect_tx(full(r.idx), C::kStageBytes);
+          tma_load(st, &P.a, full(r.idx), 0, mt * C::kBM, pol);                     // u / du rows of the tile
           if (DX) {
 #pragma unroll
             for (int i = 0; i < C::kBN / 64; ++i)                                  // a[0..RP)[k..k+63]
@@ -178,8 +162,7 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       constexpr uint32_t lay = layout_for_span(C::kSpan);
       Ring r, b;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        bool ok = wait(full(r.idx), r.phase, ab, 13) && wait(rows(r.idx), r.phase, ab, 16);
-        if (u < int(blockIdx.x) + C::kLocal * int(gridDim.x)) ok = ok && wait(ufirst, 0u, ab, 18);
+        bool ok = wait(full(r.idx), r.phase, ab, 13);
         ok = ok && wait(tempty(b.idx), b.phase ^ 1u, ab, 14);
         if (ok) {
           tc_fence_after();
@@ -212,45 +195,6 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
     const uint32_t my_stg = stg0 + (warp - 2) * C::kStg * C::kStgBytes;
     const uint64_t pol_out = policy_evict_first();
     uint8_t* my_stg_ptr = stg_ptr + (warp - 2) * C::kStg * C::kStgBytes;
-    {
-      // the rows of u / du of this CTA's first kLocal units = bf16(tree over the S slice partials),
-      // straight into stages 0 .. kLocal-1 in the layout a TMA load of the rows would give (rows
-      // of RP * 2 bytes, 16-byte chunks swizzled by the row's place in the 8-row swizzle atom);
-      // all loads of a thread are issued before its first store. A unit in column tile 0 also
-      // writes its rows to u / du.
-      constexpr int kItems = C::kLocal * C::kBM * (RP / 8) / (32 * C::kEpiWarps);
-      uint4 v[kItems];
-#pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        const int i = int(threadIdx.x) - 64 + j * 32 * C::kEpiWarps;
-        const int k = i / (C::kBM * (RP / 8)), row = (i / (RP / 8)) % C::kBM, g = i % (RP / 8);
-        const int u = int(blockIdx.x) + k * int(gridDim.x);
-        v[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (u < total) {
-          const UpSite& P = site(u);
-          const int grow = ((u - P.u0) / P.n_nt) * C::kBM + row;
-          if (grow < P.M && g < R / 8)
-            v[j] = slices_to_bf16x8(P.part + size_t(grow) * RP + g * 8, size_t(P.M) * RP, P.S);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        const int i = int(threadIdx.x) - 64 + j * 32 * C::kEpiWarps;
-        const int k = i / (C::kBM * (RP / 8)), row = (i / (RP / 8)) % C::kBM, g = i % (RP / 8);
-        const uint32_t o = uint32_t(row * C::kSpan + g * 16);
-        *reinterpret_cast<uint4*>(gbase + size_t(k) * C::kStageBytes + (o ^ (((o >> 7) & uint32_t(C::kSpan / 16 - 1)) << 4))) = v[j];
-        const int u = int(blockIdx.x) + k * int(gridDim.x);
-        if (u < total) {
-          const UpSite& P = site(u);
-          const int grow = ((u - P.u0) / P.n_nt) * C::kBM + row;
-          if ((u - P.u0) % P.n_nt == 0 && grow < P.M && g < R / 8)
-            *reinterpret_cast<uint4*>(P.out_bf16 + size_t(grow) * R + g * 8) = v[j];
-        }
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ufirst);
-    }
     int sidx = 0;
     Ring b;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -344,36 +288,6 @@ __global__ void __launch_bounds__(UpCfg<RP, DX>::kThreads, 1)
       b.next<C::kBufs>();
     }
     if (lane == 0) tma_store_wait_all<0>();
-  } else {
-    // -------------------------------------------------------- row warps
-    // The u / du rows of this CTA's units from the kLocal-th on: bf16(tree over the S slice
-    // partials) into the unit's stage once the stage is free (the producer brings only the
-    // weight tile); a unit in column tile 0 also writes its rows to u / du.
-    const int t = threadIdx.x - 32 * (2 + C::kEpiWarps);
-    Ring r;
-    int k = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++k) {
-      if (k >= C::kLocal && wait(empty(r.idx), r.phase ^ 1u, ab, 19)) {
-        const UpSite& P = site(u);
-        const int mt = (u - P.u0) / P.n_nt, nt = (u - P.u0) % P.n_nt;
-        uint8_t* stage = gbase + size_t(r.idx) * C::kStageBytes;
-        for (int i = t; i < C::kBM * (RP / 8); i += 32 * C::kRowWarps) {
-          const int row = i / (RP / 8), g = i % (RP / 8);
-          const int grow = mt * C::kBM + row;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (grow < P.M && g < R / 8) {
-            v = slices_to_bf16x8(P.part + size_t(grow) * RP + g * 8, size_t(P.M) * RP, P.S);
-            if (nt == 0) *reinterpret_cast<uint4*>(P.out_bf16 + size_t(grow) * R + g * 8) = v;
-          }
-          const uint32_t o = uint32_t(row * C::kSpan + g * 16);
-          *reinterpret_cast<uint4*>(stage + (o ^ (((o >> 7) & uint32_t(C::kSpan / 16 - 1)) << 4))) = v;
-        }
-        fence_proxy_async();                 // generic writes, read by the tensor core
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(rows(r.idx));
-      r.next<C::kStages>();
-    }
   }
 
   tc_fence_before();

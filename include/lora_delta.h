@@ -90,8 +90,8 @@ typedef enum lora_status {
  *   delta_y  [M][N] fp32   out: (U @ B^T) * alpha
  *   u        [M][R] bf16   out: U = bf16(X @ A^T), saved for the backward pass
  *   workspace, workspace_bytes: >= lora_delta_fwd_workspace_size(M, K, N, R)
- * Kernels: down-projection (U partials over K-slices), up-projection (adds the
- * partials into U, writes u, expands to delta_y).
+ * Kernels: down-projection (U partials over K-slices), rows (adds the partials
+ * into U and writes u), up-projection (expands u to delta_y).
  */
 lora_status lora_delta_fwd(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K, int64_t N,
                            int64_t R, float *delta_y, void *u, void *workspace, size_t workspace_bytes, void *stream);
@@ -178,8 +178,8 @@ lora_status lora_delta_bwd_grouped(const lora_bwd_site *sites, int count, int64_
  *   workspace, workspace_bytes: >= lora_delta_bwd_workspace_size(M, K, N, R)
  * dA and dB reduce over all M rows in fixed 256-row chunks whose partials are
  * added by the canonical pairwise tree over the chunk index.
- * Kernels: dU partials, dB partials, dX (adds the dU partials, writes du),
- * dA partials, combine (dA, dB).
+ * Kernels: dU and dB partials (one pass over dY for R <= 16), rows (adds the
+ * dU partials into dU and writes du), dX, dA partials, combine (dA, dB).
  */
 lora_status lora_delta_bwd(const void *dy, const void *x, const void *a, const void *b, const void *u, float alpha,
                            int64_t M, int64_t K, int64_t N, int64_t R, float *dx, float *da, float *db, void *du,

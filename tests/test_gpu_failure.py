@@ -21,6 +21,7 @@ import gpu_util as G  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
+
 # (kernel kind, workspace holding the hook, rank, site of the stall wait)
 CASES = [
     (1, "fwd", 16, 9),    # down-projection, U partials
@@ -72,6 +73,7 @@ def test_a_wait_that_runs_out_is_reported_and_leaves_nothing_behind(kind, where,
     assert ld.lora_delta_device_status(hooked) == (site << 8) | 1
     assert ld.lora_delta_device_status(other) == 0
     assert int(hooked.view(torch.int32)[2].item()) == kind     # hook words are read, never written
+    assert not hooked[16:256].any().item()                      # nothing else in the block is written
     assert torch.ones(4, device="cuda").sum().item() == 4.0    # the context is still usable
 
     words[0] = 0             # the caller reads and clears the code ...
@@ -83,9 +85,9 @@ def test_a_wait_that_runs_out_is_reported_and_leaves_nothing_behind(kind, where,
         G.assert_bitwise(k, got[k].view(torch.uint8).cpu().numpy(), ref[k].view(torch.uint8).cpu().numpy())
 
 
-def test_status_block_words_beyond_the_code_stay_untouched():
-    """The kernels write word 0 only, and only on a timeout: after normal calls the whole
-    256-byte block is still zero (no barrier counters or other state live there)."""
+def test_status_block_is_zero_after_every_call():
+    """The kernels write status word 0 only, and only on a timeout: after normal calls of several
+    shapes the whole 256-byte status block is still zero (no state is carried between calls)."""
     from deterministic_arithmetic_gb300 import lora_delta as ld
 
     M, K, N, R = 1000, 512, 1024, 16
@@ -93,7 +95,8 @@ def test_status_block_words_beyond_the_code_stay_untouched():
     t = {k: G.dev_bf16(v) for k, v in w.generate(1).items()}
     wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), "cuda")
     wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), "cuda")
-    for _ in range(3):
-        _step(t, 2.0, wf, wb)
-    assert not wf[:256].any().item() and not wb[:256].any().item()
+    for m in (M, 1, 129, M):
+        tm = dict(t, x=t["x"][:m], dy=t["dy"][:m])
+        _step(tm, 2.0, wf, wb)
+        assert not wf[:256].any().item() and not wb[:256].any().item(), m
     assert np.array_equal(wf[:256].cpu().numpy(), np.zeros(256, np.uint8))
