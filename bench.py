@@ -38,8 +38,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
-KERNELS = ["down U", "rows U", "up dY_lora", "dy dU+dB", "rows dU", "up dX", "wgrad dA", "combine dA+dB"]
-N_FWD = 3      # forward kernels; the rest are the backward's
+# kernels of one step: the forward's three launches, the backward's five (R <= 16)
+KERNELS_FWD = ["down U", "rows U", "up dY_lora"]
+KERNELS_BWD = ["dy dU+dB", "rows dU", "up dX", "wgrad dA", "combine dA+dB"]
+KERNELS = KERNELS_FWD + KERNELS_BWD
+N_FWD = len(KERNELS_FWD)
+FUSED_FWD = "fwd down+rows+up"   # lora_delta_fwd_fused: the same three steps in one launch
 N_ROTATE = 3   # physical copies of the streamed inputs (X, dY), rotated step to step
 HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal (context beside the measured copy peak)
 GRAPH_STEPS = 48   # steps captured in the CUDA graph of the untimed graph pass
@@ -54,10 +58,14 @@ def algorithmic_bytes(M, K, N, R):
     sums they and the final combine read are scratch (L2), not algorithmic
     bytes."""
     bf, f4 = 2, 4
-    return {
+    fwd = {
         "down U": M * K * bf + R * K * bf,                          # X, A -> U partials
         "rows U": M * R * bf,                                       # -> U
         "up dY_lora": M * R * bf + N * R * bf + M * N * f4,         # U, B -> dY_lora
+    }
+    return {
+        "fwd down+rows+up": sum(fwd.values()),                      # the single-launch forward
+        **fwd,
         "dy dU+dB": M * N * bf + N * R * bf + M * R * bf            # dY (read once), B, U -> dU, dB partials
                     + N * R * f4,                                   # (dB written by the combine)
         "rows dU": M * R * bf,                                      # -> dU
@@ -65,6 +73,12 @@ def algorithmic_bytes(M, K, N, R):
         "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA partials (dA written by the combine)
         "combine dA+dB": 0,
     }
+
+
+def step_bytes(M, K, N, R):
+    """Algorithmic bytes of one forward + backward step (the kernels of KERNELS)."""
+    alg = algorithmic_bytes(M, K, N, R)
+    return sum(alg[k] for k in KERNELS)
 
 
 def measured_peaks():
@@ -77,22 +91,19 @@ def measured_peaks():
 
 
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by kernel, with the hash of the kernel source
-# the counters were taken on; a kernel changed since then reports null.
-NCU_TRAFFIC = {   # ncu, training step, warm caches (--cache-control none), per launch
-    "down U": {"bytes": 71610000, "src_hash": "2a4b5ad0158cc814"},
-    "up dY_lora": {"bytes": 124820000, "src_hash": "094f138f10a9f88e"},
-    "dy dU+dB": {"bytes": 79910000, "src_hash": "7971a7838ffbc72d"},
-    "up dX": {"bytes": 126770000, "src_hash": "094f138f10a9f88e"},
-    "wgrad dA": {"bytes": 76030000, "src_hash": "086a1ed9dabedcad"},
-    "combine dA+dB": {"bytes": 1040000, "src_hash": "b45fe2f879bdf9ea"},
-}
+# dram__bytes_write.sum), keyed by kernel, with the hash of the kernel sources
+# the counters were taken on (every file under csrc/); after any change to the
+# sources the line reports null until the counters are taken again.
+NCU_TRAFFIC = {}
 
 
-def source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "deterministic_arithmetic_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "deterministic_arithmetic_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
 
 
 class ClockSampler:
@@ -249,7 +260,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     shape = S.train().shape
-    total_bytes = sum(algorithmic_bytes(shape.M, shape.K, shape.N, shape.R).values())
+    total_bytes = step_bytes(shape.M, shape.K, shape.N, shape.R)
     probe = OracleSample(shape, 64)
     per_row = probe.seconds_full() / shape.M
     rows = int(min(shape.M, max(16, args.reference_budget_s / max(1, args.steps + args.warmup) / per_row)))
@@ -272,19 +283,23 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
-    """Forward only, FP32 dY_lora against the BF16 output variant: CUDA-graph
-    timed like the main step (inputs rotated over the same copies of X)."""
+def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, peak, steps=40, reps=25):
+    """Forward only: FP32 dY_lora against the BF16 output variant, and the single-launch forward
+    (lora_delta_fwd_fused) against the three launches of lora_delta_fwd; CUDA-graph timed like
+    the main step (inputs rotated over the same copies of X). The single launch is also timed
+    alone with CUDA events (its roofline fraction as one kernel)."""
     import torch
 
     out = {}
     bf, f4 = 2, 4
-    for name, ydt, ysz in (("fwd_fp32_dy", torch.float32, f4), ("fwd_bf16_dy", torch.bfloat16, bf)):
+    for name, ydt, ysz in (("fwd_fp32_dy", torch.float32, f4), ("fwd_bf16_dy", torch.bfloat16, bf),
+                           ("fwd_fused_fp32_dy", torch.float32, f4)):
+        call = ld.lora_delta_fwd_fused if "fused" in name else ld.lora_delta_fwd
         Y = torch.empty((M, N), dtype=ydt, device=dev)
         U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
         wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
         for i in range(5):
-            ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf)
+            call(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
@@ -293,7 +308,7 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
             with torch.cuda.graph(graph, stream=cap):
                 gst = torch.cuda.current_stream(dev)
                 for i in range(steps):
-                    ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=gst)
+                    call(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=gst)
         torch.cuda.current_stream(dev).wait_stream(cap)
         graph.replay()
         torch.cuda.synchronize()
@@ -306,7 +321,17 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
         ms = e0.elapsed_time(e1) / (reps * steps)
         nbytes = M * K * bf + R * K * bf + 2 * M * R * bf + N * R * bf + M * N * ysz
         out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                     "launches_per_step": 3}
+                     "launches_per_step": 1 if "fused" in name else 3}
+        if "fused" in name:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(8)]
+            for i in range(8):
+                ld.lora_delta_set_profile_events(ev[i])
+                call(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf)
+            ld.lora_delta_set_profile_events(None)
+            torch.cuda.synchronize()
+            k_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+            out[name]["kernel_event_ms"] = round(k_ms, 5)
+            out[name]["kernel_frac"] = round(nbytes / (k_ms * 1e-3) / 1e9 / peak, 4)
         assert ld.lora_delta_device_status(wf) == 0
     return out
 
@@ -451,10 +476,15 @@ def decode_variants(ld, dev, steps=50, reps=20, copies=8):
             j = i % copies
             ld.lora_delta_fwd(Xs[j], As[j], Bs[j], alpha, delta_y=Ys[j], u=Us[j], workspace=wf, stream=st)
 
-        ms = graph_ms(fwd)
+        def fwd_fused(i, st):
+            j = i % copies
+            ld.lora_delta_fwd_fused(Xs[j], As[j], Bs[j], alpha, delta_y=Ys[j], u=Us[j], workspace=wf, stream=st)
+
         nbytes = M * K * bf + R * K * bf + 2 * M * R * bf + N * R * bf + M * N * f4
-        out[f"decode_fwd_M{M}"] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes,
-                                   "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "launches_per_step": 3}
+        for label, fn, launches in ((f"decode_fwd_M{M}", fwd, 3), (f"decode_fwd_fused_M{M}", fwd_fused, 1)):
+            ms = graph_ms(fn)
+            out[label] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                          "launches_per_step": launches}
         assert ld.lora_delta_device_status(wf) == 0
         if M == 64:
             DYs = [rnd(M, N) for _ in range(copies)]
@@ -522,7 +552,7 @@ def grouped_variants(ld, dev, peak, steps=10, reps=20):
         ld.lora_delta_bwd_grouped(bw_sites, workspace=wbg, stream=st)
 
     out = {}
-    nbytes = sum(sum(algorithmic_bytes(M, s["x"].shape[1], s["b"].shape[0], R).values()) for s in sites)
+    nbytes = sum(step_bytes(M, s["x"].shape[1], s["b"].shape[0], R) for s in sites)
     for name, fn, launches in (("mlp_fc1_fc2_separate", separate, 2 * (3 + 5)), ("mlp_fc1_fc2_grouped", grouped, 3 + 5)):
         for _ in range(3):
             fn(torch.cuda.current_stream(dev))
@@ -559,12 +589,13 @@ def grouped_variants(ld, dev, peak, steps=10, reps=20):
               ("mlp_fc1_fc2_grouped", lambda i: ld.lora_delta_fwd_grouped(fw_sites, workspace=wfg, stream=stream),
                lambda i: ld.lora_delta_bwd_grouped(bw_sites, workspace=wbg, stream=stream), sites))
     for label, f, b, ss in passes:
-        kavg = kernel_event_pass(ld, KERNELS, N_FWD, 8, stream, f, b)
-        alg = {k: sum(algorithmic_bytes(M, s["x"].shape[1], s["b"].shape[0], R)[k] for s in ss) for k in KERNELS}
+        names = KERNELS
+        kavg = kernel_event_pass(ld, names, N_FWD, 8, stream, f, b)
+        alg = {k: sum(algorithmic_bytes(M, s["x"].shape[1], s["b"].shape[0], R)[k] for s in ss) for k in names}
         kern = {k: {"ms": round(kavg[k], 5), "algorithmic_bytes": alg[k],
                     "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
-                    "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None} for k in KERNELS}
-        worst = min((k for k in KERNELS if alg[k]), key=lambda k: kern[k]["frac"])
+                    "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None} for k in names}
+        worst = min((k for k in names if alg[k]), key=lambda k: kern[k]["frac"])
         out.setdefault(label, {}).update({"kernels": kern, "worst_kernel": worst,
                                           "kernels_note": "untimed pass of 8 steps with a CUDA event between kernels"})
     for s in sites:
@@ -671,19 +702,18 @@ def run_ours(args, world, rank, local):
                              lambda i: ld.lora_delta_bwd(DYs[i % N_ROTATE], Xs[i % N_ROTATE], A, B, U, alpha, dx=DX,
                                                          da=DA, db=DB, du=DU, workspace=wb, stream=stream))
     alg = algorithmic_bytes(M, K, N, R)
-    total_bytes = sum(alg.values())
+    total_bytes = step_bytes(M, K, N, R)
     peak, peak_kind = measured_peaks()
     value = total_bytes * world / (ms_step * 1e-3) / 1e9
     dominant = max(kavg, key=lambda k: kavg[k])
     achieved = alg[dominant] / (kavg[dominant] * 1e-3) / 1e9
-    src = dominant.split()[0] + ".cu"                   # down.cu, up.cu, dy.cu, wgrad.cu, combine.cu
     tr = NCU_TRAFFIC.get(dominant)
-    traffic = tr["bytes"] if tr and tr.get("src_hash") == source_hash(src) else None
+    traffic = tr["bytes"] if tr and tr.get("src_hash") == source_hash() else None
 
     # ---------------------------------------- forward variants (FP32 / BF16 dY_lora)
     variants = None
     if not args.no_variants:
-        variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev)
+        variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, measured_peaks()[0])
         variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(grouped_variants(ld, dev, measured_peaks()[0]))
         variants.update(exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))

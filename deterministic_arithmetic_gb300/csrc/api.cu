@@ -19,6 +19,11 @@ using namespace lora;
 namespace {
 
 constexpr size_t kStatusBytes = 256;
+// Control block: the status block, then control words (the fused forward's tickets and row-tile
+// words), zero before a workspace's first use and zero again after every call.
+constexpr size_t kControlBytes = kStatusBytes + 65536;
+static_assert(kControlBytes == LORA_DELTA_CONTROL_BYTES, "control block size of the public header");
+static_assert(kFusedCtlWords * 4 <= 65536, "control words fit the control block");
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -50,7 +55,7 @@ lora_status device_ready(int* num_sms) {
     d.usable = (major == 10 && minor == 3);
     if (d.usable) {
       if (prepare_down() != cudaSuccess || prepare_up() != cudaSuccess || prepare_wgrad() != cudaSuccess ||
-          prepare_dy() != cudaSuccess || prepare_exact() != cudaSuccess) {
+          prepare_dy() != cudaSuccess || prepare_exact() != cudaSuccess || prepare_fwd_fused() != cudaSuccess) {
         d.probed = false;
         return LORA_ERR_CUDA;
       }
@@ -101,29 +106,31 @@ lora_status check_shape(int64_t M, int64_t K, int64_t N, int64_t R) {
 
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Scratch of one site (offsets from the start of the site's region; a call's workspace is the
+// control block, then the regions of its sites in site order).
 struct FwdLayout {
-  size_t upart, total;
+  size_t upart, bytes;     // U slice partials [S][M][RP]; region size
 };
 FwdLayout fwd_layout(int64_t M, int64_t K, int64_t R) {
   const int RP = padded_rank(int(R));
   const size_t S = size_t(ceil_div(K, down_slice(RP)));
   FwdLayout l;
-  l.upart = kStatusBytes;
-  l.total = l.upart + round256(S * size_t(M) * RP * 4);
+  l.upart = 0;
+  l.bytes = round256(S * size_t(M) * RP * 4);
   return l;
 }
 struct BwdLayout {
-  size_t dupart, dbpart, dapart, total;
+  size_t dupart, dbpart, dapart, bytes;   // dU slice partials, dB and dA chunk partials; region size
 };
 BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int64_t R) {
   const int RP = padded_rank(int(R));
   const size_t S = size_t(ceil_div(N, du_slice(RP)));
   const size_t C = size_t(ceil_div(M, kWgradChunk));
   BwdLayout l;
-  l.dupart = kStatusBytes;
+  l.dupart = 0;
   l.dbpart = l.dupart + round256(S * size_t(M) * RP * 4);
   l.dapart = l.dbpart + round256(C * RP * size_t(N) * 4);
-  l.total = l.dapart + round256(C * RP * size_t(K) * 4);
+  l.bytes = l.dapart + round256(C * RP * size_t(K) * 4);
   return l;
 }
 
@@ -160,12 +167,12 @@ const char* lora_status_str(lora_status s) {
 
 size_t lora_delta_fwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
   if (check_shape(M, K, N, R) != LORA_OK) return 0;
-  return fwd_layout(M, K, R).total;
+  return kControlBytes + fwd_layout(M, K, R).bytes;
 }
 
 size_t lora_delta_bwd_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
   if (check_shape(M, K, N, R) != LORA_OK) return 0;
-  return bwd_layout(M, K, N, R).total;
+  return kControlBytes + bwd_layout(M, K, N, R).bytes;
 }
 
 size_t lora_delta_fwd_workspace(int64_t M, int64_t K, int64_t N, int64_t R) {
@@ -197,11 +204,8 @@ struct BwdIn {
   void* du;
 };
 
-// Workspace: the 256-byte status block, then each site's partial-sum regions in site order.
-size_t fwd_site_bytes(int64_t M, int64_t K, int64_t R) { return fwd_layout(M, K, R).total - kStatusBytes; }
-size_t bwd_site_bytes(int64_t M, int64_t K, int64_t N, int64_t R) {
-  return bwd_layout(M, K, N, R).total - kStatusBytes;
-}
+size_t fwd_site_bytes(int64_t M, int64_t K, int64_t R) { return fwd_layout(M, K, R).bytes; }
+size_t bwd_site_bytes(int64_t M, int64_t K, int64_t N, int64_t R) { return bwd_layout(M, K, N, R).bytes; }
 
 // Shared checks, in the order the single-site entry points document: shapes, NULL pointers,
 // alignment, workspace size. *active = sites with M > 0 (indices), *need = workspace bytes.
@@ -238,21 +242,23 @@ struct BwdPtrs {
 };
 
 size_t fwd_need(const FwdIn* in, int n, int64_t R) {
-  size_t t = kStatusBytes;
+  size_t t = kControlBytes;
   for (int i = 0; i < n; ++i)
     if (in[i].M > 0) t += fwd_site_bytes(in[i].M, in[i].K, R);
   return t;
 }
 size_t bwd_need(const BwdIn* in, int n, int64_t R) {
-  size_t t = kStatusBytes;
+  size_t t = kControlBytes;
   for (int i = 0; i < n; ++i)
     if (in[i].M > 0) t += bwd_site_bytes(in[i].M, in[i].K, in[i].N, R);
   return t;
 }
 
-// The forward of every site in two launches (down over all sites' units, then up).
+// The forward of every site: three launches over all sites' units (down, rows, up), or, with
+// `fused` (one site, batches of up to kFusedMaxTiles row tiles), one launch doing the same
+// three steps. Both give the same bits.
 lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      void* stream, bool fused = false) {
   int active[kMaxSites], m = 0;
   lora_status s = check_sites(in, n, R, workspace, workspace_bytes, FwdPtrs{}, active, &m);
   if (s != LORA_OK || m == 0) return s;
@@ -271,12 +277,13 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   dargs.n = rargs.n = uargs.n = m;
   rargs.R = uargs.R = int(R);
   rargs.RP = RP;
-  size_t off = kStatusBytes;
+  size_t off = kControlBytes;
   int64_t n_down = 0, n_up = 0;
   for (int j = 0; j < m; ++j) {
     const FwdIn& p = in[active[j]];
-    float* upart = reinterpret_cast<float*>(ws + off);
-    off += fwd_site_bytes(p.M, p.K, R);
+    const FwdLayout L = fwd_layout(p.M, p.K, R);
+    float* upart = reinterpret_cast<float*>(ws + off + L.upart);
+    off += L.bytes;
     DownSite& d = dargs.s[j];
     UpSite& q = uargs.s[j];
     if (!make_map(&d.in, p.x, false, p.M, p.K, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
@@ -297,8 +304,17 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
     n_down += down_units(p.M, p.K, RP);
     n_up += up_units(p.M, p.N, RP);
   }
+  if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
+  if (fused && m == 1 && ceil_div(in[active[0]].M, 128) <= kFusedMaxTiles) {
+    uint32_t* ctl = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+    if (launch_fwd_fused(RP, y_bf16, dargs, uargs, static_cast<__nv_bfloat16*>(in[active[0]].u), int(R), ctl, nsm,
+                         status, st) != cudaSuccess)
+      return LORA_ERR_CUDA;
+    rec.mark();
+    return LORA_OK;
+  }
   if (launch_down(RP, false, dargs, status, grid_for(n_down, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   // U = bf16(tree over the K-slice partials), written to u
@@ -334,15 +350,15 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   uargs.R = rargs.R = int(R);
   rargs.RP = RP;
   jobs.n = 2 * m;
-  size_t off = kStatusBytes;
+  size_t off = kControlBytes;
   int64_t n_dy = 0, n_du = 0, n_db = 0, n_up = 0, n_da = 0;
   for (int j = 0; j < m; ++j) {
     const BwdIn& p = in[active[j]];
     const BwdLayout L = bwd_layout(p.M, p.K, p.N, R);
-    float* dupart = reinterpret_cast<float*>(ws + off + (L.dupart - kStatusBytes));
-    float* dbpart = reinterpret_cast<float*>(ws + off + (L.dbpart - kStatusBytes));
-    float* dapart = reinterpret_cast<float*>(ws + off + (L.dapart - kStatusBytes));
-    off += bwd_site_bytes(p.M, p.K, p.N, R);
+    float* dupart = reinterpret_cast<float*>(ws + off + L.dupart);
+    float* dbpart = reinterpret_cast<float*>(ws + off + L.dbpart);
+    float* dapart = reinterpret_cast<float*>(ws + off + L.dapart);
+    off += L.bytes;
     const int M = int(p.M), K = int(p.K), N = int(p.N);
     const int C = int(ceil_div(p.M, kWgradChunk));
     UpSite& q = uargs.s[j];
@@ -397,6 +413,7 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     n_up += up_units(M, K, RP);
     n_da += wgrad_units(M, K, RP);
   }
+  if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
   if (RP == 16) {
@@ -434,6 +451,13 @@ lora_status lora_delta_fwd(const void* x, const void* a, const void* b, float al
   return fwd_group(&in, 1, R, false, workspace, workspace_bytes, stream);
 }
 
+lora_status lora_delta_fwd_fused(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K,
+                                 int64_t N, int64_t R, void* delta_y, void* u, int y_bf16, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  const FwdIn in{x, a, b, alpha, M, K, N, delta_y, u};
+  return fwd_group(&in, 1, R, y_bf16 != 0, workspace, workspace_bytes, stream, true);
+}
+
 lora_status lora_delta_fwd_bf16(const void* x, const void* a, const void* b, float alpha, int64_t M, int64_t K,
                                 int64_t N, int64_t R, void* delta_y, void* u, void* workspace, size_t workspace_bytes,
                                 void* stream) {
@@ -450,7 +474,7 @@ lora_status lora_delta_bwd(const void* dy, const void* x, const void* a, const v
 
 size_t lora_delta_bwd_f32dy_workspace_size(int64_t M, int64_t K, int64_t N, int64_t R) {
   if (check_shape(M, K, N, R) != LORA_OK) return 0;
-  return bwd_layout(M, K, N, R).total + round256(size_t(M) * size_t(N) * 2);
+  return kControlBytes + bwd_layout(M, K, N, R).bytes + round256(size_t(M) * size_t(N) * 2);
 }
 
 lora_status lora_delta_bwd_f32dy(const float* dy, const void* x, const void* a, const void* b, const void* u,
@@ -464,7 +488,7 @@ lora_status lora_delta_bwd_f32dy(const float* dy, const void* x, const void* a, 
                         static_cast<const void*>(da), static_cast<const void*>(db), static_cast<const void*>(du),
                         static_cast<const void*>(workspace)})
     if (!aligned16(p)) return LORA_ERR_ALIGN;
-  const size_t bwd_bytes = bwd_layout(M, K, N, R).total;
+  const size_t bwd_bytes = kControlBytes + bwd_layout(M, K, N, R).bytes;
   if (workspace_bytes < lora_delta_bwd_f32dy_workspace_size(M, K, N, R)) return LORA_ERR_WORKSPACE;
   int nsm = 0;
   if ((s = device_ready(&nsm)) != LORA_OK) return s;
@@ -479,7 +503,7 @@ lora_status lora_delta_bwd_f32dy(const float* dy, const void* x, const void* a, 
 
 size_t lora_delta_fwd_grouped_workspace_size(const lora_fwd_site* sites, int count, int64_t R) {
   if (!sites || count < 1 || count > kMaxSites) return 0;
-  size_t t = kStatusBytes;
+  size_t t = kControlBytes;
   for (int i = 0; i < count; ++i) {
     if (check_shape(sites[i].M, sites[i].K, sites[i].N, R) != LORA_OK) return 0;
     t += fwd_site_bytes(sites[i].M, sites[i].K, R);
@@ -489,7 +513,7 @@ size_t lora_delta_fwd_grouped_workspace_size(const lora_fwd_site* sites, int cou
 
 size_t lora_delta_bwd_grouped_workspace_size(const lora_bwd_site* sites, int count, int64_t R) {
   if (!sites || count < 1 || count > kMaxSites) return 0;
-  size_t t = kStatusBytes;
+  size_t t = kControlBytes;
   for (int i = 0; i < count; ++i) {
     if (check_shape(sites[i].M, sites[i].K, sites[i].N, R) != LORA_OK) return 0;
     t += bwd_site_bytes(sites[i].M, sites[i].K, sites[i].N, R);

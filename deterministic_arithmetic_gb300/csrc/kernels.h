@@ -143,6 +143,15 @@ struct RowsArgs {
 };
 cudaError_t launch_rows(RowsArgs& args, int nsm, cudaStream_t st);
 
+// Single-launch forward of one site (fwd_fused.cu): the down, rows and up steps, ordered by
+// claimed work. ctl: the control words (kFusedCtlWords, zero between launches); batches of up to
+// kFusedMaxTiles row tiles of 128 rows.
+constexpr int kFusedMaxTiles = 4096;
+constexpr int kFusedCtlWords = 4 + 2 * kFusedMaxTiles;
+cudaError_t launch_fwd_fused(int RP, bool y_bf16, DownArgs& dargs, UpArgs& uargs, __nv_bfloat16* u, int R,
+                             uint32_t* ctl, int nsm, uint32_t* status, cudaStream_t st);
+cudaError_t prepare_fwd_fused();
+
 // Final combine of the weight-gradient chunk partials: canonical tree over
 // the C chunks, FP32 out. part is [C][RP][cols] (cols = K for dA, N for dB).
 struct CombineJob {

@@ -61,6 +61,9 @@ def _lib() -> ctypes.CDLL:
         lib.lora_delta_fwd.restype = ctypes.c_int
         lib.lora_delta_fwd_bf16.argtypes = lib.lora_delta_fwd.argtypes
         lib.lora_delta_fwd_bf16.restype = ctypes.c_int
+        lib.lora_delta_fwd_fused.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp,
+                                             ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        lib.lora_delta_fwd_fused.restype = ctypes.c_int
         lib.lora_delta_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
                                        _vp, _vp, ctypes.c_size_t, _vp]
         lib.lora_delta_bwd.restype = ctypes.c_int
@@ -182,6 +185,29 @@ def lora_delta_fwd(x, a, b, alpha: float, *, delta_y=None, u=None, workspace=Non
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != LORA_OK:
         raise LoraDeltaError(rc, name)
+    return delta_y, u
+
+
+def lora_delta_fwd_fused(x, a, b, alpha: float, *, delta_y=None, u=None, workspace=None, stream=None):
+    """The forward in a single launch (same bits as ``lora_delta_fwd``); a BF16 ``delta_y``
+    selects the BF16 output."""
+    M, K = x.shape
+    R = a.shape[0]
+    N = b.shape[0]
+    _check(x, "x", torch.bfloat16, (M, K)); _check(a, "a", torch.bfloat16, (R, K)); _check(b, "b", torch.bfloat16, (N, R))
+    if delta_y is None:
+        delta_y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if u is None:
+        u = torch.empty((M, R), dtype=torch.bfloat16, device=x.device)
+    y_bf16 = delta_y.dtype == torch.bfloat16
+    _check(delta_y, "delta_y", torch.bfloat16 if y_bf16 else torch.float32, (M, N)); _check(u, "u", torch.bfloat16, (M, R))
+    if workspace is None:
+        workspace = new_workspace(lora_delta_fwd_workspace_size(M, K, N, R), x.device)
+    rc = _lib().lora_delta_fwd_fused(_ptr(x), _ptr(a), _ptr(b), float(alpha), M, K, N, R, _ptr(delta_y), _ptr(u),
+                                     int(y_bf16), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_fwd_fused")
     return delta_y, u
 
 

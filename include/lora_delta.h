@@ -35,10 +35,15 @@
  *     and the call returns without waiting for it.
  *   - Argument errors are detected on the host before anything is enqueued.
  *   - `workspace` is scratch owned by the caller, at least the size the
- *     matching *_workspace_size() query returns, 256-byte aligned. Its first
- *     256 bytes are a device status block, which must be zero before the first
- *     call that uses the workspace (for example, allocate it zeroed). Its
- *     32-bit words:
+ *     matching *_workspace_size() query returns, 256-byte aligned. It starts
+ *     with a control block of LORA_DELTA_CONTROL_BYTES, which must be zero
+ *     before the first call that uses the workspace (for example, allocate
+ *     the workspace zeroed): a 256-byte device status block, then control
+ *     words of lora_delta_fwd_fused (work tickets, row-tile counters),
+ *     which every call leaves at zero again, also a call whose kernels gave
+ *     up on a wait. The rest is scratch that no call reads before writing, so
+ *     a workspace serves calls of any shape that fit in it. The status
+ *     block's 32-bit words:
  *       word 0  status: a kernel that gives up on an internal wait (every wait
  *               is bounded, 1 s by default) writes (site << 8) | 1 there, unless
  *               the word already holds a code (the first failure stays), and
@@ -69,6 +74,9 @@
 extern "C" {
 #endif
 
+/* Bytes at the start of every workspace that must be zero before its first use. */
+#define LORA_DELTA_CONTROL_BYTES (256 + 65536)
+
 typedef enum lora_status {
   LORA_OK = 0,
   LORA_ERR_NULL = 1,       /* a required pointer is NULL */
@@ -95,6 +103,27 @@ typedef enum lora_status {
  */
 lora_status lora_delta_fwd(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K, int64_t N,
                            int64_t R, float *delta_y, void *u, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The forward pass in a single launch (the fusion of the two GEMMs asked for in
+ * the review thread of page "[DSv4][P5-3] shared_grouped_lora_delta: CUDA +
+ * Triton, both batch-invariant"; U is still stored). Arguments, outputs, bits,
+ * workspace and errors are those of lora_delta_fwd (y_bf16 != 0: a BF16
+ * delta_y, as lora_delta_fwd_bf16). Inside the launch the three steps of
+ * lora_delta_fwd are ordered by claimed work and counters in the workspace's
+ * control block, not by grid barriers: down-projection units are claimed from a
+ * ticket counter, a row tile's U rows are formed once all of its slice
+ * partials are counted, and an up-projection unit starts once its row tile is
+ * flagged ready. No CTA ever waits for work held by a CTA that is not running,
+ * so the launch needs no co-residency. Batches of more than 4096 row tiles of
+ * 128 rows run the three launches of lora_delta_fwd instead. On a GB300 the
+ * three launches of lora_delta_fwd are the faster of the two at every shape
+ * measured (the counters and flags cost as much as the launch boundaries they
+ * replace); this call exists for callers that want a single launch.
+ */
+lora_status lora_delta_fwd_fused(const void *x, const void *a, const void *b, float alpha, int64_t M, int64_t K,
+                                 int64_t N, int64_t R, void *delta_y, void *u, int y_bf16, void *workspace,
+                                 size_t workspace_bytes, void *stream);
 
 /*
  * Forward pass with a BF16 delta_y: the half-size output a reviewer asks for
@@ -158,7 +187,8 @@ typedef struct lora_bwd_site {
 size_t lora_delta_fwd_grouped_workspace_size(const lora_fwd_site *sites, int count, int64_t R);
 size_t lora_delta_bwd_grouped_workspace_size(const lora_bwd_site *sites, int count, int64_t R);
 
-/* Forward of every site (two launches); y_bf16: every delta_y is BF16 (as lora_delta_fwd_bf16). */
+/* Forward of every site (three launches: down, rows, up, each over all sites' units); y_bf16:
+ * every delta_y is BF16 (as lora_delta_fwd_bf16). */
 lora_status lora_delta_fwd_grouped(const lora_fwd_site *sites, int count, int64_t R, int y_bf16, void *workspace,
                                    size_t workspace_bytes, void *stream);
 /* Backward of every site (the launches of one lora_delta_bwd). */

@@ -75,11 +75,14 @@ def test_workspace_sizes():
 
     f = ld.lora_delta_fwd_workspace_size(8192, 4096, 4096, 16)
     b = ld.lora_delta_bwd_workspace_size(8192, 4096, 4096, 16)
-    # U partials: 4 slices of 1024 x 8192 rows x 16 x fp32, plus the 256-byte status block
-    assert f == 256 + 4 * 8192 * 16 * 4
+    control = 256 + 65536     # status block and control words (LORA_DELTA_CONTROL_BYTES)
+    # U partials: 4 slices of 1024 x 8192 rows x 16 x fp32
+    assert f == control + 4 * 8192 * 16 * 4
     # dU partials (8 slices of 512 columns: the fused dY pass), dB and dA chunk partials (32 chunks of 256 rows)
-    assert b == 256 + 8 * 8192 * 16 * 4 + 32 * 16 * 4096 * 4 + 32 * 16 * 4096 * 4
-    assert ld.lora_delta_fwd_workspace_size(0, 128, 96, 8) == 256
+    assert b == control + 8 * 8192 * 16 * 4 + 32 * 16 * 4096 * 4 + 32 * 16 * 4096 * 4
+    assert ld.lora_delta_fwd_workspace_size(0, 128, 96, 8) == control
+    text = open(HEADER).read()
+    assert re.search(r"#define LORA_DELTA_CONTROL_BYTES \(256 \+ 65536\)", text)
     for bad in ((8, 100, 96, 8), (8, 128, 90, 8), (8, 128, 96, 12), (8, 128, 96, 72), (-1, 128, 96, 8), (8, 0, 96, 8)):
         assert ld.lora_delta_fwd_workspace_size(*bad) == 0
         assert ld.lora_delta_bwd_workspace_size(*bad) == 0
@@ -180,13 +183,14 @@ def test_grouped_calls_host_checks(lib):
     f = lib.lora_delta_fwd_grouped
     g = lib.lora_delta_bwd_grouped
     big = 1 << 30
-    # workspace: one status block plus every site's partial sums
+    # workspace: one control block plus every site's partial sums
+    control = 256 + 65536
     two = arr(ld.FwdSite, [fsite(), fsite(M=300, K=264, N=136)])
     assert lib.lora_delta_fwd_grouped_workspace_size(two, 2, 8) == \
-        ld.lora_delta_fwd_workspace_size(64, 128, 96, 8) + ld.lora_delta_fwd_workspace_size(300, 264, 136, 8) - 256
+        ld.lora_delta_fwd_workspace_size(64, 128, 96, 8) + ld.lora_delta_fwd_workspace_size(300, 264, 136, 8) - control
     btwo = arr(ld.BwdSite, [bsite(), bsite(M=300, K=264, N=136)])
     assert lib.lora_delta_bwd_grouped_workspace_size(btwo, 2, 16) == \
-        ld.lora_delta_bwd_workspace_size(64, 128, 96, 16) + ld.lora_delta_bwd_workspace_size(300, 264, 136, 16) - 256
+        ld.lora_delta_bwd_workspace_size(64, 128, 96, 16) + ld.lora_delta_bwd_workspace_size(300, 264, 136, 16) - control
     assert lib.lora_delta_fwd_grouped_workspace_size(two, 5, 8) == 0
     assert lib.lora_delta_fwd_grouped_workspace_size(arr(ld.FwdSite, [fsite(), fsite(K=100)]), 2, 8) == 0
     # errors, each site checked as a single-site call would be
