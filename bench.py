@@ -413,15 +413,26 @@ def exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, reps=5):
     prod = M * R * (K + N)
     ms = t_da + t_db
     rate = prod / (ms * 1e-3) / 1e12
-    # integer-issue roofline: one wide multiply-add per product, 32 per SM per cycle (8 lanes per
-    # scheduler per cycle, inferred from the FMA-heavy pipe counters), at the 2070 MHz SM maximum
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    peak = sms * 32 * 2.07e9 / 1e12
+    # integer-issue roofline, measured: the library's probe of independent 32-bit wide
+    # multiply-adds (the product step) in the digit kernel's launch shape, median of 5 launches
+    sink = torch.empty(ld.library().lora_delta_exact_rate_probe_sink_bytes(), dtype=torch.uint8, device=dev)
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(5)]
+    ld.lora_delta_exact_rate_probe(256, sink=sink)
+    n_mad = 0
+    for e in pev:
+        e[0].record()
+        n_mad = ld.lora_delta_exact_rate_probe(8192, sink=sink)
+        e[1].record()
+    torch.cuda.synchronize()
+    p_ms = sorted(e[0].elapsed_time(e[1]) for e in pev)[2]
+    peak = n_mad / (p_ms * 1e-3) / 1e12
     return {"grads_exact": {"ms": round(ms, 4), "ms_da": round(t_da, 4), "ms_db": round(t_db, 4),
                             "products": prod, "gproducts_per_s": round(rate * 1e3, 1),
-                            "roofline": {"bound": "alu", "achieved": round(rate, 3), "peak": round(peak, 2),
+                            "roofline": {"bound": "alu", "achieved": round(rate, 3), "peak": round(peak, 3),
                                          "unit": "Tproducts/s", "frac": round(rate / peak, 4),
-                                         "peak_kind": "derived: 32 wide integer multiply-adds per SM per cycle at 2070 MHz"},
+                                         "peak_kind": "measured: independent 32-bit wide multiply-add chains in the "
+                                                      "digit kernel's launch shape (lora_delta_exact_rate_probe)",
+                                         "peak_probe_ms": round(p_ms, 4), "peak_probe_products": n_mad},
                             "launches_per_step": 4, "median_of": reps}}
 
 
@@ -843,6 +854,35 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def profile_site(args):
+    """A few forward + backward steps of one MLP insertion point (fc1: K5120 -> N17408, fc2:
+    K17408 -> N5120; M4096, R16, alpha 1; device-drawn BF16 inputs), for an ncu capture of the
+    kernels at that shape; prints nothing that is a measurement."""
+    import torch
+    from deterministic_arithmetic_gb300 import build_lib
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    M, R = 4096, 16
+    K, N = (5120, 17408) if args.profile_site == "fc1" else (17408, 5120)
+
+    def rnd(*shape, s=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * s).to(torch.bfloat16)
+
+    x, a, b, dy = rnd(M, K), rnd(R, K, s=K ** -0.5), rnd(N, R, s=R ** -0.5), rnd(M, N, s=0.1)
+    wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+    wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
+    for _ in range(args.steps + args.warmup):
+        y, u = ld.lora_delta_fwd(x, a, b, 1.0, workspace=wf)
+        ld.lora_delta_bwd(dy, x, a, b, u, 1.0, workspace=wb)
+    torch.cuda.synchronize()
+    assert ld.lora_delta_device_status(wf) == 0 and ld.lora_delta_device_status(wb) == 0
+    print(f"profile-site {args.profile_site}: M={M} K={K} N={N} R={R}, {args.steps + args.warmup} steps done")
+
+
 def main():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
@@ -856,9 +896,14 @@ def main():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-variants", action="store_true", help="skip the forward-only FP32 / BF16 dY_lora timing")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-site", choices=["fc1", "fc2"], default=None,
+                   help="only run a few steps of one MLP site (for an ncu capture) and exit")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
+    if args.profile_site:
+        profile_site(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

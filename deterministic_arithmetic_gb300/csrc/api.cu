@@ -618,6 +618,28 @@ lora_status lora_delta_grads_exact_f32dy(const float* dy, const void* x, const v
                                 workspace, exact_bytes, stream);
 }
 
+lora_status lora_delta_exact_rate_probe(int64_t iters, void* sink, size_t sink_bytes, int64_t* products,
+                                        void* stream) {
+  if (!products) return LORA_ERR_NULL;
+  if (iters < 1 || iters >= (int64_t(1) << 31)) return LORA_ERR_SHAPE;
+  int nsm = 0;
+  lora_status s = device_ready(&nsm);
+  if (s != LORA_OK) return s;
+  if (!sink) return LORA_ERR_NULL;
+  if (!aligned16(sink)) return LORA_ERR_ALIGN;
+  if (sink_bytes < exact_probe_sink_bytes(nsm)) return LORA_ERR_WORKSPACE;
+  return launch_exact_rate_probe(int(iters), static_cast<long long*>(sink), nsm, products,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LORA_OK
+             : LORA_ERR_CUDA;
+}
+
+size_t lora_delta_exact_rate_probe_sink_bytes(void) {
+  int nsm = 0;
+  if (device_ready(&nsm) != LORA_OK) return 0;
+  return exact_probe_sink_bytes(nsm);
+}
+
 lora_status lora_delta_exact_combine(const int64_t* a, const int64_t* b, int64_t n, int64_t* out_digits, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 38)) return LORA_ERR_SHAPE;   // grid of n / 256 blocks
   if (n == 0) return LORA_OK;

@@ -40,7 +40,8 @@ struct DyCfg {
   static constexpr int kLeaves = 8;                        // MMAs of K=16 per product per stage
   static constexpr int kGroupCols = 2 * kLeaves * RP;      // dU leaves + dB leaves: 256 TMEM columns
   static constexpr int kGroups = 512 / kGroupCols;
-  static constexpr int kSliceTiles = kDySlice / kBN;       // 4 column tiles per unit
+  static constexpr int kSliceTiles = kDySlice / kBN;       // column tiles per unit (1, 2 or 4)
+  static constexpr int kSliceLevels = kSliceTiles == 4 ? 2 : (kSliceTiles == 2 ? 1 : 0);
   static constexpr int kChunkTiles = kDyChunk / kBM;       // 2 row tiles per unit
   static constexpr int kPrefetch = 4;                      // dY tiles warmed in L2 before the dependency wait
   static constexpr int kEpiWarps = 8, kXfWarps = 4;
@@ -48,7 +49,7 @@ struct DyCfg {
   static constexpr int kCPT = RP / 2;                      // columns of R per epilogue thread
   static constexpr int kNumBars = 3 * kStages + 2 * kGroups + 2;
   static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 + kNumBars * 8 + 16;
-  static_assert(kSliceTiles == 4 && kChunkTiles == 2, "epilogue tree shape");
+  static_assert((1 << kSliceLevels) == kSliceTiles && kChunkTiles == 2, "epilogue tree shape");
   static_assert(kStageBytes % 1024 == 0, "tiles must stay 1024-byte aligned");
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
       const int M = P.M, N = P.N;
       float* __restrict__ du_part = P.du_part;
       float* __restrict__ db_part = P.db_part;
-      float du_stk[C::kChunkTiles][2][C::kCPT];           // per row tile: canonical-tree stack over column tiles
+      float du_stk[C::kChunkTiles][C::kSliceLevels > 0 ? C::kSliceLevels : 1][C::kCPT];   // per row tile: tree stack
       float db_first[C::kCPT];
       bool ok_all = true;
 #pragma unroll
@@ -273,25 +274,26 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::kCPT; ++c) dun[c] = dbn[c] = 0.0f;   // zero leaves: neutral in the tree
           }
-          // dU of row tile j: canonical tree over the slice's column tiles i = 0..3
-          if ((i & 1) == 0) {
+          // dU of row tile j: canonical tree over the slice's column tiles (merge once per trailing
+          // one of i); after the last tile `dun` holds the slice's partial
+          bool merged = true;
 #pragma unroll
-            for (int c = 0; c < C::kCPT; ++c) du_stk[j][0][c] = dun[c];
-          } else {
+          for (int l = 0; l < C::kSliceLevels; ++l) {
+            if (((i >> l) & 1) == 0) {
 #pragma unroll
-            for (int c = 0; c < C::kCPT; ++c) dun[c] = __fadd_rn(du_stk[j][0][c], dun[c]);
-            if ((i & 2) == 0) {
+              for (int c = 0; c < C::kCPT; ++c) du_stk[j][l][c] = dun[c];
+              merged = false;
+              break;
+            }
 #pragma unroll
-              for (int c = 0; c < C::kCPT; ++c) du_stk[j][1][c] = dun[c];
-            } else {
-#pragma unroll
-              for (int c = 0; c < C::kCPT; ++c) dun[c] = __fadd_rn(du_stk[j][1][c], dun[c]);
-              const int row = ch * kDyChunk + j * C::kBM + tr;
-              if (ok_all && j < nrt && row < M) {
-                float4* dst = reinterpret_cast<float4*>(du_part + (size_t(sl) * M + row) * RP + h * C::kCPT);
-                dst[0] = make_float4(dun[0], dun[1], dun[2], dun[3]);
-                dst[1] = make_float4(dun[4], dun[5], dun[6], dun[7]);
-              }
+            for (int c = 0; c < C::kCPT; ++c) dun[c] = __fadd_rn(du_stk[j][l][c], dun[c]);
+          }
+          if (merged && i == C::kSliceTiles - 1) {
+            const int row = ch * kDyChunk + j * C::kBM + tr;
+            if (ok_all && j < nrt && row < M) {
+              float4* dst = reinterpret_cast<float4*>(du_part + (size_t(sl) * M + row) * RP + h * C::kCPT);
+              dst[0] = make_float4(dun[0], dun[1], dun[2], dun[3]);
+              dst[1] = make_float4(dun[4], dun[5], dun[6], dun[7]);
             }
           }
           // dB of column tile i: the chunk's two row tiles

@@ -597,6 +597,40 @@ cudaError_t launch_exact_combine(const long long* a, const long long* b, int64_t
                     out);
 }
 
+// The ceiling of the digit kernel's product step, measured: independent chains of 32-bit wide
+// multiply-adds (one per product of an exact sum) in the digit kernel's launch shape (two CTAs of
+// kThreads threads per SM). Each thread runs kProbeChains chains for `iters` rounds; the right
+// factor changes every round, so every product is a new one, and the chains' sum goes to
+// sink[thread] so that none of the work can be dropped.
+constexpr int kProbeChains = 8;
+__global__ void __launch_bounds__(kThreads, 2) exact_rate_probe_kernel(int iters, long long* sink) {
+  int a[kProbeChains];
+  long long acc[kProbeChains];
+#pragma unroll
+  for (int j = 0; j < kProbeChains; ++j) {
+    a[j] = int(threadIdx.x) * kProbeChains + j + 1;
+    acc[j] = j;
+  }
+  const int b0 = int(blockIdx.x) | 1;
+  for (int i = 0; i < iters; ++i) {
+    const int b = b0 + i;
+#pragma unroll
+    for (int j = 0; j < kProbeChains; ++j) asm volatile("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[j]) : "r"(a[j]), "r"(b));
+  }
+  long long t = 0;
+#pragma unroll
+  for (int j = 0; j < kProbeChains; ++j) t += acc[j];
+  sink[size_t(blockIdx.x) * blockDim.x + threadIdx.x] = t;
+}
+
+size_t exact_probe_sink_bytes(int nsm) { return size_t(2) * nsm * kThreads * sizeof(long long); }
+
+cudaError_t launch_exact_rate_probe(int iters, long long* sink, int nsm, int64_t* products, cudaStream_t st) {
+  *products = int64_t(2) * nsm * kThreads * kProbeChains * int64_t(iters);
+  exact_rate_probe_kernel<<<dim3(unsigned(2 * nsm)), dim3(kThreads), 0, st>>>(iters, sink);
+  return cudaGetLastError();
+}
+
 cudaError_t prepare_exact() {
   cudaError_t e = cudaFuncSetAttribute(exact_digits_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(sizeof(ExactSmem)));

@@ -187,6 +187,10 @@ cudaError_t launch_exact(const void* left, int ldl, const void* right, int ldr, 
 cudaError_t launch_exact_combine(const long long* a, const long long* b, int64_t n, long long* out_digits, float* out,
                                  cudaStream_t st);
 cudaError_t prepare_exact();
+// Multiply-add rate probe of the exact mode (the roofline of its digit kernel): `products` is set
+// to the number of 32-bit wide multiply-adds the launch performs; sink: exact_probe_sink_bytes.
+size_t exact_probe_sink_bytes(int nsm);
+cudaError_t launch_exact_rate_probe(int iters, long long* sink, int nsm, int64_t* products, cudaStream_t st);
 
 // Raise the dynamic shared-memory limit of every kernel instance in a
 // translation unit (once per device, with that device current).

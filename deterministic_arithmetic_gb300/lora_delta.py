@@ -107,6 +107,10 @@ def _lib() -> ctypes.CDLL:
             lib.lora_delta_exact_combine.restype = ctypes.c_int
             lib.lora_delta_exact_finalize.argtypes = [_vp, _i64, _vp, _vp]
             lib.lora_delta_exact_finalize.restype = ctypes.c_int
+            lib.lora_delta_exact_rate_probe.argtypes = [_i64, _vp, ctypes.c_size_t, ctypes.POINTER(_i64), _vp]
+            lib.lora_delta_exact_rate_probe.restype = ctypes.c_int
+            lib.lora_delta_exact_rate_probe_sink_bytes.argtypes = []
+            lib.lora_delta_exact_rate_probe_sink_bytes.restype = ctypes.c_size_t
         lib.lora_status_str.argtypes = [ctypes.c_int]
         lib.lora_status_str.restype = ctypes.c_char_p
         lib.lora_delta_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
@@ -313,6 +317,22 @@ def lora_delta_exact_combine(a, b=None, *, out=None, stream=None):
     if rc != LORA_OK:
         raise LoraDeltaError(rc, "lora_delta_exact_combine")
     return out
+
+
+def lora_delta_exact_rate_probe(iters: int, *, sink=None, stream=None) -> int:
+    """Enqueue the exact mode's multiply-add rate probe; returns the number of multiply-adds the
+    launch performs (time it with CUDA events on ``stream``)."""
+    need = int(_lib().lora_delta_exact_rate_probe_sink_bytes())
+    if need == 0:
+        raise LoraDeltaError(7, "lora_delta_exact_rate_probe_sink_bytes")
+    if sink is None:
+        sink = torch.empty(need, dtype=torch.uint8, device="cuda")
+    products = _i64(0)
+    rc = _lib().lora_delta_exact_rate_probe(int(iters), _ptr(sink), sink.numel() * sink.element_size(),
+                                            ctypes.byref(products), _stream(stream))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_exact_rate_probe")
+    return int(products.value)
 
 
 def lora_delta_exact_all_reduce(digits, *, group=None, stream=None):

@@ -360,6 +360,21 @@ lora_status lora_delta_exact_combine(const int64_t *a, const int64_t *b, int64_t
  * n as for lora_delta_exact_combine. */
 lora_status lora_delta_exact_finalize(const int64_t *digits, int64_t n, float *out, void *stream);
 
+/*
+ * Measurement aid: the rate at which this device performs the exact mode's
+ * product step (one 32-bit by 32-bit multiply-add into a 64-bit sum per
+ * product), the ceiling of lora_delta_grads_exact's digit kernel. Enqueues one
+ * launch in the digit kernel's shape that performs *products independent such
+ * multiply-adds (iters rounds per chain, 1 <= iters < 2^31); time it with CUDA
+ * events on `stream`. sink: device scratch of at least
+ * lora_delta_exact_rate_probe_sink_bytes() bytes (16-byte aligned; its
+ * contents are meaningless), which the launch writes so that no work can be
+ * dropped. The sink-size query returns 0 when the current device is unusable.
+ */
+lora_status lora_delta_exact_rate_probe(int64_t iters, void *sink, size_t sink_bytes, int64_t *products,
+                                        void *stream);
+size_t lora_delta_exact_rate_probe_sink_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

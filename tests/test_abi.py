@@ -332,3 +332,13 @@ def test_no_base_weight_in_the_signatures():
         assert m, struct
         fields = re.findall(r"(\w+)\s*;", m.group(1).replace(",", ";"))
         assert set(fields) <= allowed, f"{struct}: unexpected fields {set(fields) - allowed}"
+
+
+def test_exact_rate_probe_host_checks(lib):
+    f = lib.lora_delta_exact_rate_probe
+    f.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    n = ctypes.c_int64(0)
+    assert f(16, 0x10000, 1 << 20, None, None) == 1            # LORA_ERR_NULL (products)
+    assert f(0, 0x10000, 1 << 20, ctypes.byref(n), None) == 2  # LORA_ERR_SHAPE (iters)
+    assert f(1 << 31, 0x10000, 1 << 20, ctypes.byref(n), None) == 2

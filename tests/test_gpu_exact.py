@@ -267,3 +267,18 @@ def test_f32_dy(oracle):
     b = ld.lora_delta_grads_exact(t["dy"], t["x"], t["u"], t["du"], alpha, want=("db",))
     torch.cuda.synchronize()
     _bits_equal("dB: f32 dy holding BF16 values", a["db"].cpu().numpy(), b["db"].cpu().numpy())
+
+
+def test_rate_probe_runs_and_counts_its_products():
+    """The multiply-add rate probe (the exact mode's measured roofline): the launch performs the
+    number of multiply-adds it reports (two CTAs of 512 threads per SM, 8 chains per thread) and
+    writes every thread's sum."""
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.zeros(ld.library().lora_delta_exact_rate_probe_sink_bytes(), dtype=torch.uint8, device="cuda")
+    assert sink.numel() == 2 * nsm * 512 * 8
+    n = ld.lora_delta_exact_rate_probe(16, sink=sink)
+    torch.cuda.synchronize()
+    assert n == 2 * nsm * 512 * 8 * 16
+    assert sink.view(torch.int64).ne(0).all().item()
