@@ -434,4 +434,64 @@ __device__ __forceinline__ uint4 slices_to_bf16x8(const float* p, size_t stride,
   return pack_bf16x8(v);
 }
 
+// The same value for S > 8 slices, formed by four consecutive lanes of one warp (l4 = lane & 3,
+// gmask = the four lanes' mask, all four active): lane l adds block 4 s + l of 8 slices (all its
+// loads in flight; a partial last block is padded with zeros, as in the one-thread tree), the
+// four block sums meet by shuffles in the canonical order (a block past the last one passes its
+// partner up unchanged), and the sums of the 32-slice groups go through the canonical tree over
+// the group index. Same bits as slices_to_bf16x8; every lane returns the packed value.
+__device__ __forceinline__ uint4 slices_to_bf16x8_4lanes(const float* p, size_t stride, int S, int l4,
+                                                         unsigned gmask) {
+  const int nb = (S + 7) / 8, nsg = (nb + 3) / 4;
+  float stk[24][8];
+  int top = 0;
+  for (int sg = 0; sg < nsg; ++sg) {
+    const int b = 4 * sg + l4;
+    float x[1][8];
+    if (b < nb) {
+      block_slices<8, 1>(p + size_t(b) * 8 * stride, stride, min(8, S - 8 * b), x);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) x[0][c] = 0.0f;
+    }
+    // pairs (0, 1) and (2, 3): left + right, or left alone when the right block does not exist
+    const bool has_right = 4 * sg + (l4 | 1) < nb;
+    float pr[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float y = __shfl_xor_sync(gmask, x[0][c], 1, 4);
+      const float left = (l4 & 1) ? y : x[0][c], right = (l4 & 1) ? x[0][c] : y;
+      pr[c] = has_right ? __fadd_rn(left, right) : left;
+    }
+    // the two pairs: (0, 1) + (2, 3), or (0, 1) alone when block 2 does not exist
+    const bool has_second = 4 * sg + 2 < nb;
+    float sgs[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float y = __shfl_xor_sync(gmask, pr[c], 2, 4);
+      const float first = (l4 & 2) ? y : pr[c], second = (l4 & 2) ? pr[c] : y;
+      sgs[c] = has_second ? __fadd_rn(first, second) : first;
+    }
+    // canonical tree over the 32-slice groups: merge once per trailing one of sg
+    for (int t = sg; t & 1; t >>= 1) {
+      --top;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) sgs[c] = __fadd_rn(stk[top][c], sgs[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) stk[top][c] = sgs[c];
+    ++top;
+  }
+  float o[8];
+  --top;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) o[c] = stk[top][c];
+  while (top > 0) {
+    --top;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) o[c] = __fadd_rn(stk[top][c], o[c]);
+  }
+  return pack_bf16x8(o);
+}
+
 }  // namespace lora

@@ -40,15 +40,9 @@ __global__ void __launch_bounds__(256) rows_kernel(const __grid_constant__ RowsA
   }
 }
 
-// The same for more than 8 slices, with four lanes per group of 8 values: lane l adds block
-// 4 s + l of 8 slices (every load of its block in flight; a partial last block is padded with
-// zeros, as in the one-thread tree), the four block sums meet by shuffles in the canonical
-// order (a block past the last one passes its partner up unchanged), and the sums of the
-// 32-slice groups go through the canonical tree over the group index. Same bits as the
-// one-thread tree of slices_to_bf16x8 for every slice count (a site with at most 8 slices
-// takes that function itself: its zero padding differs, which decides the sign of a zero).
-// The four lanes of an item are consecutive threads of one warp, all active or all idle
-// together.
+// The same for more than 8 slices, with four lanes per group of 8 values
+// (slices_to_bf16x8_4lanes; a site with at most 8 slices takes the one-thread tree). The four
+// lanes of an item are consecutive threads of one warp, all active or all idle together.
 template <bool GR>
 __global__ void __launch_bounds__(256) rows4_kernel(const __grid_constant__ RowsArgs args) {
   grid_dependency_wait();
@@ -67,60 +61,13 @@ __global__ void __launch_bounds__(256) rows4_kernel(const __grid_constant__ Rows
     const int g = int(li % G);
     const float* p = P.part + size_t(row) * RP + g * 8;
     const size_t stride = size_t(P.M) * RP;
-    const int S = P.S, nb = (S + 7) / 8, nsg = (nb + 3) / 4;
+    const int S = P.S;
     if (S <= 8) {   // a site of a grouped call with few slices: the one-thread tree
       if (l4 == 0) *reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8) = slices_to_bf16x8(p, stride, S);
       continue;
     }
-    float stk[24][8];
-    int top = 0;
-    for (int sg = 0; sg < nsg; ++sg) {
-      const int b = 4 * sg + l4;
-      float x[1][8];
-      if (b < nb) {
-        block_slices<8, 1>(p + size_t(b) * 8 * stride, stride, min(8, S - 8 * b), x);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) x[0][c] = 0.0f;
-      }
-      // pairs (0, 1) and (2, 3): left + right, or left alone when the right block does not exist
-      const bool has_right = 4 * sg + (l4 | 1) < nb;
-      float pr[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float y = __shfl_xor_sync(gmask, x[0][c], 1, 4);
-        const float left = (l4 & 1) ? y : x[0][c], right = (l4 & 1) ? x[0][c] : y;
-        pr[c] = has_right ? __fadd_rn(left, right) : left;
-      }
-      // the two pairs: (0, 1) + (2, 3), or (0, 1) alone when block 2 does not exist
-      const bool has_second = 4 * sg + 2 < nb;
-      float sgs[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float y = __shfl_xor_sync(gmask, pr[c], 2, 4);
-        const float first = (l4 & 2) ? y : pr[c], second = (l4 & 2) ? pr[c] : y;
-        sgs[c] = has_second ? __fadd_rn(first, second) : first;
-      }
-      // canonical tree over the 32-slice groups: merge once per trailing one of sg
-      for (int t = sg; t & 1; t >>= 1) {
-        --top;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) sgs[c] = __fadd_rn(stk[top][c], sgs[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) stk[top][c] = sgs[c];
-      ++top;
-    }
-    float o[8];
-    --top;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) o[c] = stk[top][c];
-    while (top > 0) {
-      --top;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) o[c] = __fadd_rn(stk[top][c], o[c]);
-    }
-    if (l4 == 0) *reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8) = pack_bf16x8(o);
+    const uint4 o = slices_to_bf16x8_4lanes(p, stride, S, l4, gmask);
+    if (l4 == 0) *reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8) = o;
   }
 }
 
