@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
 # kernels of one step: the forward's three launches, the backward's five (R <= 16)
 KERNELS_FWD = ["down U", "rows U", "up dY_lora"]
-KERNELS_BWD = ["dy dU+dB", "rows dU", "up dX", "wgrad dA", "combine dA+dB"]
+KERNELS_BWD = ["dy dU+dB", "rows dU+dB", "up dX", "wgrad dA", "combine dA"]
 KERNELS = KERNELS_FWD + KERNELS_BWD
 N_FWD = len(KERNELS_FWD)
 FUSED_FWD = "fwd down+rows+up"   # lora_delta_fwd_fused: the same three steps in one launch
@@ -68,10 +68,10 @@ def algorithmic_bytes(M, K, N, R):
         **fwd,
         "dy dU+dB": M * N * bf + N * R * bf + M * R * bf            # dY (read once), B, U -> dU, dB partials
                     + N * R * f4,                                   # (dB written by the combine)
-        "rows dU": M * R * bf,                                      # -> dU
+        "rows dU+dB": M * R * bf,                                   # -> dU (and dB from its chunk partials)
         "up dX": M * R * bf + R * K * bf + M * K * f4,              # dU, A -> dX
         "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA partials (dA written by the combine)
-        "combine dA+dB": 0,
+        "combine dA": 0,
     }
 
 

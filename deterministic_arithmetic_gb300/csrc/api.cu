@@ -318,7 +318,7 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   if (launch_down(RP, false, dargs, status, grid_for(n_down, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   // U = bf16(tree over the K-slice partials), written to u
-  if (launch_rows(rargs, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
+  if (launch_rows(rargs, nullptr, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   if (launch_up(RP, false, y_bf16, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
@@ -345,11 +345,11 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   WgArgs bargs{}, aargs{};
   UpArgs uargs{};
   RowsArgs rargs{};
-  CombineJobs jobs{};
+  CombineJobs da_jobs{}, db_jobs{};
   yargs.n = dargs.n = bargs.n = aargs.n = uargs.n = rargs.n = m;
   uargs.R = rargs.R = int(R);
   rargs.RP = RP;
-  jobs.n = 2 * m;
+  da_jobs.n = db_jobs.n = m;
   size_t off = kControlBytes;
   int64_t n_dy = 0, n_du = 0, n_db = 0, n_up = 0, n_da = 0;
   for (int j = 0; j < m; ++j) {
@@ -408,8 +408,8 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     wa.M = M;
     wa.Cw = K;
     wa.alpha = 1.0f;
-    jobs.j[2 * j] = CombineJob{dapart, p.da, C, K, int(R), RP, 0};
-    jobs.j[2 * j + 1] = CombineJob{dbpart, p.db, C, N, int(R), RP, 1};
+    da_jobs.j[j] = CombineJob{dapart, p.da, C, K, int(R), RP, 0};
+    db_jobs.j[j] = CombineJob{dbpart, p.db, C, N, int(R), RP, 1};
     n_up += up_units(M, K, RP);
     n_da += wgrad_units(M, K, RP);
   }
@@ -428,15 +428,16 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     if (launch_wgrad(RP, true, bargs, status, grid_for(n_db, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
   }
-  // dU = bf16(tree over the N-slice partials), written to du
-  if (launch_rows(rargs, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
+  // dU = bf16(tree over the N-slice partials), written to du; in the same launch dB = the
+  // canonical tree over the chunk partials just written (still in L2)
+  if (launch_rows(rargs, &db_jobs, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
-  // dA and dB: canonical tree over the chunk partials
-  if (launch_combine(jobs, st) != cudaSuccess) return LORA_ERR_CUDA;
+  // dA: canonical tree over the chunk partials
+  if (launch_combine(da_jobs, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
   return LORA_OK;
 }

@@ -141,7 +141,7 @@ struct RowsArgs {
   int64_t total;
   int n, R, RP;
 };
-cudaError_t launch_rows(RowsArgs& args, int nsm, cudaStream_t st);
+
 
 // Single-launch forward of one site (fwd_fused.cu): the down, rows and up steps, ordered by
 // claimed work. ctl: the control words (kFusedCtlWords, zero between launches); batches of up to
@@ -167,6 +167,9 @@ struct CombineJobs {
   int n;
 };
 cudaError_t launch_combine(const CombineJobs& jobs, cudaStream_t st);
+// The rows launch (rows.cu); jobs (may be null): combine jobs run by the same launch after the
+// rows blocks (the backward's dB, whose chunk partials the preceding kernel has just written).
+cudaError_t launch_rows(RowsArgs& args, const CombineJobs* jobs, int nsm, cudaStream_t st);
 
 // dV = bf16(fp32(dy * alpha)) from a binary32 dY of n values (n a multiple of 8), into dv.
 cudaError_t launch_dv_from_f32(const float* dy, float alpha, int64_t n, void* dv, int nsm, cudaStream_t st);

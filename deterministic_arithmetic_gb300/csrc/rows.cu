@@ -14,44 +14,34 @@
 // writes). The partials were just written by the preceding kernel and are read
 // from L2 (cache-global loads). This is the only consumer of the partials, so
 // every row is formed once; the up-projection that follows loads finished rows.
+//
+// The launch may also carry combine jobs (combine.cuh): in the backward pass,
+// the dB tree over the chunk partials that the dy kernel has just written,
+// while they are still in L2; those blocks follow the rows blocks.
 #include <algorithm>
 
-#include "common.cuh"
-#include "kernels.h"
+#include "combine.cuh"
 
 namespace lora {
 
-template <bool GR>
-__global__ void __launch_bounds__(256) rows_kernel(const __grid_constant__ RowsArgs args) {
+// FOUR: four lanes per item (some site has more than 8 slices; slices_to_bf16x8_4lanes),
+// otherwise one thread per item. The first nrb blocks form rows; the rest run combine jobs.
+template <bool GR, bool FOUR>
+__global__ void __launch_bounds__(256)
+    rows_kernel(const __grid_constant__ RowsArgs args, const __grid_constant__ CombineJobs cj, int nrb) {
   grid_dependency_wait();      // the partials of the preceding kernel are complete
   grid_dependents_launch();
-  const int R = args.R, RP = args.RP, G = R / 8;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < args.total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    int k = 0;
-    if constexpr (GR)
-      while (k + 1 < args.n && i >= args.s[k + 1].item0) ++k;
-    const RowsSite& P = args.s[k];
-    const int64_t li = i - P.item0;
-    const int64_t row = li / G;
-    const int g = int(li % G);
-    *reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8) =
-        slices_to_bf16x8(P.part + size_t(row) * RP + g * 8, size_t(P.M) * RP, P.S);
+  if (int(blockIdx.x) >= nrb) {
+    combine_table_block(cj, int(blockIdx.x) - nrb);
+    return;
   }
-}
-
-// The same for more than 8 slices, with four lanes per group of 8 values
-// (slices_to_bf16x8_4lanes; a site with at most 8 slices takes the one-thread tree). The four
-// lanes of an item are consecutive threads of one warp, all active or all idle together.
-template <bool GR>
-__global__ void __launch_bounds__(256) rows4_kernel(const __grid_constant__ RowsArgs args) {
-  grid_dependency_wait();
-  grid_dependents_launch();
   const int R = args.R, RP = args.RP, G = R / 8;
-  const int l4 = threadIdx.x & 3;
+  constexpr int L = FOUR ? 4 : 1;                     // lanes per item
+  const int l4 = FOUR ? int(threadIdx.x & 3) : 0;
   const unsigned gmask = 0xFu << (threadIdx.x & 28u);
-  for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 2; i < args.total;
-       i += (int64_t(gridDim.x) * blockDim.x) >> 2) {
+  // the L lanes of an item are consecutive threads of one warp, all active or all idle together
+  for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / L; i < args.total;
+       i += int64_t(nrb) * blockDim.x / L) {
     int k = 0;
     if constexpr (GR)
       while (k + 1 < args.n && i >= args.s[k + 1].item0) ++k;
@@ -61,35 +51,42 @@ __global__ void __launch_bounds__(256) rows4_kernel(const __grid_constant__ Rows
     const int g = int(li % G);
     const float* p = P.part + size_t(row) * RP + g * 8;
     const size_t stride = size_t(P.M) * RP;
-    const int S = P.S;
-    if (S <= 8) {   // a site of a grouped call with few slices: the one-thread tree
-      if (l4 == 0) *reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8) = slices_to_bf16x8(p, stride, S);
-      continue;
+    uint4* out = reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8);
+    if (!FOUR || P.S <= 8) {   // the one-thread tree (in the four-lane form: lane 0 alone)
+      if (l4 == 0) *out = slices_to_bf16x8(p, stride, P.S);
+    } else {
+      const uint4 o = slices_to_bf16x8_4lanes(p, stride, P.S, l4, gmask);
+      if (l4 == 0) *out = o;
     }
-    const uint4 o = slices_to_bf16x8_4lanes(p, stride, S, l4, gmask);
-    if (l4 == 0) *reinterpret_cast<uint4*>(P.out + size_t(row) * R + g * 8) = o;
   }
 }
 
-cudaError_t launch_rows(RowsArgs& args, int nsm, cudaStream_t st) {
+template <bool GR, bool FOUR>
+static cudaError_t launch_inst(const RowsArgs& args, const CombineJobs& cj, int nrb, cudaStream_t st) {
+  const int blocks = nrb + combine_table_blocks(cj);
+  return launch_pdl(rows_kernel<GR, FOUR>, dim3(unsigned(blocks)), dim3(256), 0, st, args, cj, nrb);
+}
+
+cudaError_t launch_rows(RowsArgs& args, const CombineJobs* jobs, int nsm, cudaStream_t st) {
   if (args.n < 1 || args.n > kMaxSites) return cudaErrorInvalidValue;
+  CombineJobs cj{};
+  if (jobs) {
+    if (jobs->n < 0 || jobs->n > 2 * kMaxSites) return cudaErrorInvalidValue;
+    cj = *jobs;
+  }
   int64_t item0 = 0;
+  int smax = 0;
   for (int i = 0; i < args.n; ++i) {
     args.s[i].item0 = item0;
     item0 += int64_t(args.s[i].M) * (args.R / 8);
+    smax = std::max(smax, args.s[i].S);
   }
   args.total = item0;
-  if (item0 == 0) return cudaSuccess;
-  int smax = 0;
-  for (int i = 0; i < args.n; ++i) smax = std::max(smax, args.s[i].S);
-  if (smax > 8) {   // many slices: four lanes per item
-    const int blocks = int(std::min<int64_t>(ceil_div(item0 * 4, 256), int64_t(nsm) * 8));
-    if (args.n > 1) return launch_pdl(rows4_kernel<true>, dim3(blocks), dim3(256), 0, st, args);
-    return launch_pdl(rows4_kernel<false>, dim3(blocks), dim3(256), 0, st, args);
-  }
-  const int blocks = int(std::min<int64_t>(ceil_div(item0, 256), int64_t(nsm) * 8));
-  if (args.n > 1) return launch_pdl(rows_kernel<true>, dim3(blocks), dim3(256), 0, st, args);
-  return launch_pdl(rows_kernel<false>, dim3(blocks), dim3(256), 0, st, args);
+  const bool four = smax > 8;
+  const int nrb = item0 == 0 ? 0 : int(std::min<int64_t>(ceil_div(item0 * (four ? 4 : 1), 256), int64_t(nsm) * 8));
+  if (nrb + combine_table_blocks(cj) == 0) return cudaSuccess;
+  if (four) return args.n > 1 ? launch_inst<true, true>(args, cj, nrb, st) : launch_inst<false, true>(args, cj, nrb, st);
+  return args.n > 1 ? launch_inst<true, false>(args, cj, nrb, st) : launch_inst<false, false>(args, cj, nrb, st);
 }
 
 }  // namespace lora

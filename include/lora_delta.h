@@ -209,7 +209,8 @@ lora_status lora_delta_bwd_grouped(const lora_bwd_site *sites, int count, int64_
  * dA and dB reduce over all M rows in fixed 256-row chunks whose partials are
  * added by the canonical pairwise tree over the chunk index.
  * Kernels: dU and dB partials (one pass over dY for R <= 16), rows (adds the
- * dU partials into dU and writes du), dX, dA partials, combine (dA, dB).
+ * dU partials into dU and writes du; its other blocks add the dB chunk
+ * partials into db while they are still in L2), dX, dA partials, combine (dA).
  */
 lora_status lora_delta_bwd(const void *dy, const void *x, const void *a, const void *b, const void *u, float alpha,
                            int64_t M, int64_t K, int64_t N, int64_t R, float *dx, float *da, float *db, void *du,
