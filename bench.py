@@ -94,7 +94,16 @@ def measured_peaks():
 # dram__bytes_write.sum), keyed by kernel, with the hash of the kernel sources
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
+    "down U": {"bytes": 71_010_000, "src_hash": "bc88ce45787982e6"},
+    "rows U": {"bytes": 30_000, "src_hash": "bc88ce45787982e6"},
+    "up dY_lora": {"bytes": 125_210_000, "src_hash": "bc88ce45787982e6"},
+    "dy dU+dB": {"bytes": 80_690_000, "src_hash": "bc88ce45787982e6"},
+    "rows dU+dB": {"bytes": 1_220_000, "src_hash": "bc88ce45787982e6"},
+    "up dX": {"bytes": 126_520_000, "src_hash": "bc88ce45787982e6"},
+    "wgrad dA": {"bytes": 75_200_000, "src_hash": "bc88ce45787982e6"},
+    "combine dA": {"bytes": 430_000, "src_hash": "bc88ce45787982e6"},
+}
 
 
 def source_hash() -> str:
@@ -718,8 +727,13 @@ def run_ours(args, world, rank, local):
     value = total_bytes * world / (ms_step * 1e-3) / 1e9
     dominant = max(kavg, key=lambda k: kavg[k])
     achieved = alg[dominant] / (kavg[dominant] * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(dominant)
-    traffic = tr["bytes"] if tr and tr.get("src_hash") == source_hash() else None
+    src = source_hash()
+
+    def ncu_traffic(k):
+        tr = NCU_TRAFFIC.get(k)
+        return tr["bytes"] if tr and tr.get("src_hash") == src else None
+
+    traffic = ncu_traffic(dominant)
 
     # ---------------------------------------- forward variants (FP32 / BF16 dY_lora)
     variants = None
@@ -842,7 +856,8 @@ def run_ours(args, world, rank, local):
                             "includes its launch boundary; events stop the kernels' launch overlap)",
             "kernels": {k: {"ms": round(kavg[k], 5), "algorithmic_bytes": alg[k],
                             "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
-                            "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None}
+                            "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None,
+                            "traffic": ncu_traffic(k)}
                         for k in KERNELS},
             "gpu_launches": len(KERNELS) * args.steps,
             "e2e": e2e,
