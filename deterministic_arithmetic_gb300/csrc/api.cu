@@ -38,6 +38,51 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 void* g_events[64];
 int g_nevents = 0;
 
+// Cluster size of the single-launch cluster kernels (lora_delta_set_cluster_size): -1 off (the
+// separate launches, the default), 0 automatic, else 2, 4 or 8 CTAs.
+int g_cluster = -1;
+constexpr int kDefaultCluster = 4;
+// A CTA of a cluster waits for its peers' share of a tile (forward: 128 rows x K / cl of x; backward:
+// 256 rows x N / cl of dY): the cluster launches take shapes whose share is at most this many bytes
+// (about a millisecond of streaming), far inside the kernels' wait limit; larger shapes run the
+// separate launches.
+constexpr int64_t kClusterShareBytes = int64_t(32) << 20;
+// Clusters of each instance that fit on a device at once: [device][RP 16 / 32][bf16 output][log2 cl]
+// (forward) and [device][log2 cl] (backward)
+int g_max_clusters[kMaxDevices][2][2][4];
+int g_max_bwd_clusters[kMaxDevices][4];
+
+// Clusters of cl CTAs of the forward cluster kernel for (RP, y_bf16) that fit on the current
+// device at once (queried once per device and instance); 0 when none.
+int fwd_clusters(int RP, bool y_bf16, int cl) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int li = cl == 1 ? 0 : (cl == 2 ? 1 : (cl == 4 ? 2 : 3));
+  std::lock_guard<std::mutex> lock(g_mu);
+  int& v = g_max_clusters[dev][RP == 16 ? 0 : 1][y_bf16 ? 1 : 0][li];
+  if (v == 0) {
+    int n = 0;
+    if (fwd_cluster_max_clusters(RP, y_bf16, cl, &n) != cudaSuccess || n < 1) return 0;
+    v = n;
+  }
+  return v;
+}
+
+// The same for the backward cluster kernel.
+int bwd_clusters(int cl) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int li = cl == 1 ? 0 : (cl == 2 ? 1 : (cl == 4 ? 2 : 3));
+  std::lock_guard<std::mutex> lock(g_mu);
+  int& v = g_max_bwd_clusters[dev][li];
+  if (v == 0) {
+    int n = 0;
+    if (bwd_cluster_max_clusters(cl, &n) != cudaSuccess || n < 1) return 0;
+    v = n;
+  }
+  return v;
+}
+
 lora_status device_ready(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
@@ -55,7 +100,8 @@ lora_status device_ready(int* num_sms) {
     d.usable = (major == 10 && minor == 3);
     if (d.usable) {
       if (prepare_down() != cudaSuccess || prepare_up() != cudaSuccess || prepare_wgrad() != cudaSuccess ||
-          prepare_dy() != cudaSuccess || prepare_exact() != cudaSuccess || prepare_fwd_fused() != cudaSuccess) {
+          prepare_dy() != cudaSuccess || prepare_exact() != cudaSuccess || prepare_fwd_fused() != cudaSuccess ||
+          prepare_fwd_cluster() != cudaSuccess || prepare_bwd_cluster() != cudaSuccess) {
         d.probed = false;
         return LORA_ERR_CUDA;
       }
@@ -307,6 +353,30 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
+  const int fcl = g_cluster > 0 ? g_cluster : kDefaultCluster;
+  if (!fused && m == 1 && RP <= 32 && g_cluster >= 0 && 128 * in[active[0]].K * 2 / fcl <= kClusterShareBytes) {
+    // one launch on clusters: down, rows and up steps per 128-row tile
+    const FwdIn& p = in[active[0]];
+    const int cl = fcl;
+    const int mc = fwd_clusters(RP, y_bf16, cl);
+    if (mc < 1) return LORA_ERR_CUDA;
+    FcArgs fa{};
+    fa.x = dargs.s[0].in;
+    fa.a = dargs.s[0].w;
+    fa.out = uargs.s[0].out;
+    if (!make_map(&fa.b, p.b, false, p.N, R, RP, fc_bn(RP), swizzle_for_span(span))) return LORA_ERR_CUDA;
+    fa.part = dargs.s[0].part;
+    fa.u = static_cast<__nv_bfloat16*>(p.u);
+    fa.M = int(p.M);
+    fa.K = int(p.K);
+    fa.N = int(p.N);
+    fa.R = int(R);
+    fa.alpha = p.alpha;
+    const int ncl = int(std::min<int64_t>(mc, ceil_div(p.M, 128)));
+    if (launch_fwd_cluster(RP, y_bf16, fa, status, cl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
+    rec.mark();
+    return LORA_OK;
+  }
   if (fused && m == 1 && ceil_div(in[active[0]].M, 128) <= kFusedMaxTiles) {
     uint32_t* ctl = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
     if (launch_fwd_fused(RP, y_bf16, dargs, uargs, static_cast<__nv_bfloat16*>(in[active[0]].u), int(R), ctl, nsm,
@@ -416,6 +486,41 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
+  const int bcl = g_cluster > 0 ? g_cluster : kDefaultCluster;
+  if (m == 1 && RP == 16 && g_cluster >= 0 && int64_t(kDyChunk) * in[active[0]].N * 2 / bcl <= kClusterShareBytes) {
+    // one launch on clusters (dU, dB partials; dU rows; dX, dA partials per 256-row chunk), then
+    // the canonical trees over the chunk partials of dA and dB
+    const BwdIn& p = in[active[0]];
+    const int cl = bcl;
+    const int mc = bwd_clusters(cl);
+    if (mc < 1) return LORA_ERR_CUDA;
+    BcArgs ba{};
+    ba.dy = yargs.s[0].dy;
+    ba.b = yargs.s[0].b;
+    ba.u = yargs.s[0].u;
+    ba.x = aargs.s[0].in;
+    ba.a = uargs.s[0].b;
+    ba.dx = uargs.s[0].out;
+    ba.du_part = yargs.s[0].du_part;
+    ba.db_part = yargs.s[0].db_part;
+    ba.da_part = aargs.s[0].part;
+    ba.du = static_cast<__nv_bfloat16*>(p.du);
+    ba.M = int(p.M);
+    ba.K = int(p.K);
+    ba.N = int(p.N);
+    ba.R = int(R);
+    ba.alpha = p.alpha;
+    const int ncl = int(std::min<int64_t>(mc, ceil_div(p.M, kDyChunk)));
+    if (launch_bwd_cluster(ba, status, cl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
+    rec.mark();
+    CombineJobs jobs{};
+    jobs.n = 2;
+    jobs.j[0] = da_jobs.j[0];
+    jobs.j[1] = db_jobs.j[0];
+    if (launch_combine(jobs, st) != cudaSuccess) return LORA_ERR_CUDA;
+    rec.mark();
+    return LORA_OK;
+  }
   if (RP == 16) {
     // one pass over dY: dU partials over 512-column slices, dB partials over 256-row chunks
     if (launch_dy(yargs, status, grid_for(n_dy, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
@@ -675,6 +780,14 @@ lora_status lora_delta_device_status(const void* workspace, int* code) {
   *code = int(v);
   return v == 0 ? LORA_OK : LORA_ERR_TIMEOUT;
 }
+
+lora_status lora_delta_set_cluster_size(int cl) {
+  if (cl != -1 && cl != 0 && cl != 2 && cl != 4 && cl != 8) return LORA_ERR_SHAPE;   // the setting stays
+  g_cluster = cl;
+  return LORA_OK;
+}
+
+int lora_delta_cluster_size(void) { return g_cluster; }
 
 lora_status lora_delta_set_profile_events(void* const* events, int count) {
   if (count < 0 || count > 64) return LORA_ERR_SHAPE;

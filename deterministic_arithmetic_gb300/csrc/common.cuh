@@ -11,11 +11,14 @@
 namespace lora {
 
 // ----------------------------------------------------------------- limits
-// A wait on an mbarrier gives up after this long (ns of %globaltimer). The
-// kernels finish in micro- to milliseconds; reaching the limit means the
-// pipeline is broken, and the kernel reports it instead of hanging the GPU.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
-constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s, for teardown waits
+// A wait on an mbarrier gives up after this long (ns of %globaltimer). Every
+// wait covers one pipeline stage (or, in the cluster kernels, one peer's share
+// of a tile, bounded on the host); the kernels finish in micro- to
+// milliseconds, so reaching the limit means the pipeline is broken, and the
+// kernel reports it and returns within a fraction of a second instead of
+// holding the GPU.
+constexpr uint64_t kWaitLimitNs = 100000000ull;    // 0.1 s
+constexpr uint64_t kDrainLimitNs = 20000000ull;    // 0.02 s, for teardown waits
 
 // Status block (the first bytes of the caller's workspace), 32-bit words:
 //   word 0  status code, written by a kernel that gives up on a wait: (site << 8) | kDevTimeout;
@@ -127,6 +130,76 @@ struct Ring {
     if (++idx == N) { idx = 0; phase ^= 1u; }
   }
 };
+
+// ---------------------------------------------------------- thread-block clusters
+// A cluster's CTAs run at the same time (the hardware schedules them together),
+// so one may wait for another. Peers signal each other through mbarriers in the
+// waiting CTA's shared memory (remote arrive, release at cluster scope; the
+// waiter's try_wait acquires at cluster scope).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders shared and global memory at cluster scope.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of the same shared-memory location in the CTA of the given cluster rank.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of a peer CTA (address from peer_addr), releasing this thread's prior
+// writes -- and those ordered before them by a CTA barrier -- at cluster scope.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0u;
+}
+// Bounded wait for a phase completed by cluster peers (acquire at cluster scope); false: abort.
+static __device__ __noinline__ bool wait_cluster(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*ab.flag) return false;
+      if (global_ns() - t0 > ab.limit_ns) {
+        *ab.flag = 1u;
+        if (ab.status) atomicCAS(ab.status, 0u, (site << 8) | kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
 
 // ------------------------------------------- programmatic dependent launch
 // The kernels are launched with programmatic stream serialization: a kernel may

@@ -152,6 +152,41 @@ cudaError_t launch_fwd_fused(int RP, bool y_bf16, DownArgs& dargs, UpArgs& uargs
                              uint32_t* ctl, int nsm, uint32_t* status, cudaStream_t st);
 cudaError_t prepare_fwd_fused();
 
+// Single-launch forward of one site on thread-block clusters (fwd_cluster.cu), padded ranks 16 and
+// 32: a cluster of cl CTAs owns a 128-row tile at a time, each CTA a share of its K-slices and of
+// its column tiles; the slice partials meet through the workspace, ordered by mbarriers at cluster
+// scope. Column tiles of the expansion are fc_bn(RP) wide.
+constexpr int fc_bn(int RP) { return 128 / (RP / 16); }
+struct FcArgs {
+  CUtensorMap x, a, b, out;   // x boxes 128 x 32 (64-byte swizzle); a RP x 64 (128-byte); b fc_bn x RP (row span); out 32 x 32
+  float* part;                // [S][M][RP] slice partials
+  __nv_bfloat16* u;           // [M][R]
+  int M, K, N, R, S, n_mt, n_nt;   // S, n_mt, n_nt: set by the launcher
+  float alpha;
+};
+cudaError_t launch_fwd_cluster(int RP, bool y_bf16, FcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st);
+// Clusters of cl CTAs of that instance that fit on the device at once.
+cudaError_t fwd_cluster_max_clusters(int RP, bool y_bf16, int cl, int* n);
+cudaError_t prepare_fwd_cluster();
+
+// Backward of one site (padded rank 16) on thread-block clusters (bwd_cluster.cu): a cluster of cl
+// CTAs owns a 256-row chunk at a time; each CTA a share of its 512-column dU slices (phase A: dU
+// and dB partials from one pass over dY), then, after the cluster has met and every CTA holds the
+// chunk's dU rows, a share of its 128-column tiles of K (phase C: dX and the dA chunk partials).
+struct BcArgs {
+  CUtensorMap dy, b, u, x, a, dx;   // dy 128 x 32 (64-byte swizzle); b, u 128 x RP (row span); x 64 x 64 and
+                                    // a RP x 64 (128-byte); dx 32 x 32 FP32 (128-byte)
+  float* du_part;                   // [S][M][RP] dU slice partials
+  float* db_part;                   // [C][RP][N] dB chunk partials
+  float* da_part;                   // [C][RP][K] dA chunk partials
+  __nv_bfloat16* du;                // [M][R]
+  int M, K, N, R, S, n_ch, n_kt;    // S, n_ch, n_kt: set by the launcher
+  float alpha;
+};
+cudaError_t launch_bwd_cluster(BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st);
+cudaError_t bwd_cluster_max_clusters(int cl, int* n);
+cudaError_t prepare_bwd_cluster();
+
 // Final combine of the weight-gradient chunk partials: canonical tree over
 // the C chunks, FP32 out. part is [C][RP][cols] (cols = K for dA, N for dB).
 struct CombineJob {

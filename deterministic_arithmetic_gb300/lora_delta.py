@@ -117,6 +117,10 @@ def _lib() -> ctypes.CDLL:
         lib.lora_delta_device_status.restype = ctypes.c_int
         lib.lora_delta_set_profile_events.argtypes = [ctypes.POINTER(_vp), ctypes.c_int]
         lib.lora_delta_set_profile_events.restype = ctypes.c_int
+        lib.lora_delta_set_cluster_size.argtypes = [ctypes.c_int]
+        lib.lora_delta_set_cluster_size.restype = ctypes.c_int
+        lib.lora_delta_cluster_size.argtypes = []
+        lib.lora_delta_cluster_size.restype = ctypes.c_int
         lib.lora_delta_describe.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.lora_delta_describe.restype = ctypes.c_size_t
         _LIB = lib
@@ -408,6 +412,18 @@ def lora_delta_set_profile_events(events) -> None:
     rc = _lib().lora_delta_set_profile_events(arr, len(events))
     if rc != LORA_OK:
         raise LoraDeltaError(rc, "lora_delta_set_profile_events")
+
+
+def lora_delta_set_cluster_size(cl: int) -> None:
+    """Schedule of the single-site passes: -1 (default) the separate launches, 0 the cluster
+    launches with the default cluster size, 2 / 4 / 8 a forced size. Changes no result bit."""
+    rc = _lib().lora_delta_set_cluster_size(int(cl))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_set_cluster_size")
+
+
+def lora_delta_cluster_size() -> int:
+    return int(_lib().lora_delta_cluster_size())
 
 
 def lora_delta_describe() -> str:

@@ -45,7 +45,7 @@
  *     a workspace serves calls of any shape that fit in it. The status
  *     block's 32-bit words:
  *       word 0  status: a kernel that gives up on an internal wait (every wait
- *               is bounded, 1 s by default) writes (site << 8) | 1 there, unless
+ *               is bounded, 0.1 s by default) writes (site << 8) | 1 there, unless
  *               the word already holds a code (the first failure stays), and
  *               returns; the call's outputs are then undefined. The code stays
  *               until the caller clears the word (read it with
@@ -244,6 +244,25 @@ lora_status lora_delta_device_status(const void *workspace, int *code);
  * owned by the caller.
  */
 lora_status lora_delta_set_profile_events(void *const *events, int count);
+
+/*
+ * Schedule selection (process-wide; not thread-safe; no effect on any result
+ * bit). Besides its separate launches (forward: down-projection, rows,
+ * up-projection; backward: dU + dB pass, rows, dX, dA, combine), the operator
+ * has single-launch schedules on thread-block clusters: the single-site
+ * forward of padded rank 16 or 32 (R <= 32) as one launch, a cluster of `cl`
+ * CTAs sharing each 128-row tile; the single-site backward of R <= 16 as one
+ * launch (a cluster per 256-row chunk) plus the combine launch of the weight
+ * gradients. Shapes whose per-CTA share of a tile exceeds 32 MiB of input keep
+ * the separate launches. cl = -1 (the default) selects the separate launches,
+ * the faster schedule on a GB300 at the measured training and MLP shapes;
+ * cl = 0 the cluster launches with the default size (4); 2, 4 or 8 force the
+ * size. Outputs are bit for bit the same in every setting (same leaves, trees
+ * and rounding points). Returns LORA_ERR_SHAPE for any other value, leaving
+ * the setting unchanged. lora_delta_cluster_size returns the current setting.
+ */
+lora_status lora_delta_set_cluster_size(int cl);
+int lora_delta_cluster_size(void);
 
 /*
  * Writes a NUL-terminated JSON description of the numerics and tiling

@@ -54,8 +54,19 @@ def _step(t, alpha, wf, wb):
     return dict(y=y, u=u, dx=dx, da=da, db=db, du=du)
 
 
+@pytest.fixture(params=[-1, 0], ids=["separate", "cluster"])
+def schedule(request):
+    """Both schedules of the passes: the separate launches (default) and the cluster launches
+    (forward R <= 32, backward R <= 16), whose producers honour the same stall hooks and sites."""
+    from deterministic_arithmetic_gb300 import lora_delta as ld
+
+    ld.lora_delta_set_cluster_size(request.param)
+    yield request.param
+    ld.lora_delta_set_cluster_size(-1)
+
+
 @pytest.mark.parametrize("kind,where,R,site", CASES)
-def test_a_wait_that_runs_out_is_reported_and_leaves_nothing_behind(kind, where, R, site):
+def test_a_wait_that_runs_out_is_reported_and_leaves_nothing_behind(kind, where, R, site, schedule):
     from deterministic_arithmetic_gb300 import lora_delta as ld
 
     M, K, N, alpha = 640, 1024, 2048, 2.0
@@ -87,7 +98,7 @@ def test_a_wait_that_runs_out_is_reported_and_leaves_nothing_behind(kind, where,
         G.assert_bitwise(k, got[k].view(torch.uint8).cpu().numpy(), ref[k].view(torch.uint8).cpu().numpy())
 
 
-def test_control_block_is_zero_after_every_call():
+def test_control_block_is_zero_after_every_call(schedule):
     """The kernels write status word 0 only, and only on a timeout, and leave the control words
     at zero: after normal calls of several shapes the whole control block is zero."""
     from deterministic_arithmetic_gb300 import lora_delta as ld
