@@ -38,46 +38,47 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 void* g_events[64];
 int g_nevents = 0;
 
-// Cluster size of the single-launch cluster kernels (lora_delta_set_cluster_size): -1 off (the
-// separate launches, the default), 0 automatic, else 2, 4 or 8 CTAs.
-int g_cluster = -1;
+// Schedule of the single-site passes (lora_delta_set_schedule): separate launches, cluster
+// reductions or single cluster launches; cluster size 0 = kDefaultCluster.
+int g_schedule = LORA_SCHEDULE_SEPARATE;
+int g_cluster = 0;
 constexpr int kDefaultCluster = 4;
 // A CTA of a cluster waits for its peers' share of a tile (forward: 128 rows x K / cl of x; backward:
 // 256 rows x N / cl of dY): the cluster launches take shapes whose share is at most this many bytes
 // (about a millisecond of streaming), far inside the kernels' wait limit; larger shapes run the
 // separate launches.
 constexpr int64_t kClusterShareBytes = int64_t(32) << 20;
-// Clusters of each instance that fit on a device at once: [device][RP 16 / 32][bf16 output][log2 cl]
-// (forward) and [device][log2 cl] (backward)
-int g_max_clusters[kMaxDevices][2][2][4];
-int g_max_bwd_clusters[kMaxDevices][4];
+int cluster_of_setting() { return g_cluster > 0 ? g_cluster : kDefaultCluster; }
+int log2_cl(int cl) { return cl == 1 ? 0 : (cl == 2 ? 1 : (cl == 4 ? 2 : 3)); }
+// Clusters of each instance that fit on a device at once: forward [device][RP 16 / 32][bf16 output]
+// [with the expansion][log2 cl], backward [device][with phase C][log2 cl]; 0 = not yet queried.
+int g_max_clusters[kMaxDevices][2][2][2][4];
+int g_max_bwd_clusters[kMaxDevices][2][4];
 
-// Clusters of cl CTAs of the forward cluster kernel for (RP, y_bf16) that fit on the current
-// device at once (queried once per device and instance); 0 when none.
-int fwd_clusters(int RP, bool y_bf16, int cl) {
+// Clusters of cl CTAs of the forward cluster kernel instance that fit on the current device at
+// once (queried once per device and instance); 0 when none.
+int fwd_clusters(int RP, bool y_bf16, bool up, int cl) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  const int li = cl == 1 ? 0 : (cl == 2 ? 1 : (cl == 4 ? 2 : 3));
   std::lock_guard<std::mutex> lock(g_mu);
-  int& v = g_max_clusters[dev][RP == 16 ? 0 : 1][y_bf16 ? 1 : 0][li];
+  int& v = g_max_clusters[dev][RP == 16 ? 0 : 1][(y_bf16 && up) ? 1 : 0][up ? 1 : 0][log2_cl(cl)];
   if (v == 0) {
     int n = 0;
-    if (fwd_cluster_max_clusters(RP, y_bf16, cl, &n) != cudaSuccess || n < 1) return 0;
+    if (fwd_cluster_max_clusters(RP, y_bf16 && up, up, cl, &n) != cudaSuccess || n < 1) return 0;
     v = n;
   }
   return v;
 }
 
 // The same for the backward cluster kernel.
-int bwd_clusters(int cl) {
+int bwd_clusters(bool phase_c, int cl) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  const int li = cl == 1 ? 0 : (cl == 2 ? 1 : (cl == 4 ? 2 : 3));
   std::lock_guard<std::mutex> lock(g_mu);
-  int& v = g_max_bwd_clusters[dev][li];
+  int& v = g_max_bwd_clusters[dev][phase_c ? 1 : 0][log2_cl(cl)];
   if (v == 0) {
     int n = 0;
-    if (bwd_cluster_max_clusters(cl, &n) != cudaSuccess || n < 1) return 0;
+    if (bwd_cluster_max_clusters(phase_c, cl, &n) != cudaSuccess || n < 1) return 0;
     v = n;
   }
   return v;
@@ -353,18 +354,22 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
-  const int fcl = g_cluster > 0 ? g_cluster : kDefaultCluster;
-  if (!fused && m == 1 && RP <= 32 && g_cluster >= 0 && 128 * in[active[0]].K * 2 / fcl <= kClusterShareBytes) {
-    // one launch on clusters: down, rows and up steps per 128-row tile
+  const int fcl = cluster_of_setting();
+  if (!fused && m == 1 && RP <= 32 && g_schedule != LORA_SCHEDULE_SEPARATE &&
+      128 * in[active[0]].K * 2 / fcl <= kClusterShareBytes) {
+    // single: one launch on clusters (down, rows and up steps per 128-row tile); reduce: the
+    // down and rows steps on clusters, then the up-projection launch
+    const bool single = g_schedule == LORA_SCHEDULE_CLUSTER_SINGLE;
     const FwdIn& p = in[active[0]];
-    const int cl = fcl;
-    const int mc = fwd_clusters(RP, y_bf16, cl);
+    const int mc = fwd_clusters(RP, y_bf16, single, fcl);
     if (mc < 1) return LORA_ERR_CUDA;
     FcArgs fa{};
     fa.x = dargs.s[0].in;
     fa.a = dargs.s[0].w;
-    fa.out = uargs.s[0].out;
-    if (!make_map(&fa.b, p.b, false, p.N, R, RP, fc_bn(RP), swizzle_for_span(span))) return LORA_ERR_CUDA;
+    if (single) {
+      fa.out = uargs.s[0].out;
+      if (!make_map(&fa.b, p.b, false, p.N, R, RP, fc_bn(RP), swizzle_for_span(span))) return LORA_ERR_CUDA;
+    }
     fa.part = dargs.s[0].part;
     fa.u = static_cast<__nv_bfloat16*>(p.u);
     fa.M = int(p.M);
@@ -373,8 +378,12 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
     fa.R = int(R);
     fa.alpha = p.alpha;
     const int ncl = int(std::min<int64_t>(mc, ceil_div(p.M, 128)));
-    if (launch_fwd_cluster(RP, y_bf16, fa, status, cl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
+    if (launch_fwd_cluster(RP, y_bf16, single, fa, status, fcl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
+    if (!single) {
+      if (launch_up(RP, false, y_bf16, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+      rec.mark();
+    }
     return LORA_OK;
   }
   if (fused && m == 1 && ceil_div(in[active[0]].M, 128) <= kFusedMaxTiles) {
@@ -486,21 +495,25 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
-  const int bcl = g_cluster > 0 ? g_cluster : kDefaultCluster;
-  if (m == 1 && RP == 16 && g_cluster >= 0 && int64_t(kDyChunk) * in[active[0]].N * 2 / bcl <= kClusterShareBytes) {
-    // one launch on clusters (dU, dB partials; dU rows; dX, dA partials per 256-row chunk), then
-    // the canonical trees over the chunk partials of dA and dB
+  const int bcl = cluster_of_setting();
+  if (m == 1 && RP == 16 && g_schedule != LORA_SCHEDULE_SEPARATE &&
+      int64_t(kDyChunk) * in[active[0]].N * 2 / bcl <= kClusterShareBytes) {
+    // single: one launch on clusters (dU, dB partials; dU rows; dX, dA partials per 256-row chunk);
+    // reduce: the dU, dB partials and dU rows on clusters, then the dX and dA launches. Then the
+    // canonical trees over the chunk partials of dA and dB.
+    const bool single = g_schedule == LORA_SCHEDULE_CLUSTER_SINGLE;
     const BwdIn& p = in[active[0]];
-    const int cl = bcl;
-    const int mc = bwd_clusters(cl);
+    const int mc = bwd_clusters(single, bcl);
     if (mc < 1) return LORA_ERR_CUDA;
     BcArgs ba{};
     ba.dy = yargs.s[0].dy;
     ba.b = yargs.s[0].b;
     ba.u = yargs.s[0].u;
-    ba.x = aargs.s[0].in;
-    ba.a = uargs.s[0].b;
-    ba.dx = uargs.s[0].out;
+    if (single) {
+      ba.x = aargs.s[0].in;
+      ba.a = uargs.s[0].b;
+      ba.dx = uargs.s[0].out;
+    }
     ba.du_part = yargs.s[0].du_part;
     ba.db_part = yargs.s[0].db_part;
     ba.da_part = aargs.s[0].part;
@@ -511,8 +524,14 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     ba.R = int(R);
     ba.alpha = p.alpha;
     const int ncl = int(std::min<int64_t>(mc, ceil_div(p.M, kDyChunk)));
-    if (launch_bwd_cluster(ba, status, cl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
+    if (launch_bwd_cluster(single, ba, status, bcl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
+    if (!single) {
+      if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+      rec.mark();
+      if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
+      rec.mark();
+    }
     CombineJobs jobs{};
     jobs.n = 2;
     jobs.j[0] = da_jobs.j[0];
@@ -781,13 +800,20 @@ lora_status lora_delta_device_status(const void* workspace, int* code) {
   return v == 0 ? LORA_OK : LORA_ERR_TIMEOUT;
 }
 
-lora_status lora_delta_set_cluster_size(int cl) {
-  if (cl != -1 && cl != 0 && cl != 2 && cl != 4 && cl != 8) return LORA_ERR_SHAPE;   // the setting stays
-  g_cluster = cl;
+lora_status lora_delta_set_schedule(int schedule, int cluster_size) {
+  if (schedule != LORA_SCHEDULE_SEPARATE && schedule != LORA_SCHEDULE_CLUSTER_REDUCE &&
+      schedule != LORA_SCHEDULE_CLUSTER_SINGLE)
+    return LORA_ERR_SHAPE;
+  if (cluster_size != 0 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8) return LORA_ERR_SHAPE;
+  g_schedule = schedule;
+  g_cluster = cluster_size;
   return LORA_OK;
 }
 
-int lora_delta_cluster_size(void) { return g_cluster; }
+int lora_delta_schedule(int* cluster_size) {
+  if (cluster_size) *cluster_size = g_cluster;
+  return g_schedule;
+}
 
 lora_status lora_delta_set_profile_events(void* const* events, int count) {
   if (count < 0 || count > 64) return LORA_ERR_SHAPE;

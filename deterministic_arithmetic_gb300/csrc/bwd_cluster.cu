@@ -41,6 +41,7 @@
 
 namespace lora {
 
+template <bool PC>
 struct BcCfg {
   static constexpr int RP = 16;
   static constexpr int kBM = 128;
@@ -52,7 +53,7 @@ struct BcCfg {
   static constexpr int kXBytes = 128 * 128 * 2;            // 32 KB
   static constexpr int kABytes = RP * 128 * 2;             // 4 KB
   static constexpr int kSlotBytes = kTileBytes + 2 * kWBytes;   // 40 KB (phase C uses 36 KB)
-  static constexpr int kSlots = 4;
+  static constexpr int kSlots = PC ? 4 : 5;
   static constexpr int kLeaves = 8;                        // 16-term leaves per 128 of the reduction
   static constexpr int kTCols = 256, kTSlots = 2;          // TMEM ring
   static constexpr int kSliceTiles = kDySlice / 128;       // column tiles per dU slice
@@ -64,7 +65,7 @@ struct BcCfg {
   static constexpr int kDuBytes = 2 * kBM * RP * 2;        // the chunk's 256 dU rows: 8 KB
   static constexpr size_t kDuOff = size_t(kSlots) * kSlotBytes;
   static constexpr size_t kStgOff = kDuOff + kDuBytes;
-  static constexpr size_t kArea = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
+  static constexpr size_t kArea = PC ? kStgOff + size_t(kEpiWarps) * kStg * kStgBytes : kDuOff;
   // mbarriers: slots (full, ready, empty), TMEM (full, empty), dU exchange [2], dU set, drain, never
   static constexpr int kNumBars = 3 * kSlots + 2 * kTSlots + 2 + 1 + 2;
   static constexpr size_t kSmem = kArea + 1024 + kNumBars * 8 + 16;
@@ -92,9 +93,12 @@ __device__ __forceinline__ void bc_leaves4(uint32_t taddr, bool ok, float (&o)[8
     o[c] = tree4(__uint_as_float(v[0][c]), __uint_as_float(v[1][c]), __uint_as_float(v[2][c]), __uint_as_float(v[3][c]));
 }
 
-__global__ void __launch_bounds__(BcCfg::kThreads, 1)
+// PC = false: phase A and the dU rows only (each CTA forms and stores its share of the chunk's
+// rows); dX and the dA partials then run as the separate up-projection and weight-gradient launches.
+template <bool PC>
+__global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
     bwd_cluster_kernel(const __grid_constant__ BcArgs args, uint32_t* status) {
-  using C = BcCfg;
+  using C = BcCfg<PC>;
   constexpr int RP = C::RP;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -116,7 +120,8 @@ __global__ void __launch_bounds__(BcCfg::kThreads, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   const int CL = int(cluster_size()), rank = int(cluster_rank());
   const int cid = int(cluster_index()), ncl = int(cluster_count());
-  const int M = args.M, K = args.K, N = args.N, S = args.S, n_ch = args.n_ch, n_kt = args.n_kt;
+  const int M = args.M, K = args.K, N = args.N, S = args.S, n_ch = args.n_ch;
+  const int n_kt = PC ? args.n_kt : 0;   // phase C column tiles (none without phase C)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(full(s), 1);
@@ -137,9 +142,11 @@ __global__ void __launch_bounds__(BcCfg::kThreads, 1)
     prefetch_map(&args.dy);
     prefetch_map(&args.b);
     prefetch_map(&args.u);
-    prefetch_map(&args.x);
-    prefetch_map(&args.a);
-    prefetch_map(&args.dx);
+    if constexpr (PC) {
+      prefetch_map(&args.x);
+      prefetch_map(&args.a);
+      prefetch_map(&args.dx);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -396,15 +403,17 @@ __global__ void __launch_bounds__(BcCfg::kThreads, 1)
       const bool okx = wait_cluster(duready(k & 1), uint32_t(k >> 1) & 1u, ab, 88);
       // ---- dU rows of the chunk: canonical tree over the slices, BF16, into the swizzled tile
       // (32-byte rows: chunk ^ ((row / 4) % 2)); rank r stores its share of du
-      for (int it = et; it < 2 * C::kBM * (RP / 8); it += 32 * C::kEpiWarps) {
-        const int i = it / (RP / 8), gg = it % (RP / 8);
+      // Without phase C a CTA forms its share only.
+      const int i0 = PC ? 0 : rank * rows_per_rank, ni = PC ? 2 * C::kBM : rows_per_rank;
+      for (int it = et; it < ni * (RP / 8); it += 32 * C::kEpiWarps) {
+        const int i = i0 + it / (RP / 8), gg = it % (RP / 8);
         const int row = ch * kDyChunk + i;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (okx && gg < R / 8 && row < M) {
           v = slices_to_bf16x8(args.du_part + size_t(row) * RP + gg * 8, size_t(M) * RP, S);
           if (i / rows_per_rank == rank) *reinterpret_cast<uint4*>(args.du + size_t(row) * R + gg * 8) = v;
         }
-        *reinterpret_cast<uint4*>(dutile + i * 32 + ((gg ^ ((i >> 2) & 1)) << 4)) = v;
+        if constexpr (PC) *reinterpret_cast<uint4*>(dutile + i * 32 + ((gg ^ ((i >> 2) & 1)) << 4)) = v;
       }
       fence_proxy_async();     // generic writes of the dU tile before the tensor core reads it
       named_bar(1, 32 * C::kEpiWarps);
@@ -527,11 +536,12 @@ __global__ void __launch_bounds__(BcCfg::kThreads, 1)
   }
 }
 
+template <bool PC>
 static cudaLaunchConfig_t bc_config(int cl, int ncl, cudaStream_t st, cudaLaunchAttribute (&attr)[2], int nattr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(ncl * cl));
-  cfg.blockDim = dim3(BcCfg::kThreads);
-  cfg.dynamicSmemBytes = BcCfg::kSmem;
+  cfg.blockDim = dim3(BcCfg<PC>::kThreads);
+  cfg.dynamicSmemBytes = BcCfg<PC>::kSmem;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(cl);
@@ -544,24 +554,36 @@ static cudaLaunchConfig_t bc_config(int cl, int ncl, cudaStream_t st, cudaLaunch
   return cfg;
 }
 
-cudaError_t bwd_cluster_max_clusters(int cl, int* n) {
+cudaError_t bwd_cluster_max_clusters(bool phase_c, int cl, int* n) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = bc_config(cl, 1, nullptr, attr, 1);
-  return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel, &cfg);
+  if (phase_c) {
+    cudaLaunchConfig_t cfg = bc_config<true>(cl, 1, nullptr, attr, 1);
+    return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel<true>, &cfg);
+  }
+  cudaLaunchConfig_t cfg = bc_config<false>(cl, 1, nullptr, attr, 1);
+  return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel<false>, &cfg);
 }
 
-cudaError_t launch_bwd_cluster(BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
+cudaError_t launch_bwd_cluster(bool phase_c, BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
   a.S = int(ceil_div(a.N, kDySlice));
   a.n_ch = int(ceil_div(a.M, kDyChunk));
   a.n_kt = int(ceil_div(a.K, 128));
   if (cl < 1 || cl > 8 || (256 % cl) != 0 || ncl < 1) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = bc_config(cl, ncl, st, attr, 2);
-  return cudaLaunchKernelEx(&cfg, bwd_cluster_kernel, a, status);
+  if (phase_c) {
+    cudaLaunchConfig_t cfg = bc_config<true>(cl, ncl, st, attr, 2);
+    return cudaLaunchKernelEx(&cfg, bwd_cluster_kernel<true>, a, status);
+  }
+  cudaLaunchConfig_t cfg = bc_config<false>(cl, ncl, st, attr, 2);
+  return cudaLaunchKernelEx(&cfg, bwd_cluster_kernel<false>, a, status);
 }
 
 cudaError_t prepare_bwd_cluster() {
-  return cudaFuncSetAttribute(bwd_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(BcCfg::kSmem));
+  const cudaError_t e = cudaFuncSetAttribute(bwd_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(BcCfg<true>::kSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(bwd_cluster_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(BcCfg<false>::kSmem));
 }
 
 }  // namespace lora

@@ -38,7 +38,7 @@
 
 namespace lora {
 
-template <int RP>
+template <int RP, bool UP>
 struct FcCfg {
   static constexpr int kBM = 128, kBK = 64;
   // down-projection stages: X [128][64] as two [128][32] K-slabs + a [RP][64]
@@ -46,7 +46,7 @@ struct FcCfg {
   static constexpr int kSlabBytes = kInBytes / 2;
   static constexpr int kWBytes = RP * kBK * 2;
   static constexpr int kDStageBytes = kInBytes + kWBytes;
-  static constexpr int kDStages = 6;
+  static constexpr int kDStages = UP ? 6 : 10;           // without the expansion: a deeper read ring
   static constexpr int kLeaves = kBK / 16;               // leaves per stage
   static constexpr int kGroupCols = kLeaves * RP;        // TMEM columns per stage
   static constexpr int kGroups = 256 / kGroupCols;       // down TMEM ring in columns [0, 256)
@@ -72,7 +72,7 @@ struct FcCfg {
   static constexpr size_t kUOff = size_t(kDStages) * kDStageBytes;
   static constexpr size_t kBOff = kUOff + kUBytes;
   static constexpr size_t kStgOff = kBOff + size_t(kBStages) * kBBytes;
-  static constexpr size_t kArea = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
+  static constexpr size_t kArea = UP ? kStgOff + size_t(kEpiWarps) * kStg * kStgBytes : kUOff;
   // mbarriers: down ring (full, empty), down TMEM (full, empty), b ring (full, empty),
   // up TMEM (full, empty), U exchange [2], U tile set, drains (down, up), never
   static constexpr int kB0 = 0, kB1 = kB0 + 2 * kDStages, kB2 = kB1 + 2 * kGroups, kB3 = kB2 + 2 * kBStages,
@@ -94,10 +94,12 @@ __device__ __forceinline__ uint32_t utile_offset(int i, int g) {
   else return uint32_t(i * 128 + ((g ^ (i & 7)) << 4));
 }
 
-template <int RP, bool YBF>
-__global__ void __launch_bounds__(FcCfg<RP>::kThreads, 1)
+// UP = false: the down-projection and the U rows only (each CTA forms and stores its share of the
+// tile's rows); the expansion then runs as the separate up-projection launch.
+template <int RP, bool YBF, bool UP>
+__global__ void __launch_bounds__(FcCfg<RP, UP>::kThreads, 1)
     fwd_cluster_kernel(const __grid_constant__ FcArgs args, uint32_t* status) {
-  using C = FcCfg<RP>;
+  using C = FcCfg<RP, UP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -122,7 +124,9 @@ __global__ void __launch_bounds__(FcCfg<RP>::kThreads, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   const int CL = int(cluster_size()), rank = int(cluster_rank());
   const int cid = int(cluster_index()), ncl = int(cluster_count());
-  const int M = args.M, K = args.K, N = args.N, S = args.S, n_mt = args.n_mt, n_nt = args.n_nt;
+  const int M = args.M, K = args.K, N = args.N, S = args.S, n_mt = args.n_mt;
+  // column tiles of the expansion: none without it (its shared memory is then not allocated)
+  const int n_nt = UP ? args.n_nt : 0;
   const bool has_up = rank < n_nt;   // this CTA expands some column tile of every row tile
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kDStages; ++s) {
@@ -151,8 +155,10 @@ __global__ void __launch_bounds__(FcCfg<RP>::kThreads, 1)
     mbar_fence_init();
     prefetch_map(&args.x);
     prefetch_map(&args.a);
-    prefetch_map(&args.b);
-    prefetch_map(&args.out);
+    if constexpr (UP) {
+      prefetch_map(&args.b);
+      prefetch_map(&args.out);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -330,16 +336,18 @@ __global__ void __launch_bounds__(FcCfg<RP>::kThreads, 1)
         for (int p = 0; p < CL; ++p) mbar_arrive_peer(peer_addr(uready(k & 1), uint32_t(p)));
       const bool okx = wait_cluster(uready(k & 1), uint32_t(k >> 1) & 1u, ab, 67);
       // (3) the U rows of the tile: canonical tree over the slices, BF16, into the swizzled U
-      // tile (padded columns and rows past M are zero); rank r also stores its share of u
-      for (int it = et; it < C::kBM * (RP / 8); it += 32 * C::kEpiWarps) {
-        const int i = it / (RP / 8), gg = it % (RP / 8);
+      // tile (padded columns and rows past M are zero); rank r also stores its share of u.
+      // Without the expansion a CTA forms its share only.
+      const int i0 = UP ? 0 : rank * rows_per_rank, ni = UP ? C::kBM : rows_per_rank;
+      for (int it = et; it < ni * (RP / 8); it += 32 * C::kEpiWarps) {
+        const int i = i0 + it / (RP / 8), gg = it % (RP / 8);
         const int row = mt * C::kBM + i;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (okx && gg < R / 8 && row < M) {
           v = slices_to_bf16x8(args.part + size_t(row) * RP + gg * 8, size_t(M) * RP, S);
           if (i / rows_per_rank == rank) *reinterpret_cast<uint4*>(args.u + size_t(row) * R + gg * 8) = v;
         }
-        *reinterpret_cast<uint4*>(utile + utile_offset<RP>(i, gg)) = v;
+        if constexpr (UP) *reinterpret_cast<uint4*>(utile + utile_offset<RP>(i, gg)) = v;
       }
       fence_proxy_async();     // generic writes of the U tile before the tensor core reads it
       named_bar(1, 32 * C::kEpiWarps);
@@ -478,12 +486,12 @@ __global__ void __launch_bounds__(FcCfg<RP>::kThreads, 1)
   }
 }
 
-template <int RP, bool YBF>
+template <int RP, bool YBF, bool UP>
 static cudaError_t launch_inst(const FcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(ncl * cl));
-  cfg.blockDim = dim3(FcCfg<RP>::kThreads);
-  cfg.dynamicSmemBytes = FcCfg<RP>::kSmem;
+  cfg.blockDim = dim3(FcCfg<RP, UP>::kThreads);
+  cfg.dynamicSmemBytes = FcCfg<RP, UP>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -494,15 +502,15 @@ static cudaError_t launch_inst(const FcArgs& a, uint32_t* status, int cl, int nc
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, fwd_cluster_kernel<RP, YBF>, a, status);
+  return cudaLaunchKernelEx(&cfg, fwd_cluster_kernel<RP, YBF, UP>, a, status);
 }
 
-template <int RP, bool YBF>
+template <int RP, bool YBF, bool UP>
 static cudaError_t max_clusters_inst(int cl, int* n) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(cl));
-  cfg.blockDim = dim3(FcCfg<RP>::kThreads);
-  cfg.dynamicSmemBytes = FcCfg<RP>::kSmem;
+  cfg.blockDim = dim3(FcCfg<RP, UP>::kThreads);
+  cfg.dynamicSmemBytes = FcCfg<RP, UP>::kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(cl);
@@ -510,45 +518,56 @@ static cudaError_t max_clusters_inst(int cl, int* n) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, fwd_cluster_kernel<RP, YBF>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, fwd_cluster_kernel<RP, YBF, UP>, &cfg);
 }
 
-cudaError_t fwd_cluster_max_clusters(int RP, bool y_bf16, int cl, int* n) {
-  switch (RP * 2 + (y_bf16 ? 1 : 0)) {
-    case 32: return max_clusters_inst<16, false>(cl, n);
-    case 33: return max_clusters_inst<16, true>(cl, n);
-    case 64: return max_clusters_inst<32, false>(cl, n);
-    case 65: return max_clusters_inst<32, true>(cl, n);
+// Instance code: padded rank, BF16 output, expansion in the launch.
+// (The output type matters only with the expansion.)
+static int fc_code(int RP, bool y_bf16, bool up) { return RP * 4 + (y_bf16 && up ? 1 : 0) + (up ? 2 : 0); }
+
+cudaError_t fwd_cluster_max_clusters(int RP, bool y_bf16, bool up, int cl, int* n) {
+  switch (fc_code(RP, y_bf16, up)) {
+    case 66: return max_clusters_inst<16, false, true>(cl, n);
+    case 67: return max_clusters_inst<16, true, true>(cl, n);
+    case 130: return max_clusters_inst<32, false, true>(cl, n);
+    case 131: return max_clusters_inst<32, true, true>(cl, n);
+    case 64: return max_clusters_inst<16, false, false>(cl, n);
+    case 128: return max_clusters_inst<32, false, false>(cl, n);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_fwd_cluster(int RP, bool y_bf16, FcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
+cudaError_t launch_fwd_cluster(int RP, bool y_bf16, bool up, FcArgs& a, uint32_t* status, int cl, int ncl,
+                               cudaStream_t st) {
   a.S = int(ceil_div(a.K, down_slice(RP)));
   a.n_mt = int(ceil_div(a.M, 128));
   a.n_nt = int(ceil_div(a.N, fc_bn(RP)));
   if (cl < 1 || cl > 8 || (128 % cl) != 0 || ncl < 1) return cudaErrorInvalidValue;
-  switch (RP * 2 + (y_bf16 ? 1 : 0)) {
-    case 32: return launch_inst<16, false>(a, status, cl, ncl, st);
-    case 33: return launch_inst<16, true>(a, status, cl, ncl, st);
-    case 64: return launch_inst<32, false>(a, status, cl, ncl, st);
-    case 65: return launch_inst<32, true>(a, status, cl, ncl, st);
+  switch (fc_code(RP, y_bf16, up)) {
+    case 66: return launch_inst<16, false, true>(a, status, cl, ncl, st);
+    case 67: return launch_inst<16, true, true>(a, status, cl, ncl, st);
+    case 130: return launch_inst<32, false, true>(a, status, cl, ncl, st);
+    case 131: return launch_inst<32, true, true>(a, status, cl, ncl, st);
+    case 64: return launch_inst<16, false, false>(a, status, cl, ncl, st);
+    case 128: return launch_inst<32, false, false>(a, status, cl, ncl, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int RP, bool YBF>
+template <int RP, bool YBF, bool UP>
 static cudaError_t prep_one() {
-  return cudaFuncSetAttribute(fwd_cluster_kernel<RP, YBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(FcCfg<RP>::kSmem));
+  return cudaFuncSetAttribute(fwd_cluster_kernel<RP, YBF, UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(FcCfg<RP, UP>::kSmem));
 }
 
 cudaError_t prepare_fwd_cluster() {
   cudaError_t e;
-  if ((e = prep_one<16, false>()) != cudaSuccess) return e;
-  if ((e = prep_one<16, true>()) != cudaSuccess) return e;
-  if ((e = prep_one<32, false>()) != cudaSuccess) return e;
-  return prep_one<32, true>();
+  if ((e = prep_one<16, false, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<16, true, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, false, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<32, true, true>()) != cudaSuccess) return e;
+  if ((e = prep_one<16, false, false>()) != cudaSuccess) return e;
+  return prep_one<32, false, false>();
 }
 
 }  // namespace lora

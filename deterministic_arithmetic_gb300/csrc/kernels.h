@@ -164,9 +164,12 @@ struct FcArgs {
   int M, K, N, R, S, n_mt, n_nt;   // S, n_mt, n_nt: set by the launcher
   float alpha;
 };
-cudaError_t launch_fwd_cluster(int RP, bool y_bf16, FcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st);
+// up = false: the down-projection and the U rows only (the up-projection launch follows; y_bf16 and
+// the b and out maps are then unused).
+cudaError_t launch_fwd_cluster(int RP, bool y_bf16, bool up, FcArgs& a, uint32_t* status, int cl, int ncl,
+                               cudaStream_t st);
 // Clusters of cl CTAs of that instance that fit on the device at once.
-cudaError_t fwd_cluster_max_clusters(int RP, bool y_bf16, int cl, int* n);
+cudaError_t fwd_cluster_max_clusters(int RP, bool y_bf16, bool up, int cl, int* n);
 cudaError_t prepare_fwd_cluster();
 
 // Backward of one site (padded rank 16) on thread-block clusters (bwd_cluster.cu): a cluster of cl
@@ -183,8 +186,10 @@ struct BcArgs {
   int M, K, N, R, S, n_ch, n_kt;    // S, n_ch, n_kt: set by the launcher
   float alpha;
 };
-cudaError_t launch_bwd_cluster(BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st);
-cudaError_t bwd_cluster_max_clusters(int cl, int* n);
+// phase_c = false: phase A and the dU rows only (the dX, dA and combine launches follow; the x, a
+// and dx maps are then unused).
+cudaError_t launch_bwd_cluster(bool phase_c, BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st);
+cudaError_t bwd_cluster_max_clusters(bool phase_c, int cl, int* n);
 cudaError_t prepare_bwd_cluster();
 
 // Final combine of the weight-gradient chunk partials: canonical tree over

@@ -117,10 +117,10 @@ def _lib() -> ctypes.CDLL:
         lib.lora_delta_device_status.restype = ctypes.c_int
         lib.lora_delta_set_profile_events.argtypes = [ctypes.POINTER(_vp), ctypes.c_int]
         lib.lora_delta_set_profile_events.restype = ctypes.c_int
-        lib.lora_delta_set_cluster_size.argtypes = [ctypes.c_int]
-        lib.lora_delta_set_cluster_size.restype = ctypes.c_int
-        lib.lora_delta_cluster_size.argtypes = []
-        lib.lora_delta_cluster_size.restype = ctypes.c_int
+        lib.lora_delta_set_schedule.argtypes = [ctypes.c_int, ctypes.c_int]
+        lib.lora_delta_set_schedule.restype = ctypes.c_int
+        lib.lora_delta_schedule.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.lora_delta_schedule.restype = ctypes.c_int
         lib.lora_delta_describe.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.lora_delta_describe.restype = ctypes.c_size_t
         _LIB = lib
@@ -414,16 +414,21 @@ def lora_delta_set_profile_events(events) -> None:
         raise LoraDeltaError(rc, "lora_delta_set_profile_events")
 
 
-def lora_delta_set_cluster_size(cl: int) -> None:
-    """Schedule of the single-site passes: -1 (default) the separate launches, 0 the cluster
-    launches with the default cluster size, 2 / 4 / 8 a forced size. Changes no result bit."""
-    rc = _lib().lora_delta_set_cluster_size(int(cl))
+SCHEDULE_SEPARATE, SCHEDULE_CLUSTER_REDUCE, SCHEDULE_CLUSTER_SINGLE = 0, 1, 2
+
+
+def lora_delta_set_schedule(schedule: int, cluster_size: int = 0) -> None:
+    """Launch schedule of the single-site passes (``SCHEDULE_*``) and the cluster size of the
+    cluster schedules (0: the default). Changes no result bit."""
+    rc = _lib().lora_delta_set_schedule(int(schedule), int(cluster_size))
     if rc != LORA_OK:
-        raise LoraDeltaError(rc, "lora_delta_set_cluster_size")
+        raise LoraDeltaError(rc, "lora_delta_set_schedule")
 
 
-def lora_delta_cluster_size() -> int:
-    return int(_lib().lora_delta_cluster_size())
+def lora_delta_schedule() -> tuple[int, int]:
+    """(schedule, cluster size setting)."""
+    cl = ctypes.c_int(0)
+    return int(_lib().lora_delta_schedule(ctypes.byref(cl))), int(cl.value)
 
 
 def lora_delta_describe() -> str:

@@ -246,23 +246,37 @@ lora_status lora_delta_device_status(const void *workspace, int *code);
 lora_status lora_delta_set_profile_events(void *const *events, int count);
 
 /*
- * Schedule selection (process-wide; not thread-safe; no effect on any result
- * bit). Besides its separate launches (forward: down-projection, rows,
- * up-projection; backward: dU + dB pass, rows, dX, dA, combine), the operator
- * has single-launch schedules on thread-block clusters: the single-site
- * forward of padded rank 16 or 32 (R <= 32) as one launch, a cluster of `cl`
- * CTAs sharing each 128-row tile; the single-site backward of R <= 16 as one
- * launch (a cluster per 256-row chunk) plus the combine launch of the weight
- * gradients. Shapes whose per-CTA share of a tile exceeds 32 MiB of input keep
- * the separate launches. cl = -1 (the default) selects the separate launches,
- * the faster schedule on a GB300 at the measured training and MLP shapes;
- * cl = 0 the cluster launches with the default size (4); 2, 4 or 8 force the
- * size. Outputs are bit for bit the same in every setting (same leaves, trees
- * and rounding points). Returns LORA_ERR_SHAPE for any other value, leaving
- * the setting unchanged. lora_delta_cluster_size returns the current setting.
+ * Schedule of the single-site passes (process-wide; not thread-safe; no
+ * effect on any result bit -- every schedule runs the same leaves, trees and
+ * rounding points). The operator's steps can be grouped into launches three
+ * ways:
+ *   LORA_SCHEDULE_SEPARATE (default): forward down-projection, rows,
+ *     up-projection; backward dU + dB pass, rows (with the dB tree), dX, dA,
+ *     combine.
+ *   LORA_SCHEDULE_CLUSTER_REDUCE: the reductions that feed a BF16 row on
+ *     thread-block clusters -- a cluster of `cluster_size` CTAs shares each
+ *     128-row tile (forward: U partials and the U rows) or 256-row chunk
+ *     (backward, R <= 16: the dU + dB pass and the dU rows), the CTAs meeting
+ *     at mbarriers in each other's shared memory instead of at a launch
+ *     boundary -- then the expansions and dA as separate launches and one
+ *     combine launch for dA and dB.
+ *   LORA_SCHEDULE_CLUSTER_SINGLE: the forward in one cluster launch (each CTA
+ *     also expands its share of the tile's columns of delta_y); the backward
+ *     (R <= 16) in one cluster launch (each CTA also writes its share of dX and
+ *     the dA chunk partials) and the combine launch.
+ * The cluster schedules cover the single-site forward of R <= 32 and the
+ * single-site backward of R <= 16 whose per-CTA share of a tile is at most
+ * 32 MiB of input; other calls run the separate launches. cluster_size is 0
+ * (the default size, 4 CTAs), 2, 4 or 8. Returns LORA_ERR_SHAPE, leaving the
+ * setting unchanged, for any other value. lora_delta_schedule returns the
+ * current schedule and stores the cluster size setting in *cluster_size (if
+ * not NULL).
  */
-lora_status lora_delta_set_cluster_size(int cl);
-int lora_delta_cluster_size(void);
+#define LORA_SCHEDULE_SEPARATE 0
+#define LORA_SCHEDULE_CLUSTER_REDUCE 1
+#define LORA_SCHEDULE_CLUSTER_SINGLE 2
+lora_status lora_delta_set_schedule(int schedule, int cluster_size);
+int lora_delta_schedule(int *cluster_size);
 
 /*
  * Writes a NUL-terminated JSON description of the numerics and tiling

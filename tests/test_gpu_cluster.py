@@ -1,12 +1,15 @@
-"""The single-launch schedules on thread-block clusters (lora_delta_set_cluster_size)
-against the separate launches: the same leaves, trees and rounding points, so
-every output of the forward (U, dY_lora) and of the backward (dU, dX, dA, dB)
-must agree bit for bit, whatever the cluster size. The cluster's CTAs exchange
+"""The schedules on thread-block clusters (lora_delta_set_schedule: the cluster
+reductions, and the single cluster launches) against the separate launches: the
+same leaves, trees and rounding points, so every output of the forward (U,
+dY_lora) and of the backward (dU, dX, dA, dB) must agree bit for bit, whatever
+the schedule and the cluster size. The cluster's CTAs exchange
 slice partials through the workspace and meet at mbarriers in each other's
 shared memory; the control block must be untouched afterwards. The separate
 launches, the default schedule, are checked against the oracle in
 test_gpu_parity.py; the stall hooks of the cluster backward are exercised by
 test_gpu_failure.py with the cluster launches selected."""
+import contextlib
+
 import numpy as np
 import pytest
 
@@ -19,6 +22,18 @@ import gpu_util as G  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 CONTROL = 256 + 65536      # LORA_DELTA_CONTROL_BYTES
+SEP, RED, ONE = ld.SCHEDULE_SEPARATE, ld.SCHEDULE_CLUSTER_REDUCE, ld.SCHEDULE_CLUSTER_SINGLE
+# (schedule, cluster size) pairs compared with the separate launches
+VARIANTS = [(RED, 2), (RED, 4), (RED, 8), (ONE, 2), (ONE, 4), (ONE, 8)]
+
+
+@contextlib.contextmanager
+def schedule(sched, cl=0):
+    ld.lora_delta_set_schedule(sched, cl)
+    try:
+        yield
+    finally:
+        ld.lora_delta_set_schedule(SEP, 0)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,7 +44,7 @@ def _built():
 
     build_lib.build()
     yield
-    ld.lora_delta_set_cluster_size(-1)
+    ld.lora_delta_set_schedule(SEP, 0)
 
 
 def _inputs(M, K, N, R, alpha, seed):
@@ -38,18 +53,15 @@ def _inputs(M, K, N, R, alpha, seed):
     return {k: G.dev_bf16(v) for k, v in d.items()}
 
 
-def _fwd(t, alpha, cl, y_dtype=torch.float32, ws=None):
+def _fwd(t, alpha, sv, y_dtype=torch.float32, ws=None):
     M, K = t["x"].shape
     N, R = t["b"].shape
     ws = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), "cuda") if ws is None else ws
     y = torch.full((M, N), float("nan"), dtype=y_dtype, device="cuda")
     u = torch.full((M, R), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ld.lora_delta_set_cluster_size(cl)
-    try:
+    with schedule(*sv):
         y, u = ld.lora_delta_fwd(t["x"], t["a"], t["b"], alpha, delta_y=y, u=u, workspace=ws)   # BF16 y: _bf16
         torch.cuda.synchronize()
-    finally:
-        ld.lora_delta_set_cluster_size(-1)
     assert ld.lora_delta_device_status(ws) == 0
     assert not ws[:CONTROL].any().item(), "control block not at zero"
     return y, u
@@ -72,17 +84,17 @@ SHAPES = [  # (M, K, N, R, alpha): padded ranks 16 and 32, ragged M / K / N, one
 @pytest.mark.parametrize("M,K,N,R,alpha", SHAPES)
 def test_cluster_forward_equals_the_separate_launches(M, K, N, R, alpha):
     t = _inputs(M, K, N, R, alpha, 21)
-    ref = _fwd(t, alpha, -1)
-    for cl in (2, 4, 8):
-        _same(f"M{M} K{K} N{N} R{R} cluster {cl}", ref, _fwd(t, alpha, cl))
+    ref = _fwd(t, alpha, (SEP, 0))
+    for sv in VARIANTS:
+        _same(f"M{M} K{K} N{N} R{R} schedule {sv}", ref, _fwd(t, alpha, sv))
 
 
 @pytest.mark.parametrize("M,K,N,R,alpha", [(300, 1032, 520, 16, 2.0), (129, 512, 264, 32, 0.5)])
 def test_cluster_forward_bf16_output(M, K, N, R, alpha):
     t = _inputs(M, K, N, R, alpha, 22)
-    ref = _fwd(t, alpha, -1, torch.bfloat16)
-    for cl in (2, 4):
-        _same(f"bf16 output, cluster {cl}", ref, _fwd(t, alpha, cl, torch.bfloat16))
+    ref = _fwd(t, alpha, (SEP, 0), torch.bfloat16)
+    for sv in ((RED, 4), (ONE, 2), (ONE, 4)):
+        _same(f"bf16 output, schedule {sv}", ref, _fwd(t, alpha, sv, torch.bfloat16))
 
 
 def test_cluster_forward_training_shape_and_workspace_reuse():
@@ -92,19 +104,18 @@ def test_cluster_forward_training_shape_and_workspace_reuse():
     ws = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), "cuda")
     for m in (M, 1, 4097, 128, M):
         tm = dict(t, x=t["x"][:m])
-        _same(f"rows {m}", _fwd(tm, alpha, -1), _fwd(tm, alpha, 0, ws=ws))
+        ref = _fwd(tm, alpha, (SEP, 0))
+        for sv in ((RED, 0), (ONE, 0)):
+            _same(f"rows {m} schedule {sv}", ref, _fwd(tm, alpha, sv, ws=ws))
 
 
 def test_cluster_forward_reruns_and_empty_batch():
     t = _inputs(513, 1024, 520, 32, 2.0, 24)
     ws = ld.new_workspace(ld.lora_delta_fwd_workspace_size(513, 1024, 520, 32), "cuda")
-    ld.lora_delta_set_cluster_size(0)
-    try:
+    with schedule(ONE):
         outs = [ld.lora_delta_fwd(t["x"], t["a"], t["b"], 2.0, workspace=ws) for _ in range(3)]
         torch.cuda.synchronize()
         y0, u0 = ld.lora_delta_fwd(t["x"][:0], t["a"], t["b"], 2.0, workspace=ws)
-    finally:
-        ld.lora_delta_set_cluster_size(-1)
     for y, u in outs[1:]:
         G.assert_bitwise("rerun delta_y", y.cpu().numpy(), outs[0][0].cpu().numpy())
         G.assert_bitwise("rerun u", G.host_bits(u), G.host_bits(outs[0][1]))
@@ -112,16 +123,20 @@ def test_cluster_forward_reruns_and_empty_batch():
     assert not ws[:CONTROL].any().item()
 
 
-def test_cluster_size_setting():
-    assert ld.lora_delta_cluster_size() == -1      # the separate launches by default
-    for bad in (1, 3, 16, -2):
+def test_schedule_setting():
+    assert ld.lora_delta_schedule() == (SEP, 0)      # the separate launches by default
+    for bad in ((3, 0), (-1, 0), (RED, 1), (ONE, 3), (ONE, 16)):
         with pytest.raises(ld.LoraDeltaError):
-            ld.lora_delta_set_cluster_size(bad)
-    assert ld.lora_delta_cluster_size() == -1
+            ld.lora_delta_set_schedule(*bad)
+    assert ld.lora_delta_schedule() == (SEP, 0)
+    with schedule(RED, 8):
+        assert ld.lora_delta_schedule() == (RED, 8)
+    assert ld.lora_delta_schedule() == (SEP, 0)
 
 
+@pytest.mark.parametrize("sched", [RED, ONE])
 @pytest.mark.parametrize("kind,site", [(1, 9), (2, 10)])
-def test_cluster_forward_wait_that_runs_out(kind, site):
+def test_cluster_forward_wait_that_runs_out(kind, site, sched):
     """The stall test hook (status word 2): the X / A producer (kind 1) or the b producer (kind 2)
     waits on a barrier that nothing completes; the wait runs out, the status names the site, the
     peers' waits for the stalled CTA give up too, every CTA leaves, and the next call on the same
@@ -132,19 +147,16 @@ def test_cluster_forward_wait_that_runs_out(kind, site):
     words = ws.view(torch.int32)
     words[2] = kind
     words[3] = 1000
-    ld.lora_delta_set_cluster_size(0)
-    try:
+    with schedule(sched):
         ld.lora_delta_fwd(t["x"], t["a"], t["b"], 2.0, workspace=ws)
         torch.cuda.synchronize()
-    finally:
-        ld.lora_delta_set_cluster_size(-1)
     assert ld.lora_delta_device_status(ws) == (site << 8) | 1
     assert not ws[16:CONTROL].any().item()
     assert torch.ones(4, device="cuda").sum().item() == 4.0    # the context is still usable
     words[0] = 0
     words[2] = 0
     words[3] = 0
-    _same("after a timeout", _fwd(t, 2.0, -1), _fwd(t, 2.0, 0, ws=ws))
+    _same("after a timeout", _fwd(t, 2.0, (SEP, 0)), _fwd(t, 2.0, (sched, 0), ws=ws))
     assert np.array_equal(ws[:CONTROL].cpu().numpy(), np.zeros(CONTROL, np.uint8))
 
 
@@ -158,19 +170,16 @@ def _bwd_inputs(M, K, N, R, alpha, seed):
     return t
 
 
-def _bwd(t, alpha, cl, ws=None):
+def _bwd(t, alpha, sv, ws=None):
     M, K = t["x"].shape
     N, R = t["b"].shape
     ws = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), "cuda") if ws is None else ws
     outs = dict(dx=torch.full((M, K), float("nan"), device="cuda"), da=torch.full((R, K), float("nan"), device="cuda"),
                 db=torch.full((N, R), float("nan"), device="cuda"),
                 du=torch.full((M, R), float("nan"), dtype=torch.bfloat16, device="cuda"))
-    ld.lora_delta_set_cluster_size(cl)
-    try:
+    with schedule(*sv):
         dx, da, db, du = ld.lora_delta_bwd(t["dy"], t["x"], t["a"], t["b"], t["u"], alpha, workspace=ws, **outs)
         torch.cuda.synchronize()
-    finally:
-        ld.lora_delta_set_cluster_size(-1)
     assert ld.lora_delta_device_status(ws) == 0
     assert not ws[:CONTROL].any().item(), "control block not at zero"
     return dict(dx=dx, da=da, db=db, du=du)
@@ -193,9 +202,9 @@ BWD_SHAPES = [  # (M, K, N, R, alpha): R 8 and 16, ragged M / K / N, one row, ch
 @pytest.mark.parametrize("M,K,N,R,alpha", BWD_SHAPES)
 def test_cluster_backward_equals_the_separate_launches(M, K, N, R, alpha):
     t = _bwd_inputs(M, K, N, R, alpha, 31)
-    ref = _bwd(t, alpha, -1)
-    for cl in (2, 4, 8):
-        _same_bwd(f"M{M} K{K} N{N} R{R} cluster {cl}", ref, _bwd(t, alpha, cl))
+    ref = _bwd(t, alpha, (SEP, 0))
+    for sv in VARIANTS:
+        _same_bwd(f"M{M} K{K} N{N} R{R} schedule {sv}", ref, _bwd(t, alpha, sv))
 
 
 def test_cluster_backward_training_shape_and_workspace_reuse():
@@ -204,12 +213,15 @@ def test_cluster_backward_training_shape_and_workspace_reuse():
     ws = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), "cuda")
     for m in (M, 1, 4097, 256, M):
         tm = dict(t, x=t["x"][:m], dy=t["dy"][:m], u=t["u"][:m])
-        _same_bwd(f"rows {m}", _bwd(tm, alpha, -1), _bwd(tm, alpha, 0, ws=ws))
+        ref = _bwd(tm, alpha, (SEP, 0))
+        for sv in ((RED, 0), (ONE, 0)):
+            _same_bwd(f"rows {m} schedule {sv}", ref, _bwd(tm, alpha, sv, ws=ws))
 
 
 def test_cluster_backward_reruns():
     t = _bwd_inputs(1500, 2048, 1032, 16, 2.0, 33)
     ws = ld.new_workspace(ld.lora_delta_bwd_workspace_size(1500, 2048, 1032, 16), "cuda")
-    ref = _bwd(t, 2.0, 0, ws=ws)
-    for _ in range(2):
-        _same_bwd("rerun", ref, _bwd(t, 2.0, 0, ws=ws))
+    for sv in ((RED, 0), (ONE, 0)):
+        ref = _bwd(t, 2.0, sv, ws=ws)
+        for _ in range(2):
+            _same_bwd(f"rerun {sv}", ref, _bwd(t, 2.0, sv, ws=ws))

@@ -54,15 +54,16 @@ def _step(t, alpha, wf, wb):
     return dict(y=y, u=u, dx=dx, da=da, db=db, du=du)
 
 
-@pytest.fixture(params=[-1, 0], ids=["separate", "cluster"])
+@pytest.fixture(params=[0, 1, 2], ids=["separate", "cluster-reduce", "cluster-single"])
 def schedule(request):
-    """Both schedules of the passes: the separate launches (default) and the cluster launches
-    (forward R <= 32, backward R <= 16), whose producers honour the same stall hooks and sites."""
+    """Every schedule of the passes: the separate launches (default), the cluster reductions and
+    the single cluster launches (forward R <= 32, backward R <= 16), whose producers honour the same
+    stall hooks and sites."""
     from deterministic_arithmetic_gb300 import lora_delta as ld
 
-    ld.lora_delta_set_cluster_size(request.param)
+    ld.lora_delta_set_schedule(request.param, 0)
     yield request.param
-    ld.lora_delta_set_cluster_size(-1)
+    ld.lora_delta_set_schedule(0, 0)
 
 
 @pytest.mark.parametrize("kind,where,R,site", CASES)
