@@ -95,14 +95,14 @@ def measured_peaks():
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
 NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
-    "down U": {"bytes": 71_010_000, "src_hash": "bc88ce45787982e6"},
-    "rows U": {"bytes": 30_000, "src_hash": "bc88ce45787982e6"},
-    "up dY_lora": {"bytes": 125_210_000, "src_hash": "bc88ce45787982e6"},
-    "dy dU+dB": {"bytes": 80_690_000, "src_hash": "bc88ce45787982e6"},
-    "rows dU+dB": {"bytes": 1_220_000, "src_hash": "bc88ce45787982e6"},
-    "up dX": {"bytes": 126_520_000, "src_hash": "bc88ce45787982e6"},
-    "wgrad dA": {"bytes": 75_200_000, "src_hash": "bc88ce45787982e6"},
-    "combine dA": {"bytes": 430_000, "src_hash": "bc88ce45787982e6"},
+    "down U": {"bytes": 71_033_856, "src_hash": "6d8d371c39fb4fa4"},
+    "rows U": {"bytes": 26_112, "src_hash": "6d8d371c39fb4fa4"},
+    "up dY_lora": {"bytes": 125_373_696, "src_hash": "6d8d371c39fb4fa4"},
+    "dy dU+dB": {"bytes": 80_710_144, "src_hash": "6d8d371c39fb4fa4"},
+    "rows dU+dB": {"bytes": 1_117_184, "src_hash": "6d8d371c39fb4fa4"},
+    "up dX": {"bytes": 126_388_992, "src_hash": "6d8d371c39fb4fa4"},
+    "wgrad dA": {"bytes": 75_143_936, "src_hash": "6d8d371c39fb4fa4"},
+    "combine dA": {"bytes": 508_672, "src_hash": "6d8d371c39fb4fa4"},
 }
 
 
@@ -342,6 +342,109 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, peak, steps=40, reps=25):
             out[name]["kernel_event_ms"] = round(k_ms, 5)
             out[name]["kernel_frac"] = round(nbytes / (k_ms * 1e-3) / 1e9 / peak, 4)
         assert ld.lora_delta_device_status(wf) == 0
+    return out
+
+
+# Launch schedules of lora_delta_set_schedule measured beside the default separate launches:
+# (name, schedule, cluster size, forward kernels, backward kernels)
+SCHEDULES = [
+    ("cluster_reduce_cl4", 1, 4, ["down+rows U (cluster)", "up dY_lora"],
+     ["dy dU+dB+rows dU (cluster)", "up dX", "wgrad dA", "combine dA+dB"]),
+    ("cluster_single_cl2", 2, 2, ["fwd (cluster)"], ["bwd (cluster)", "combine dA+dB"]),
+    ("cluster_single_cl4", 2, 4, ["fwd (cluster)"], ["bwd (cluster)", "combine dA+dB"]),
+]
+
+
+def schedule_kernels(schedule, M, K, N, R):
+    """Kernel names of one step under a launch schedule (forward's, then backward's) and the
+    algorithmic bytes each moves."""
+    alg = algorithmic_bytes(M, K, N, R)
+    kb = dict(alg)
+    kb.update({"down+rows U (cluster)": alg["down U"] + alg["rows U"],
+               "dy dU+dB+rows dU (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"], "combine dA+dB": 0,
+               "fwd (cluster)": alg["down U"] + alg["rows U"] + alg["up dY_lora"],
+               "bwd (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"] + alg["up dX"] + alg["wgrad dA"]})
+    if schedule == 0:
+        return KERNELS_FWD, KERNELS_BWD, kb
+    for _, sched, _, kf, kbw in SCHEDULES:
+        if sched == schedule:
+            return kf, kbw, kb
+    raise ValueError(schedule)
+
+
+def schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, peak, steps=24, reps=10):
+    """The training step under each cluster schedule (lora_delta_set_schedule): graph-replayed and
+    eager step times like the main measurement, and the per-kernel CUDA-event pass with each
+    kernel's fraction of the measured copy peak. Every schedule gives the same output bits (tested);
+    the default stays the separate launches."""
+    import torch
+
+    _, _, kb = schedule_kernels(0, M, K, N, R)
+    total = step_bytes(M, K, N, R)
+    Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    DX = torch.empty((M, K), dtype=torch.float32, device=dev)
+    DA = torch.empty((R, K), dtype=torch.float32, device=dev)
+    DB = torch.empty((N, R), dtype=torch.float32, device=dev)
+    DU = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
+    wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+
+    def fwd(i, st=None):
+        ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf, stream=st or stream)
+
+    def bwd(i, st=None):
+        ld.lora_delta_bwd(DYs[i % N_ROTATE], Xs[i % N_ROTATE], A, B, U, alpha, dx=DX, da=DA, db=DB, du=DU,
+                          workspace=wb, stream=st or stream)
+
+    for name, sched, cl, kf, kbw in SCHEDULES:
+        ld.lora_delta_set_schedule(sched, cl)
+        try:
+            for i in range(5):
+                fwd(i)
+                bwd(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps * reps // 4):
+                fwd(i)
+                bwd(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            eager_ms = e0.elapsed_time(e1) / (steps * reps // 4)
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    gst = torch.cuda.current_stream(dev)
+                    for i in range(steps):
+                        fwd(i, gst)
+                        bwd(i, gst)
+            stream.wait_stream(cap)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            graph_ms = e0.elapsed_time(e1) / (reps * steps)
+            del graph
+            kavg = kernel_event_pass(ld, kf + kbw, len(kf), PROF_STEPS, stream, fwd, bwd)
+            assert ld.lora_delta_device_status(wf) == 0 and ld.lora_delta_device_status(wb) == 0
+        finally:
+            ld.lora_delta_set_schedule(0, 0)
+        out[f"schedule_{name}"] = {
+            "launches_per_step": len(kf) + len(kbw),
+            "ms_per_step": round(eager_ms, 5), "graph_ms_per_step": round(graph_ms, 5),
+            "gbs": round(total / (eager_ms * 1e-3) / 1e9, 1),
+            "kernels": {k: {"ms": round(kavg[k], 5), "algorithmic_bytes": kb[k],
+                            "frac": round(kb[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if kb[k] else None}
+                        for k in kf + kbw},
+        }
     return out
 
 
@@ -659,6 +762,9 @@ def run_ours(args, world, rank, local):
     wf = ld.new_workspace(ld.lora_delta_fwd_workspace_size(M, K, N, R), dev)
     wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
     stream = torch.cuda.current_stream(dev)
+    ld.lora_delta_set_schedule(args.schedule, args.cluster)
+    kf_names, kb_names, kbytes = schedule_kernels(args.schedule, M, K, N, R)
+    knames = kf_names + kb_names
 
     def step(i):
         x, dy = Xs[i % N_ROTATE], DYs[i % N_ROTATE]
@@ -716,12 +822,12 @@ def run_ours(args, world, rank, local):
 
     # Untimed: per-kernel CUDA events (a mark before the first kernel of each call and after each
     # kernel). The events sit between the kernels, so each figure includes its launch boundary.
-    kavg = kernel_event_pass(ld, KERNELS, N_FWD, PROF_STEPS, stream,
+    kavg = kernel_event_pass(ld, knames, len(kf_names), PROF_STEPS, stream,
                              lambda i: ld.lora_delta_fwd(Xs[i % N_ROTATE], A, B, alpha, delta_y=Y, u=U, workspace=wf,
                                                          stream=stream),
                              lambda i: ld.lora_delta_bwd(DYs[i % N_ROTATE], Xs[i % N_ROTATE], A, B, U, alpha, dx=DX,
                                                          da=DA, db=DB, du=DU, workspace=wb, stream=stream))
-    alg = algorithmic_bytes(M, K, N, R)
+    alg = kbytes
     total_bytes = step_bytes(M, K, N, R)
     peak, peak_kind = measured_peaks()
     value = total_bytes * world / (ms_step * 1e-3) / 1e9
@@ -738,11 +844,14 @@ def run_ours(args, world, rank, local):
     # ---------------------------------------- forward variants (FP32 / BF16 dY_lora)
     variants = None
     if not args.no_variants:
+        ld.lora_delta_set_schedule(0, 0)   # the variants choose their own schedules
         variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, measured_peaks()[0])
         variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
+        variants.update(schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, measured_peaks()[0]))
         variants.update(grouped_variants(ld, dev, measured_peaks()[0]))
         variants.update(exact_variant(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(decode_variants(ld, dev))
+        ld.lora_delta_set_schedule(args.schedule, args.cluster)
 
     # ----------------------------------------------------------- end to end
     e2e = None
@@ -834,7 +943,10 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, BF16)",
-            "config": {"workload": f"LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, {len(KERNELS)} kernels)",
+            "config": {"workload": f"LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, {len(knames)} kernels)",
+                       "schedule": {0: "separate launches", 1: "cluster reductions",
+                                    2: "single cluster launches"}[args.schedule]
+                                   + (f", clusters of {args.cluster or 4}" if args.schedule else ""),
                        "M": M, "K": K, "N": N, "R": R, "alpha": alpha, "accumulate": "fp32",
                        "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
                              "output stream per step, all larger than the 129 MB L2",
@@ -858,8 +970,8 @@ def run_ours(args, world, rank, local):
                             "gbs": round(alg[k] / (kavg[k] * 1e-3) / 1e9, 1) if alg[k] else None,
                             "frac": round(alg[k] / (kavg[k] * 1e-3) / 1e9 / peak, 4) if alg[k] else None,
                             "traffic": ncu_traffic(k)}
-                        for k in KERNELS},
-            "gpu_launches": len(KERNELS) * args.steps,
+                        for k in knames},
+            "gpu_launches": len(knames) * args.steps,
             "e2e": e2e,
             "variants": variants,
             "cpu_baseline": cpu,
@@ -908,6 +1020,10 @@ def main():
     p.add_argument("--oracle-rows", type=int, default=8192, help="rows of the CPU-baseline oracle sample")
     p.add_argument("--reference-budget-s", type=float, default=120.0,
                    help="CPU seconds the --impl reference run may spend in total")
+    p.add_argument("--schedule", type=int, choices=[0, 1, 2], default=0,
+                   help="launch schedule of the timed step (lora_delta_set_schedule): 0 separate launches, "
+                        "1 cluster reductions, 2 single cluster launches")
+    p.add_argument("--cluster", type=int, choices=[0, 2, 4, 8], default=0, help="cluster size (0: default)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-variants", action="store_true", help="skip the forward-only FP32 / BF16 dY_lora timing")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -49,9 +49,11 @@
  *               the word already holds a code (the first failure stays), and
  *               returns; the call's outputs are then undefined. The code stays
  *               until the caller clears the word (read it with
- *               lora_delta_device_status). No kernel waits for another CTA, and
- *               nothing else in the block carries state from call to call, so
- *               a call after a timed-out one needs no reset to run correctly.
+ *               lora_delta_device_status). No kernel of the default schedule
+ *               waits for another CTA (those of the cluster schedules wait only
+ *               for CTAs of their own cluster, which run together), and nothing
+ *               else in the block carries state from call to call, so a call
+ *               after a timed-out one needs no reset to run correctly.
  *       word 2  test hook, 0 for normal use: a kernel kind (1 down-projection,
  *               2 up-projection / dX, 3 fused dU + dB pass, 4 weight gradients)
  *               whose producer warp first waits on a barrier that nothing
