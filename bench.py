@@ -95,14 +95,13 @@ def measured_peaks():
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
 NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
-    "down U": {"bytes": 71_033_856, "src_hash": "6d8d371c39fb4fa4"},
-    "rows U": {"bytes": 26_112, "src_hash": "6d8d371c39fb4fa4"},
-    "up dY_lora": {"bytes": 125_373_696, "src_hash": "6d8d371c39fb4fa4"},
-    "dy dU+dB": {"bytes": 80_710_144, "src_hash": "6d8d371c39fb4fa4"},
-    "rows dU+dB": {"bytes": 1_117_184, "src_hash": "6d8d371c39fb4fa4"},
-    "up dX": {"bytes": 126_388_992, "src_hash": "6d8d371c39fb4fa4"},
-    "wgrad dA": {"bytes": 75_143_936, "src_hash": "6d8d371c39fb4fa4"},
-    "combine dA": {"bytes": 508_672, "src_hash": "6d8d371c39fb4fa4"},
+    "down U": {"bytes": 71_940_864, "src_hash": "2f4e6bbd31b8253e"},
+    "rows U": {"bytes": 80_896, "src_hash": "2f4e6bbd31b8253e"},
+    "up dY_lora": {"bytes": 124_115_200, "src_hash": "2f4e6bbd31b8253e"},
+    "dy dU+dB+rows dU (cluster)": {"bytes": 79_054_336, "src_hash": "2f4e6bbd31b8253e"},
+    "up dX": {"bytes": 126_059_264, "src_hash": "2f4e6bbd31b8253e"},
+    "wgrad dA": {"bytes": 75_174_912, "src_hash": "2f4e6bbd31b8253e"},
+    "combine dA+dB": {"bytes": 899_072, "src_hash": "2f4e6bbd31b8253e"},
 }
 
 
@@ -345,17 +344,25 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, peak, steps=40, reps=25):
     return out
 
 
-# Launch schedules of lora_delta_set_schedule measured beside the default separate launches:
+# Launch schedules of lora_delta_set_schedule measured beside the default (automatic) one:
 # (name, schedule, cluster size, forward kernels, backward kernels)
 SCHEDULES = [
+    ("separate", 0, 0, KERNELS_FWD, KERNELS_BWD),
     ("cluster_reduce_cl4", 1, 4, ["down+rows U (cluster)", "up dY_lora"],
      ["dy dU+dB+rows dU (cluster)", "up dX", "wgrad dA", "combine dA+dB"]),
     ("cluster_single_cl2", 2, 2, ["fwd (cluster)"], ["bwd (cluster)", "combine dA+dB"]),
     ("cluster_single_cl4", 2, 4, ["fwd (cluster)"], ["bwd (cluster)", "combine dA+dB"]),
 ]
+SCHEDULE_NAMES = {0: "separate launches", 1: "cluster reductions", 2: "single cluster launches", 3: "automatic"}
 
 
-def schedule_kernels(schedule, M, K, N, R):
+def auto_bwd_reduces(M, R, nsm, cl=4):
+    """The library's automatic schedule (lora_delta_set_schedule): the backward of R <= 16 runs as
+    cluster reductions when its 256-row chunks give at least three quarters of the SMs a CTA."""
+    return R <= 16 and 4 * ((M + 255) // 256) * cl >= 3 * nsm
+
+
+def schedule_kernels(schedule, M, K, N, R, nsm=152):
     """Kernel names of one step under a launch schedule (forward's, then backward's) and the
     algorithmic bytes each moves."""
     alg = algorithmic_bytes(M, K, N, R)
@@ -364,8 +371,9 @@ def schedule_kernels(schedule, M, K, N, R):
                "dy dU+dB+rows dU (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"], "combine dA+dB": 0,
                "fwd (cluster)": alg["down U"] + alg["rows U"] + alg["up dY_lora"],
                "bwd (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"] + alg["up dX"] + alg["wgrad dA"]})
-    if schedule == 0:
-        return KERNELS_FWD, KERNELS_BWD, kb
+    if schedule == 3:
+        bwd = SCHEDULES[1][4] if auto_bwd_reduces(M, R, nsm) else KERNELS_BWD
+        return KERNELS_FWD, bwd, kb
     for _, sched, _, kf, kbw in SCHEDULES:
         if sched == schedule:
             return kf, kbw, kb
@@ -379,7 +387,7 @@ def schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, peak, steps=24,
     the default stays the separate launches."""
     import torch
 
-    _, _, kb = schedule_kernels(0, M, K, N, R)
+    _, _, kb = schedule_kernels(0, M, K, N, R)   # bytes per kernel name (any schedule)
     total = step_bytes(M, K, N, R)
     Y = torch.empty((M, N), dtype=torch.float32, device=dev)
     U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
@@ -436,7 +444,7 @@ def schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, peak, steps=24,
             kavg = kernel_event_pass(ld, kf + kbw, len(kf), PROF_STEPS, stream, fwd, bwd)
             assert ld.lora_delta_device_status(wf) == 0 and ld.lora_delta_device_status(wb) == 0
         finally:
-            ld.lora_delta_set_schedule(0, 0)
+            ld.lora_delta_set_schedule(3, 0)
         out[f"schedule_{name}"] = {
             "launches_per_step": len(kf) + len(kbw),
             "ms_per_step": round(eager_ms, 5), "graph_ms_per_step": round(graph_ms, 5),
@@ -763,7 +771,8 @@ def run_ours(args, world, rank, local):
     wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
     stream = torch.cuda.current_stream(dev)
     ld.lora_delta_set_schedule(args.schedule, args.cluster)
-    kf_names, kb_names, kbytes = schedule_kernels(args.schedule, M, K, N, R)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    kf_names, kb_names, kbytes = schedule_kernels(args.schedule, M, K, N, R, nsm)
     knames = kf_names + kb_names
 
     def step(i):
@@ -844,7 +853,7 @@ def run_ours(args, world, rank, local):
     # ---------------------------------------- forward variants (FP32 / BF16 dY_lora)
     variants = None
     if not args.no_variants:
-        ld.lora_delta_set_schedule(0, 0)   # the variants choose their own schedules
+        ld.lora_delta_set_schedule(3, 0)   # the variants choose their own schedules
         variants = fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, measured_peaks()[0])
         variants.update(bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev))
         variants.update(schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, measured_peaks()[0]))
@@ -944,9 +953,11 @@ def run_ours(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, BF16)",
             "config": {"workload": f"LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, {len(knames)} kernels)",
-                       "schedule": {0: "separate launches", 1: "cluster reductions",
-                                    2: "single cluster launches"}[args.schedule]
-                                   + (f", clusters of {args.cluster or 4}" if args.schedule else ""),
+                       "schedule": SCHEDULE_NAMES[args.schedule]
+                                   + (f" (backward as cluster reductions)" if args.schedule == 3 and
+                                      kb_names != KERNELS_BWD else "")
+                                   + (f", clusters of {args.cluster or 4}" if kb_names != KERNELS_BWD or
+                                      kf_names != KERNELS_FWD else ""),
                        "M": M, "K": K, "N": N, "R": R, "alpha": alpha, "accumulate": "fp32",
                        "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
                              "output stream per step, all larger than the 129 MB L2",
@@ -1020,9 +1031,9 @@ def main():
     p.add_argument("--oracle-rows", type=int, default=8192, help="rows of the CPU-baseline oracle sample")
     p.add_argument("--reference-budget-s", type=float, default=120.0,
                    help="CPU seconds the --impl reference run may spend in total")
-    p.add_argument("--schedule", type=int, choices=[0, 1, 2], default=0,
+    p.add_argument("--schedule", type=int, choices=[0, 1, 2, 3], default=3,
                    help="launch schedule of the timed step (lora_delta_set_schedule): 0 separate launches, "
-                        "1 cluster reductions, 2 single cluster launches")
+                        "1 cluster reductions, 2 single cluster launches, 3 automatic (the library's default)")
     p.add_argument("--cluster", type=int, choices=[0, 2, 4, 8], default=0, help="cluster size (0: default)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-variants", action="store_true", help="skip the forward-only FP32 / BF16 dY_lora timing")

@@ -40,7 +40,7 @@ int g_nevents = 0;
 
 // Schedule of the single-site passes (lora_delta_set_schedule): separate launches, cluster
 // reductions or single cluster launches; cluster size 0 = kDefaultCluster.
-int g_schedule = LORA_SCHEDULE_SEPARATE;
+int g_schedule = LORA_SCHEDULE_AUTO;
 int g_cluster = 0;
 constexpr int kDefaultCluster = 4;
 // A CTA of a cluster waits for its peers' share of a tile (forward: 128 rows x K / cl of x; backward:
@@ -355,11 +355,13 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   Recorder rec(st);
   rec.mark();
   const int fcl = cluster_of_setting();
-  if (!fused && m == 1 && RP <= 32 && g_schedule != LORA_SCHEDULE_SEPARATE &&
+  // automatic: the separate launches (the cluster schedules measured no faster for the forward)
+  const int sched = g_schedule == LORA_SCHEDULE_AUTO ? LORA_SCHEDULE_SEPARATE : g_schedule;
+  if (!fused && m == 1 && RP <= 32 && sched != LORA_SCHEDULE_SEPARATE &&
       128 * in[active[0]].K * 2 / fcl <= kClusterShareBytes) {
     // single: one launch on clusters (down, rows and up steps per 128-row tile); reduce: the
     // down and rows steps on clusters, then the up-projection launch
-    const bool single = g_schedule == LORA_SCHEDULE_CLUSTER_SINGLE;
+    const bool single = sched == LORA_SCHEDULE_CLUSTER_SINGLE;
     const FwdIn& p = in[active[0]];
     const int mc = fwd_clusters(RP, y_bf16, single, fcl);
     if (mc < 1) return LORA_ERR_CUDA;
@@ -496,12 +498,18 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   Recorder rec(st);
   rec.mark();
   const int bcl = cluster_of_setting();
-  if (m == 1 && RP == 16 && g_schedule != LORA_SCHEDULE_SEPARATE &&
+  // automatic: the cluster reductions where the chunks of 256 rows give at least three quarters of
+  // the SMs a CTA (fewer leave the dY pass, bound per SM, short of SMs), else the separate launches
+  int sched = g_schedule;
+  if (sched == LORA_SCHEDULE_AUTO)
+    sched = m == 1 && 4 * ceil_div(in[active[0]].M, kDyChunk) * bcl >= 3 * int64_t(nsm) ? LORA_SCHEDULE_CLUSTER_REDUCE
+                                                                                       : LORA_SCHEDULE_SEPARATE;
+  if (m == 1 && RP == 16 && sched != LORA_SCHEDULE_SEPARATE &&
       int64_t(kDyChunk) * in[active[0]].N * 2 / bcl <= kClusterShareBytes) {
     // single: one launch on clusters (dU, dB partials; dU rows; dX, dA partials per 256-row chunk);
     // reduce: the dU, dB partials and dU rows on clusters, then the dX and dA launches. Then the
     // canonical trees over the chunk partials of dA and dB.
-    const bool single = g_schedule == LORA_SCHEDULE_CLUSTER_SINGLE;
+    const bool single = sched == LORA_SCHEDULE_CLUSTER_SINGLE;
     const BwdIn& p = in[active[0]];
     const int mc = bwd_clusters(single, bcl);
     if (mc < 1) return LORA_ERR_CUDA;
@@ -802,7 +810,7 @@ lora_status lora_delta_device_status(const void* workspace, int* code) {
 
 lora_status lora_delta_set_schedule(int schedule, int cluster_size) {
   if (schedule != LORA_SCHEDULE_SEPARATE && schedule != LORA_SCHEDULE_CLUSTER_REDUCE &&
-      schedule != LORA_SCHEDULE_CLUSTER_SINGLE)
+      schedule != LORA_SCHEDULE_CLUSTER_SINGLE && schedule != LORA_SCHEDULE_AUTO)
     return LORA_ERR_SHAPE;
   if (cluster_size != 0 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8) return LORA_ERR_SHAPE;
   g_schedule = schedule;

@@ -266,27 +266,24 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
         tc_fence_after();
         const uint32_t off = r.idx * C::kSlotBytes;
         const uint32_t d = tmem + t.idx * C::kTCols;
-        if (phase_a) {
+        if (elect_one()) {   // one lane issues the step's MMAs back to back
+          if (phase_a) {
 #pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-            if (elect_one()) mma_bf16(d + j * RP, desc_advance(a_du[j], off), desc_advance(b_du[j], off), idesc_du, 0u);
+            for (int j = 0; j < C::kLeaves; ++j)
+              mma_bf16(d + j * RP, desc_advance(a_du[j], off), desc_advance(b_du[j], off), idesc_du, 0u);
 #pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-            if (elect_one())
+            for (int j = 0; j < C::kLeaves; ++j)
               mma_bf16(d + (C::kLeaves + j) * RP, desc_advance(a_db[j], off), desc_advance(b_db[j], off), idesc_db, 0u);
-        } else {
-          // du rows of this half, MN-major for dA (r contiguous), K-major for dX; 32-byte swizzle
-          const uint32_t g0 = du0 + uint32_t(hh) * (C::kBM * RP * 2);
+          } else {
+            // du rows of this half, MN-major for dA (r contiguous), K-major for dX; 32-byte swizzle
+            const uint32_t g0 = du0 + uint32_t(hh) * (C::kBM * RP * 2);
 #pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-            if (elect_one())
+            for (int j = 0; j < C::kLeaves; ++j)
               mma_bf16(d + j * RP, desc_advance(a_da[j], off), smem_desc(g0 + j * 512u, 256u, 256u, kLayoutSW32),
                        idesc_da, 0u);
-          if (elect_one())
             mma_bf16(d + 128u, smem_desc(g0, 16u, 256u, kLayoutSW32),
                      smem_desc(base + off + C::kXBytes, RP * 128u, 1024u, kLayoutSW128), idesc_dx, 0u);
-        }
-        if (elect_one()) {
+          }
           mma_commit(empty(r.idx));
           mma_commit(tfull(t.idx));
         }

@@ -161,8 +161,9 @@ struct DownPhase {
       }
     } else if (warp == 1) {
       // --------------------------------------------------------- MMA issuer
-      // The whole warp follows the schedule, one elected lane issues; operand
-      // descriptors are built once for stage 0 and advanced by the stage offset.
+      // The whole warp follows the schedule, one elected lane issues a stage's MMAs
+      // back to back; operand descriptors are built once for stage 0 and advanced
+      // by the stage offset.
       constexpr uint32_t idesc = idesc_bf16(128, RP, 0, DV ? 1 : 0);
       constexpr uint32_t w_layout = layout_for_span(C::kWSpan);
       uint64_t adesc[C::kLeaves], wdesc[C::kLeaves];
@@ -186,10 +187,10 @@ struct DownPhase {
             tc_fence_after();
             const uint32_t off = r.idx * C::kStageBytes;
             const uint32_t d = tmem + g.idx * C::kGroupCols;
+            if (elect_one()) {   // one lane issues the stage's MMAs back to back
 #pragma unroll
-            for (int j = 0; j < C::kLeaves; ++j)   // fresh accumulator: one leaf
-              if (elect_one()) mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(wdesc[j], off), idesc, 0u);
-            if (elect_one()) {
+              for (int j = 0; j < C::kLeaves; ++j)   // fresh accumulator: one leaf
+                mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(wdesc[j], off), idesc, 0u);
               mma_commit(B.empty(r.idx));
               mma_commit(B.tfull(g.idx));
             }

@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
-    // The whole warp follows the schedule; one elected lane issues. Operand
-    // descriptors are built once for stage 0 and advanced by the stage offset.
+    // The whole warp follows the schedule; one elected lane issues a stage's MMAs
+    // back to back (one election per stage: measured, an election per MMA made
+    // the issue ~60 % slower). Operand descriptors are built once for stage 0 and
+    // advanced by the stage offset.
     constexpr uint32_t idesc_du = idesc_bf16(128, RP, 0, 1);   // dV K-major, b MN-major
     constexpr uint32_t idesc_db = idesc_bf16(128, RP, 1, 1);   // dV^T MN-major, u MN-major
     uint64_t a_du[C::kLeaves], b_du[C::kLeaves], a_db[C::kLeaves], b_db[C::kLeaves];
@@ -210,14 +212,13 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
           tc_fence_after();
           const uint32_t off = r.idx * C::kStageBytes;
           const uint32_t d = tmem + g.idx * C::kGroupCols;
+          if (elect_one()) {   // one lane issues the stage's MMAs back to back
 #pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-            if (elect_one()) mma_bf16(d + j * RP, desc_advance(a_du[j], off), desc_advance(b_du[j], off), idesc_du, 0u);
+            for (int j = 0; j < C::kLeaves; ++j)
+              mma_bf16(d + j * RP, desc_advance(a_du[j], off), desc_advance(b_du[j], off), idesc_du, 0u);
 #pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-            if (elect_one())
+            for (int j = 0; j < C::kLeaves; ++j)
               mma_bf16(d + C::kLeaves * RP + j * RP, desc_advance(a_db[j], off), desc_advance(b_db[j], off), idesc_db, 0u);
-          if (elect_one()) {
             mma_commit(empty(r.idx));
             mma_commit(tfull(g.idx));
           }

@@ -231,10 +231,10 @@ __global__ void __launch_bounds__(FcCfg<RP, UP>::kThreads, 1)
             tc_fence_after();
             const uint32_t off = r.idx * C::kDStageBytes;
             const uint32_t d = tmem + g.idx * C::kGroupCols;
+            if (elect_one()) {   // one lane issues the stage's MMAs back to back
 #pragma unroll
-            for (int j = 0; j < C::kLeaves; ++j)   // fresh accumulator: one leaf
-              if (elect_one()) mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(wdesc[j], off), idesc, 0u);
-            if (elect_one()) {
+              for (int j = 0; j < C::kLeaves; ++j)   // fresh accumulator: one leaf
+                mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(wdesc[j], off), idesc, 0u);
               mma_commit(dempty(r.idx));
               mma_commit(tfull(g.idx));
             }

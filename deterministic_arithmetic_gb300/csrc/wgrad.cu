@@ -188,10 +188,10 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
           tc_fence_after();
           const uint32_t off = r.idx * C::kStageBytes;
           const uint32_t d = tmem + g.idx * C::kGroupCols;
+          if (elect_one()) {   // one lane issues the stage's MMAs back to back
 #pragma unroll
-          for (int j = 0; j < C::kLeaves; ++j)
-            if (elect_one()) mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(gdesc[j], off), idesc, 0u);
-          if (elect_one()) {
+            for (int j = 0; j < C::kLeaves; ++j)
+              mma_bf16(d + j * RP, desc_advance(adesc[j], off), desc_advance(gdesc[j], off), idesc, 0u);
             mma_commit(empty(r.idx));
             mma_commit(tfull(g.idx));
           }

@@ -414,7 +414,7 @@ def lora_delta_set_profile_events(events) -> None:
         raise LoraDeltaError(rc, "lora_delta_set_profile_events")
 
 
-SCHEDULE_SEPARATE, SCHEDULE_CLUSTER_REDUCE, SCHEDULE_CLUSTER_SINGLE = 0, 1, 2
+SCHEDULE_SEPARATE, SCHEDULE_CLUSTER_REDUCE, SCHEDULE_CLUSTER_SINGLE, SCHEDULE_AUTO = 0, 1, 2, 3
 
 
 def lora_delta_set_schedule(schedule: int, cluster_size: int = 0) -> None:

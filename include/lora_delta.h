@@ -248,13 +248,11 @@ lora_status lora_delta_device_status(const void *workspace, int *code);
 lora_status lora_delta_set_profile_events(void *const *events, int count);
 
 /*
- * Schedule of the single-site passes (process-wide; not thread-safe; no
- * effect on any result bit -- every schedule runs the same leaves, trees and
- * rounding points). The operator's steps can be grouped into launches three
- * ways:
- *   LORA_SCHEDULE_SEPARATE (default): forward down-projection, rows,
- *     up-projection; backward dU + dB pass, rows (with the dB tree), dX, dA,
- *     combine.
+ * Schedule of the passes (process-wide; not thread-safe; no effect on any
+ * result bit -- every schedule runs the same leaves, trees and rounding
+ * points). The operator's steps can be grouped into launches three ways:
+ *   LORA_SCHEDULE_SEPARATE: forward down-projection, rows, up-projection;
+ *     backward dU + dB pass, rows (with the dB tree), dX, dA, combine.
  *   LORA_SCHEDULE_CLUSTER_REDUCE: the reductions that feed a BF16 row on
  *     thread-block clusters -- a cluster of `cluster_size` CTAs shares each
  *     128-row tile (forward: U partials and the U rows) or 256-row chunk
@@ -266,17 +264,23 @@ lora_status lora_delta_set_profile_events(void *const *events, int count);
  *     also expands its share of the tile's columns of delta_y); the backward
  *     (R <= 16) in one cluster launch (each CTA also writes its share of dX and
  *     the dA chunk partials) and the combine launch.
+ *   LORA_SCHEDULE_AUTO (the default): the forward as separate launches; the
+ *     single-site backward of R <= 16 as cluster reductions where its 256-row
+ *     chunks give at least three quarters of the SMs a CTA (on a GB300, M of
+ *     about 7300 rows and more with clusters of 4), else as separate launches --
+ *     the faster choice at every shape measured.
  * The cluster schedules cover the single-site forward of R <= 32 and the
  * single-site backward of R <= 16 whose per-CTA share of a tile is at most
- * 32 MiB of input; other calls run the separate launches. cluster_size is 0
- * (the default size, 4 CTAs), 2, 4 or 8. Returns LORA_ERR_SHAPE, leaving the
- * setting unchanged, for any other value. lora_delta_schedule returns the
- * current schedule and stores the cluster size setting in *cluster_size (if
- * not NULL).
+ * 32 MiB of input; other calls (grouped calls included) run the separate
+ * launches. cluster_size is 0 (the default size, 4 CTAs), 2, 4 or 8. Returns
+ * LORA_ERR_SHAPE, leaving the setting unchanged, for any other value.
+ * lora_delta_schedule returns the current schedule and stores the cluster
+ * size setting in *cluster_size (if not NULL).
  */
 #define LORA_SCHEDULE_SEPARATE 0
 #define LORA_SCHEDULE_CLUSTER_REDUCE 1
 #define LORA_SCHEDULE_CLUSTER_SINGLE 2
+#define LORA_SCHEDULE_AUTO 3
 lora_status lora_delta_set_schedule(int schedule, int cluster_size);
 int lora_delta_schedule(int *cluster_size);
 

@@ -22,9 +22,9 @@ import gpu_util as G  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 CONTROL = 256 + 65536      # LORA_DELTA_CONTROL_BYTES
-SEP, RED, ONE = ld.SCHEDULE_SEPARATE, ld.SCHEDULE_CLUSTER_REDUCE, ld.SCHEDULE_CLUSTER_SINGLE
+SEP, RED, ONE, AUTO = ld.SCHEDULE_SEPARATE, ld.SCHEDULE_CLUSTER_REDUCE, ld.SCHEDULE_CLUSTER_SINGLE, ld.SCHEDULE_AUTO
 # (schedule, cluster size) pairs compared with the separate launches
-VARIANTS = [(RED, 2), (RED, 4), (RED, 8), (ONE, 2), (ONE, 4), (ONE, 8)]
+VARIANTS = [(RED, 2), (RED, 4), (RED, 8), (ONE, 2), (ONE, 4), (ONE, 8), (AUTO, 0)]
 
 
 @contextlib.contextmanager
@@ -33,7 +33,7 @@ def schedule(sched, cl=0):
     try:
         yield
     finally:
-        ld.lora_delta_set_schedule(SEP, 0)
+        ld.lora_delta_set_schedule(AUTO, 0)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,7 +44,7 @@ def _built():
 
     build_lib.build()
     yield
-    ld.lora_delta_set_schedule(SEP, 0)
+    ld.lora_delta_set_schedule(AUTO, 0)
 
 
 def _inputs(M, K, N, R, alpha, seed):
@@ -124,14 +124,14 @@ def test_cluster_forward_reruns_and_empty_batch():
 
 
 def test_schedule_setting():
-    assert ld.lora_delta_schedule() == (SEP, 0)      # the separate launches by default
-    for bad in ((3, 0), (-1, 0), (RED, 1), (ONE, 3), (ONE, 16)):
+    assert ld.lora_delta_schedule() == (AUTO, 0)      # the automatic choice by default
+    for bad in ((4, 0), (-1, 0), (RED, 1), (ONE, 3), (ONE, 16)):
         with pytest.raises(ld.LoraDeltaError):
             ld.lora_delta_set_schedule(*bad)
-    assert ld.lora_delta_schedule() == (SEP, 0)
+    assert ld.lora_delta_schedule() == (AUTO, 0)
     with schedule(RED, 8):
         assert ld.lora_delta_schedule() == (RED, 8)
-    assert ld.lora_delta_schedule() == (SEP, 0)
+    assert ld.lora_delta_schedule() == (AUTO, 0)
 
 
 @pytest.mark.parametrize("sched", [RED, ONE])

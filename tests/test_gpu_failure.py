@@ -63,7 +63,7 @@ def schedule(request):
 
     ld.lora_delta_set_schedule(request.param, 0)
     yield request.param
-    ld.lora_delta_set_schedule(0, 0)
+    ld.lora_delta_set_schedule(ld.SCHEDULE_AUTO, 0)
 
 
 @pytest.mark.parametrize("kind,where,R,site", CASES)
