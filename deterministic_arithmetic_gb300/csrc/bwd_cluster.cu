@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
     Ring r;
     auto pass = [&](bool transform) {
       if (wait(full(r.idx), r.phase, ab, 90)) {
-        if (transform) {
+        if (transform && !dv_is_dy(alpha)) {
           uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kSlotBytes);
 #pragma unroll
           for (int e = 0; e < C::kTileBytes / 16 / (32 * C::kXfWarps); ++e)

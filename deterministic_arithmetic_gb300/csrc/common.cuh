@@ -398,6 +398,10 @@ __device__ __forceinline__ uint4 scale_bf16x8_pow2(uint4 v, uint32_t a2) {
   for (int i = 0; i < 4; ++i) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(w[i]), "r"(a2));
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
+// alpha = 1: dV = bf16(fp32(dY) * 1) is dY itself for every BF16 value (a signaling NaN would
+// only be quieted; the tensor core treats both as NaN), so the kernels pass dY through as dV
+// without the shared-memory round trip of the transform.
+__device__ __forceinline__ bool dv_is_dy(float alpha) { return alpha == 1.0f; }
 // dV for one 16-byte chunk, taking the packed form when a2 != 0.
 __device__ __forceinline__ uint4 dv_bf16x8(uint4 v, float alpha, uint32_t a2) {
   return a2 ? scale_bf16x8_pow2(v, a2) : scale_bf16x8(v, alpha);

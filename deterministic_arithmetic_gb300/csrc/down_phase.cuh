@@ -290,10 +290,12 @@ struct DownPhase {
         const Unit tu = unit(S, u);
         for (int kb = 0; kb < tu.nkb; ++kb) {
           if (wait(B.full(r.idx), r.phase, ab, 7)) {
-            uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kStageBytes);
+            if (!dv_is_dy(alpha)) {
+              uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kStageBytes);
 #pragma unroll
-            for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = dv_bf16x8(tile[t + 128 * e], alpha, a2);
-            fence_proxy_async();
+              for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = dv_bf16x8(tile[t + 128 * e], alpha, a2);
+              fence_proxy_async();
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(B.ready(r.idx));
           }

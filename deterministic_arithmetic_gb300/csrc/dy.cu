@@ -324,11 +324,13 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
       const int nstages = n_tiles(P, sl) * r_tiles(P, ch);
       for (int k = 0; k < nstages; ++k) {
         if (wait(full(r.idx), r.phase, ab, 37)) {
-          uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kStageBytes);
+          if (!dv_is_dy(alpha)) {
+            uint4* tile = reinterpret_cast<uint4*>(gbase + size_t(r.idx) * C::kStageBytes);
 #pragma unroll
-          for (int e = 0; e < C::kTileBytes / 16 / (32 * C::kXfWarps); ++e)
-            tile[t + 32 * C::kXfWarps * e] = dv_bf16x8(tile[t + 32 * C::kXfWarps * e], alpha, a2);
-          fence_proxy_async();
+            for (int e = 0; e < C::kTileBytes / 16 / (32 * C::kXfWarps); ++e)
+              tile[t + 32 * C::kXfWarps * e] = dv_bf16x8(tile[t + 32 * C::kXfWarps * e], alpha, a2);
+            fence_proxy_async();
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(ready(r.idx));
         }

@@ -290,10 +290,12 @@ __global__ void __launch_bounds__(WgCfg<RP, DV>::kThreads, 1)
       const int ns = stages_of(P, ch);
       for (int kb = 0; kb < ns; ++kb) {
         if (wait(full(r.idx), r.phase, ab, 27)) {
-          uint4* tile = reinterpret_cast<uint4*>(smem_raw + (base - raw) + size_t(r.idx) * C::kStageBytes);
+          if (!dv_is_dy(alpha)) {
+            uint4* tile = reinterpret_cast<uint4*>(smem_raw + (base - raw) + size_t(r.idx) * C::kStageBytes);
 #pragma unroll
-          for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = dv_bf16x8(tile[t + 128 * e], alpha, a2);
-          fence_proxy_async();
+            for (int e = 0; e < C::kInBytes / 16 / 128; ++e) tile[t + 128 * e] = dv_bf16x8(tile[t + 128 * e], alpha, a2);
+            fence_proxy_async();
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(ready(r.idx));
         }
