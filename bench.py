@@ -95,13 +95,13 @@ def measured_peaks():
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
 NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
-    "down U": {"bytes": 71_940_864, "src_hash": "2f4e6bbd31b8253e"},
-    "rows U": {"bytes": 80_896, "src_hash": "2f4e6bbd31b8253e"},
-    "up dY_lora": {"bytes": 124_115_200, "src_hash": "2f4e6bbd31b8253e"},
-    "dy dU+dB+rows dU (cluster)": {"bytes": 79_054_336, "src_hash": "2f4e6bbd31b8253e"},
-    "up dX": {"bytes": 126_059_264, "src_hash": "2f4e6bbd31b8253e"},
-    "wgrad dA": {"bytes": 75_174_912, "src_hash": "2f4e6bbd31b8253e"},
-    "combine dA+dB": {"bytes": 899_072, "src_hash": "2f4e6bbd31b8253e"},
+    "down U": {"bytes": 72_015_104, "src_hash": "cd87db2509e13a82"},
+    "rows U": {"bytes": 45_824, "src_hash": "cd87db2509e13a82"},
+    "up dY_lora": {"bytes": 123_836_160, "src_hash": "cd87db2509e13a82"},
+    "dy dU+dB+rows dU (cluster)": {"bytes": 79_399_680, "src_hash": "cd87db2509e13a82"},
+    "up dX": {"bytes": 126_049_280, "src_hash": "cd87db2509e13a82"},
+    "wgrad dA": {"bytes": 74_881_536, "src_hash": "cd87db2509e13a82"},
+    "combine dA+dB": {"bytes": 817_408, "src_hash": "cd87db2509e13a82"},
 }
 
 
@@ -356,28 +356,17 @@ SCHEDULES = [
 SCHEDULE_NAMES = {0: "separate launches", 1: "cluster reductions", 2: "single cluster launches", 3: "automatic"}
 
 
-def auto_bwd_reduces(M, R, nsm, cl=4):
-    """The library's automatic schedule (lora_delta_set_schedule): the backward of R <= 16 runs as
-    cluster reductions when its 256-row chunks give at least three quarters of the SMs a CTA."""
-    return R <= 16 and 4 * ((M + 255) // 256) * cl >= 3 * nsm
-
-
-def schedule_kernels(schedule, M, K, N, R, nsm=152):
-    """Kernel names of one step under a launch schedule (forward's, then backward's) and the
-    algorithmic bytes each moves."""
+def schedule_kernels(fwd_schedule, bwd_schedule, M, K, N, R):
+    """Kernel names of one step (forward's, then backward's) when the forward and the backward take
+    the given schedules (as lora_delta_plan reports them), and the algorithmic bytes each moves."""
     alg = algorithmic_bytes(M, K, N, R)
     kb = dict(alg)
     kb.update({"down+rows U (cluster)": alg["down U"] + alg["rows U"],
                "dy dU+dB+rows dU (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"], "combine dA+dB": 0,
                "fwd (cluster)": alg["down U"] + alg["rows U"] + alg["up dY_lora"],
                "bwd (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"] + alg["up dX"] + alg["wgrad dA"]})
-    if schedule == 3:
-        bwd = SCHEDULES[1][4] if auto_bwd_reduces(M, R, nsm) else KERNELS_BWD
-        return KERNELS_FWD, bwd, kb
-    for _, sched, _, kf, kbw in SCHEDULES:
-        if sched == schedule:
-            return kf, kbw, kb
-    raise ValueError(schedule)
+    by = {sched: (kf, kbw) for _, sched, _, kf, kbw in SCHEDULES}
+    return by[fwd_schedule][0], by[bwd_schedule][1], kb
 
 
 def schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, peak, steps=24, reps=10):
@@ -387,7 +376,7 @@ def schedule_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, peak, steps=24,
     the default stays the separate launches."""
     import torch
 
-    _, _, kb = schedule_kernels(0, M, K, N, R)   # bytes per kernel name (any schedule)
+    _, _, kb = schedule_kernels(0, 0, M, K, N, R)   # bytes per kernel name (any schedule)
     total = step_bytes(M, K, N, R)
     Y = torch.empty((M, N), dtype=torch.float32, device=dev)
     U = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
@@ -771,8 +760,9 @@ def run_ours(args, world, rank, local):
     wb = ld.new_workspace(ld.lora_delta_bwd_workspace_size(M, K, N, R), dev)
     stream = torch.cuda.current_stream(dev)
     ld.lora_delta_set_schedule(args.schedule, args.cluster)
-    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-    kf_names, kb_names, kbytes = schedule_kernels(args.schedule, M, K, N, R, nsm)
+    plan_f, plan_b = ld.lora_delta_plan(False, M, K, N, R), ld.lora_delta_plan(True, M, K, N, R)
+    kf_names, kb_names, kbytes = schedule_kernels(plan_f[0], plan_b[0], M, K, N, R)
+    assert (len(kf_names), len(kb_names)) == (plan_f[1], plan_b[1]), (plan_f, plan_b)
     knames = kf_names + kb_names
 
     def step(i):
@@ -954,10 +944,8 @@ def run_ours(args, world, rank, local):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, BF16)",
             "config": {"workload": f"LoRA training step M=8192 K=N=4096 R=16 alpha=2 (fwd+bwd, {len(knames)} kernels)",
                        "schedule": SCHEDULE_NAMES[args.schedule]
-                                   + (f" (backward as cluster reductions)" if args.schedule == 3 and
-                                      kb_names != KERNELS_BWD else "")
-                                   + (f", clusters of {args.cluster or 4}" if kb_names != KERNELS_BWD or
-                                      kf_names != KERNELS_FWD else ""),
+                                   + f" (forward: {SCHEDULE_NAMES[plan_f[0]]}, backward: {SCHEDULE_NAMES[plan_b[0]]})"
+                                   + (f", clusters of {args.cluster or 4}" if plan_f[0] or plan_b[0] else ""),
                        "M": M, "K": K, "N": N, "R": R, "alpha": alpha, "accumulate": "fp32",
                        "l2": f"inputs rotated over {N_ROTATE} physical copies of X and dY (384 MiB) and a 256 MiB "
                              "output stream per step, all larger than the 129 MB L2",

@@ -70,6 +70,24 @@ int fwd_clusters(int RP, bool y_bf16, bool up, int cl) {
   return v;
 }
 
+// The schedule a forward call of m active sites takes: the cluster schedules cover one site of
+// padded rank 16 or 32 whose per-CTA share of a tile is small enough; automatic = separate (the
+// cluster schedules measured no faster for the forward).
+int fwd_schedule(int m, int RP, int64_t K) {
+  const int sched = g_schedule == LORA_SCHEDULE_AUTO ? LORA_SCHEDULE_SEPARATE : g_schedule;
+  if (m != 1 || RP > 32 || 128 * K * 2 / cluster_of_setting() > kClusterShareBytes) return LORA_SCHEDULE_SEPARATE;
+  return sched;
+}
+// The schedule a backward call takes: one site of padded rank 16 with a small enough share;
+// automatic = the cluster reductions where the chunks of 256 rows give at least three quarters of
+// the SMs a CTA (fewer leave the dY pass, bound per SM, short of SMs), else the separate launches.
+int bwd_schedule(int m, int RP, int64_t M, int64_t N, int nsm) {
+  const int cl = cluster_of_setting();
+  if (m != 1 || RP != 16 || int64_t(kDyChunk) * N * 2 / cl > kClusterShareBytes) return LORA_SCHEDULE_SEPARATE;
+  if (g_schedule != LORA_SCHEDULE_AUTO) return g_schedule;
+  return 4 * ceil_div(M, kDyChunk) * cl >= 3 * int64_t(nsm) ? LORA_SCHEDULE_CLUSTER_REDUCE : LORA_SCHEDULE_SEPARATE;
+}
+
 // The same for the backward cluster kernel.
 int bwd_clusters(bool phase_c, int cl) {
   int dev = 0;
@@ -355,10 +373,8 @@ lora_status fwd_group(const FwdIn* in, int n, int64_t R, bool y_bf16, void* work
   Recorder rec(st);
   rec.mark();
   const int fcl = cluster_of_setting();
-  // automatic: the separate launches (the cluster schedules measured no faster for the forward)
-  const int sched = g_schedule == LORA_SCHEDULE_AUTO ? LORA_SCHEDULE_SEPARATE : g_schedule;
-  if (!fused && m == 1 && RP <= 32 && sched != LORA_SCHEDULE_SEPARATE &&
-      128 * in[active[0]].K * 2 / fcl <= kClusterShareBytes) {
+  const int sched = fused ? LORA_SCHEDULE_SEPARATE : fwd_schedule(m, RP, in[active[0]].K);
+  if (sched != LORA_SCHEDULE_SEPARATE) {
     // single: one launch on clusters (down, rows and up steps per 128-row tile); reduce: the
     // down and rows steps on clusters, then the up-projection launch
     const bool single = sched == LORA_SCHEDULE_CLUSTER_SINGLE;
@@ -498,14 +514,8 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   Recorder rec(st);
   rec.mark();
   const int bcl = cluster_of_setting();
-  // automatic: the cluster reductions where the chunks of 256 rows give at least three quarters of
-  // the SMs a CTA (fewer leave the dY pass, bound per SM, short of SMs), else the separate launches
-  int sched = g_schedule;
-  if (sched == LORA_SCHEDULE_AUTO)
-    sched = m == 1 && 4 * ceil_div(in[active[0]].M, kDyChunk) * bcl >= 3 * int64_t(nsm) ? LORA_SCHEDULE_CLUSTER_REDUCE
-                                                                                       : LORA_SCHEDULE_SEPARATE;
-  if (m == 1 && RP == 16 && sched != LORA_SCHEDULE_SEPARATE &&
-      int64_t(kDyChunk) * in[active[0]].N * 2 / bcl <= kClusterShareBytes) {
+  const int sched = bwd_schedule(m, RP, in[active[0]].M, in[active[0]].N, nsm);
+  if (sched != LORA_SCHEDULE_SEPARATE) {
     // single: one launch on clusters (dU, dB partials; dU rows; dX, dA partials per 256-row chunk);
     // reduce: the dU, dB partials and dU rows on clusters, then the dX and dA launches. Then the
     // canonical trees over the chunk partials of dA and dB.
@@ -821,6 +831,31 @@ lora_status lora_delta_set_schedule(int schedule, int cluster_size) {
 int lora_delta_schedule(int* cluster_size) {
   if (cluster_size) *cluster_size = g_cluster;
   return g_schedule;
+}
+
+lora_status lora_delta_plan(int backward, int64_t M, int64_t K, int64_t N, int64_t R, int* schedule, int* launches) {
+  if (!schedule || !launches) return LORA_ERR_NULL;
+  const lora_status s0 = check_shape(M, K, N, R);
+  if (s0 != LORA_OK) return s0;
+  int nsm = 0;
+  const lora_status s1 = device_ready(&nsm);
+  if (s1 != LORA_OK) return s1;
+  const int RP = padded_rank(int(R));
+  if (M == 0) {
+    *schedule = LORA_SCHEDULE_SEPARATE;
+    *launches = 0;
+    return LORA_OK;
+  }
+  if (!backward) {
+    const int sc = fwd_schedule(1, RP, K);
+    *schedule = sc;
+    *launches = sc == LORA_SCHEDULE_CLUSTER_SINGLE ? 1 : (sc == LORA_SCHEDULE_CLUSTER_REDUCE ? 2 : 3);
+  } else {
+    const int sc = bwd_schedule(1, RP, M, N, nsm);
+    *schedule = sc;
+    *launches = sc == LORA_SCHEDULE_CLUSTER_SINGLE ? 2 : (sc == LORA_SCHEDULE_CLUSTER_REDUCE ? 4 : (RP == 16 ? 5 : 6));
+  }
+  return LORA_OK;
 }
 
 lora_status lora_delta_set_profile_events(void* const* events, int count) {

@@ -121,6 +121,9 @@ def _lib() -> ctypes.CDLL:
         lib.lora_delta_set_schedule.restype = ctypes.c_int
         lib.lora_delta_schedule.argtypes = [ctypes.POINTER(ctypes.c_int)]
         lib.lora_delta_schedule.restype = ctypes.c_int
+        lib.lora_delta_plan.argtypes = [ctypes.c_int, _i64, _i64, _i64, _i64, ctypes.POINTER(ctypes.c_int),
+                                        ctypes.POINTER(ctypes.c_int)]
+        lib.lora_delta_plan.restype = ctypes.c_int
         lib.lora_delta_describe.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.lora_delta_describe.restype = ctypes.c_size_t
         _LIB = lib
@@ -429,6 +432,15 @@ def lora_delta_schedule() -> tuple[int, int]:
     """(schedule, cluster size setting)."""
     cl = ctypes.c_int(0)
     return int(_lib().lora_delta_schedule(ctypes.byref(cl))), int(cl.value)
+
+
+def lora_delta_plan(backward: bool, M: int, K: int, N: int, R: int) -> tuple[int, int]:
+    """(schedule, launches) a single-site call of this shape takes on the current device."""
+    sc, nl = ctypes.c_int(0), ctypes.c_int(0)
+    rc = _lib().lora_delta_plan(1 if backward else 0, M, K, N, R, ctypes.byref(sc), ctypes.byref(nl))
+    if rc != LORA_OK:
+        raise LoraDeltaError(rc, "lora_delta_plan")
+    return int(sc.value), int(nl.value)
 
 
 def lora_delta_describe() -> str:

@@ -285,6 +285,15 @@ lora_status lora_delta_set_schedule(int schedule, int cluster_size);
 int lora_delta_schedule(int *cluster_size);
 
 /*
+ * The launch plan a single-site call of this shape takes on the current device under the
+ * current schedule setting (backward != 0: lora_delta_bwd, else lora_delta_fwd): the
+ * schedule actually used (LORA_SCHEDULE_SEPARATE, _CLUSTER_REDUCE or _CLUSTER_SINGLE) and the
+ * number of kernel launches it enqueues (0 for M = 0). Returns the call's shape errors, or
+ * LORA_ERR_DEVICE / LORA_ERR_CUDA when the current device cannot run the operator.
+ */
+lora_status lora_delta_plan(int backward, int64_t M, int64_t K, int64_t N, int64_t R, int *schedule, int *launches);
+
+/*
  * Writes a NUL-terminated JSON description of the numerics and tiling
  * (provenance) into buf (at most len bytes). Returns the length it needs.
  */

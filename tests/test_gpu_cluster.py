@@ -225,3 +225,26 @@ def test_cluster_backward_reruns():
         ref = _bwd(t, 2.0, sv, ws=ws)
         for _ in range(2):
             _same_bwd(f"rerun {sv}", ref, _bwd(t, 2.0, sv, ws=ws))
+
+
+def test_launch_plan():
+    """lora_delta_plan reports the schedule a call takes and its launch count: the automatic
+    schedule keeps the forward's separate launches and takes the backward's cluster reductions
+    where its 256-row chunks give at least three quarters of the SMs a CTA."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    big = (256 * ((3 * nsm + 15) // 16) + 256)   # enough chunks for clusters of 4
+    assert ld.lora_delta_plan(False, 8192, 4096, 4096, 16) == (SEP, 3)
+    assert ld.lora_delta_plan(True, big, 4096, 4096, 16) == (RED, 4)
+    assert ld.lora_delta_plan(True, 256, 4096, 4096, 16) == (SEP, 5)
+    assert ld.lora_delta_plan(True, big, 4096, 4096, 32) == (SEP, 6)       # rank above 16: separate
+    assert ld.lora_delta_plan(False, 0, 4096, 4096, 16) == (SEP, 0)
+    with schedule(ONE, 4):
+        assert ld.lora_delta_plan(False, 8192, 4096, 4096, 32) == (ONE, 1)
+        assert ld.lora_delta_plan(False, 8192, 4096, 4096, 64) == (SEP, 3)   # rank above 32: separate
+        assert ld.lora_delta_plan(True, 300, 1032, 520, 16) == (ONE, 2)
+    with schedule(RED, 2):
+        assert ld.lora_delta_plan(False, 8192, 4096, 4096, 16) == (RED, 2)
+        assert ld.lora_delta_plan(True, 8192, 4096, 4096, 16) == (RED, 4)
+        assert ld.lora_delta_plan(True, 8192, 4096, 1 << 20, 16) == (SEP, 5)   # a CTA's share too large
+    with pytest.raises(ld.LoraDeltaError):
+        ld.lora_delta_plan(True, 8192, 4095, 4096, 16)                      # K not a multiple of 8
