@@ -78,14 +78,21 @@ int fwd_schedule(int m, int RP, int64_t K) {
   if (m != 1 || RP > 32 || 128 * K * 2 / cluster_of_setting() > kClusterShareBytes) return LORA_SCHEDULE_SEPARATE;
   return sched;
 }
+// Rows per unit of the backward's cluster reductions: a 256-row chunk where the chunks give at
+// least three quarters of the SMs a CTA, else one 128-row tile (twice the units).
+int bwd_unit_rows(int64_t M, int cl, int nsm) {
+  return 4 * ceil_div(M, kDyChunk) * cl >= 3 * int64_t(nsm) ? kDyChunk : 128;
+}
 // The schedule a backward call takes: one site of padded rank 16 with a small enough share;
-// automatic = the cluster reductions where the chunks of 256 rows give at least three quarters of
-// the SMs a CTA (fewer leave the dY pass, bound per SM, short of SMs), else the separate launches.
+// automatic = the cluster reductions where their 256-row chunks give at least three quarters of
+// the SMs a CTA, else the separate launches (measured: with 128-row units, or fewer CTAs, the dY
+// pass -- bound per SM -- on fewer SMs than the separate dy kernel's costs more than the rows
+// launch it saves: fc1 78.7 vs 70.5 us).
 int bwd_schedule(int m, int RP, int64_t M, int64_t N, int nsm) {
   const int cl = cluster_of_setting();
   if (m != 1 || RP != 16 || int64_t(kDyChunk) * N * 2 / cl > kClusterShareBytes) return LORA_SCHEDULE_SEPARATE;
   if (g_schedule != LORA_SCHEDULE_AUTO) return g_schedule;
-  return 4 * ceil_div(M, kDyChunk) * cl >= 3 * int64_t(nsm) ? LORA_SCHEDULE_CLUSTER_REDUCE : LORA_SCHEDULE_SEPARATE;
+  return bwd_unit_rows(M, cl, nsm) == kDyChunk ? LORA_SCHEDULE_CLUSTER_REDUCE : LORA_SCHEDULE_SEPARATE;
 }
 
 // The same for the backward cluster kernel.
@@ -194,7 +201,8 @@ BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int64_t R) {
   BwdLayout l;
   l.dupart = 0;
   l.dbpart = l.dupart + round256(S * size_t(M) * RP * 4);
-  l.dapart = l.dbpart + round256(C * RP * size_t(N) * 4);
+  // dB partials per 128-row tile (the cluster reductions' units may be single tiles): up to 2 C
+  l.dapart = l.dbpart + round256(size_t(ceil_div(M, 128)) * RP * size_t(N) * 4);
   l.bytes = l.dapart + round256(C * RP * size_t(K) * 4);
   return l;
 }
@@ -541,7 +549,9 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     ba.N = int(p.N);
     ba.R = int(R);
     ba.alpha = p.alpha;
-    const int ncl = int(std::min<int64_t>(mc, ceil_div(p.M, kDyChunk)));
+    ba.unit_rows = single ? kDyChunk : bwd_unit_rows(p.M, bcl, nsm);
+    const int64_t n_units = ceil_div(p.M, ba.unit_rows);
+    const int ncl = int(std::min<int64_t>(mc, n_units));
     if (launch_bwd_cluster(single, ba, status, bcl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
     if (!single) {
@@ -554,6 +564,7 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     jobs.n = 2;
     jobs.j[0] = da_jobs.j[0];
     jobs.j[1] = db_jobs.j[0];
+    jobs.j[1].C = int(n_units);   // one dB partial per unit
     if (launch_combine(jobs, st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
     return LORA_OK;

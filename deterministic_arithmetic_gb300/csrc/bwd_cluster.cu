@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
   const int CL = int(cluster_size()), rank = int(cluster_rank());
   const int cid = int(cluster_index()), ncl = int(cluster_count());
   const int M = args.M, K = args.K, N = args.N, S = args.S, n_ch = args.n_ch;
+  // rows of a unit: a 256-row chunk, or (cluster reductions only) one 128-row tile, whose dB tree is
+  // then the unit's partial (the combine's first level adds the two tiles of each chunk)
+  const int UR = PC ? kDyChunk : args.unit_rows;
   const int n_kt = PC ? args.n_kt : 0;   // phase C column tiles (none without phase C)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSlots; ++s) {
@@ -159,13 +162,13 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
   cluster_sync_all();          // every peer's mbarriers are initialised before any remote arrival
   // valid column tiles of a slice, row tiles (halves) of a chunk
   auto n_tiles = [&](int sl) { return (min(N - sl * kDySlice, kDySlice) + 127) / 128; };
-  auto r_tiles = [&](int ch) { return (min(M - ch * kDyChunk, kDyChunk) + C::kBM - 1) / C::kBM; };
+  auto r_tiles = [&](int ch) { return (min(M - ch * UR, UR) + C::kBM - 1) / C::kBM; };
   if (threadIdx.x == 0 && cid < n_ch && rank < S) {
     // the first dY tiles of this CTA's first slice, into L2 while the predecessor drains
     const int nnt = n_tiles(rank), nrt = r_tiles(cid);
     for (int i = 0, n = 0; i < nnt && n < 4; ++i)
       for (int j = 0; j < nrt && n < 4; ++j, ++n)
-        for (int q = 0; q < 4; ++q) tma_prefetch_l2(&args.dy, rank * kDySlice + i * 128 + 32 * q, cid * kDyChunk + j * C::kBM);
+        for (int q = 0; q < 4; ++q) tma_prefetch_l2(&args.dy, rank * kDySlice + i * 128 + 32 * q, cid * UR + j * C::kBM);
   }
   grid_dependency_wait();      // predecessor done: its outputs may be this kernel's inputs
   grid_dependents_launch();
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
               const int s = take(C::kSlotBytes);
               if (s >= 0) {
                 const uint32_t st = base + s * C::kSlotBytes;
-                const int n0 = sl * kDySlice + i * 128, m0 = ch * kDyChunk + j * C::kBM;
+                const int n0 = sl * kDySlice + i * 128, m0 = ch * UR + j * C::kBM;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tma_load(st + q * C::kSlabBytes, &args.dy, full(s), n0 + 32 * q, m0, pol_stream);
                 tma_load(st + C::kTileBytes, &args.b, full(s), 0, n0, pol_keep);
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
     uint8_t* stg_ptr = gbase + C::kStgOff + (warp - 2) * C::kStg * C::kStgBytes;
     uint8_t* dutile = gbase + C::kDuOff;
     const uint64_t pol_out = policy_evict_first();
-    const int R = args.R, rows_per_rank = 2 * C::kBM / CL;
+    const int R = args.R, rows_per_rank = UR / CL;
     Ring t;
     int sidx = 0, k = 0;
     for (int ch = cid; ch < n_ch; ch += ncl, ++k) {
@@ -371,15 +374,22 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
               for (int c = 0; c < C::kCPT; ++c) dun[c] = __fadd_rn(du_stk[j][l][c], dun[c]);
             }
             if (merged && i == C::kSliceTiles - 1) {
-              const int row = ch * kDyChunk + j * C::kBM + tr;
+              const int row = ch * UR + j * C::kBM + tr;
               if (ok_all && j < nrt && row < M) {
                 float4* dst = reinterpret_cast<float4*>(args.du_part + (size_t(sl) * M + row) * RP + h * C::kCPT);
                 dst[0] = make_float4(dun[0], dun[1], dun[2], dun[3]);
                 dst[1] = make_float4(dun[4], dun[5], dun[6], dun[7]);
               }
             }
-            // dB of column tile i: the chunk's two row tiles
-            if (j == 0) {
+            // dB of column tile i: the unit's row tiles (one: its tree is the partial; two: added)
+            if (UR == C::kBM) {
+              const int col = sl * kDySlice + i * 128 + tr;
+              if (j == 0 && ok_all && i < nnt && col < N) {
+                float* dst = args.db_part + (size_t(ch) * RP + h * C::kCPT) * N + col;
+#pragma unroll
+                for (int c = 0; c < C::kCPT; ++c) dst[size_t(c) * N] = dbn[c];
+              }
+            } else if (j == 0) {
 #pragma unroll
               for (int c = 0; c < C::kCPT; ++c) db_first[c] = dbn[c];
             } else {
@@ -397,20 +407,26 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
       named_bar(1, 32 * C::kEpiWarps);
       if (et == 0)
         for (int p = 0; p < CL; ++p) mbar_arrive_peer(peer_addr(duready(k & 1), uint32_t(p)));
-      const bool okx = wait_cluster(duready(k & 1), uint32_t(k >> 1) & 1u, ab, 88);
+      const bool okx = __all_sync(0xffffffffu, wait_cluster(duready(k & 1), uint32_t(k >> 1) & 1u, ab, 88));
       // ---- dU rows of the chunk: canonical tree over the slices, BF16, into the swizzled tile
       // (32-byte rows: chunk ^ ((row / 4) % 2)); rank r stores its share of du
       // Without phase C a CTA forms its share only.
-      const int i0 = PC ? 0 : rank * rows_per_rank, ni = PC ? 2 * C::kBM : rows_per_rank;
-      for (int it = et; it < ni * (RP / 8); it += 32 * C::kEpiWarps) {
+      // More than 8 slices: four consecutive lanes per value (the rows kernel's four-lane tree, the
+      // same bits), all four active together (the conditions below are the same for the four).
+      const int i0 = PC ? 0 : rank * rows_per_rank, ni = PC ? UR : rows_per_rank;
+      const int L = S > 8 ? 4 : 1, l4 = et & (L - 1);
+      const unsigned gmask = 0xFu << (lane & 28u);
+      for (int it = et / L; it < ni * (RP / 8); it += 32 * C::kEpiWarps / L) {
         const int i = i0 + it / (RP / 8), gg = it % (RP / 8);
-        const int row = ch * kDyChunk + i;
+        const int row = ch * UR + i;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (okx && gg < R / 8 && row < M) {
-          v = slices_to_bf16x8(args.du_part + size_t(row) * RP + gg * 8, size_t(M) * RP, S);
-          if (i / rows_per_rank == rank) *reinterpret_cast<uint4*>(args.du + size_t(row) * R + gg * 8) = v;
+          const float* pr = args.du_part + size_t(row) * RP + gg * 8;
+          v = L == 4 ? slices_to_bf16x8_4lanes(pr, size_t(M) * RP, S, l4, gmask) : slices_to_bf16x8(pr, size_t(M) * RP, S);
+          if (l4 == 0 && i / rows_per_rank == rank) *reinterpret_cast<uint4*>(args.du + size_t(row) * R + gg * 8) = v;
         }
-        if constexpr (PC) *reinterpret_cast<uint4*>(dutile + i * 32 + ((gg ^ ((i >> 2) & 1)) << 4)) = v;
+        if constexpr (PC)
+          if (l4 == 0) *reinterpret_cast<uint4*>(dutile + i * 32 + ((gg ^ ((i >> 2) & 1)) << 4)) = v;
       }
       fence_proxy_async();     // generic writes of the dU tile before the tensor core reads it
       named_bar(1, 32 * C::kEpiWarps);
@@ -563,7 +579,9 @@ cudaError_t bwd_cluster_max_clusters(bool phase_c, int cl, int* n) {
 
 cudaError_t launch_bwd_cluster(bool phase_c, BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
   a.S = int(ceil_div(a.N, kDySlice));
-  a.n_ch = int(ceil_div(a.M, kDyChunk));
+  if (phase_c) a.unit_rows = kDyChunk;
+  if (a.unit_rows != kDyChunk && a.unit_rows != 128) return cudaErrorInvalidValue;
+  a.n_ch = int(ceil_div(a.M, a.unit_rows));
   a.n_kt = int(ceil_div(a.K, 128));
   if (cl < 1 || cl > 8 || (256 % cl) != 0 || ncl < 1) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];

@@ -334,20 +334,26 @@ __global__ void __launch_bounds__(FcCfg<RP, UP>::kThreads, 1)
       named_bar(1, 32 * C::kEpiWarps);
       if (et == 0)
         for (int p = 0; p < CL; ++p) mbar_arrive_peer(peer_addr(uready(k & 1), uint32_t(p)));
-      const bool okx = wait_cluster(uready(k & 1), uint32_t(k >> 1) & 1u, ab, 67);
+      const bool okx = __all_sync(0xffffffffu, wait_cluster(uready(k & 1), uint32_t(k >> 1) & 1u, ab, 67));
       // (3) the U rows of the tile: canonical tree over the slices, BF16, into the swizzled U
       // tile (padded columns and rows past M are zero); rank r also stores its share of u.
       // Without the expansion a CTA forms its share only.
+      // More than 8 slices: four consecutive lanes per value (the rows kernel's four-lane tree, the
+      // same bits), all four active together (the conditions below are the same for the four).
       const int i0 = UP ? 0 : rank * rows_per_rank, ni = UP ? C::kBM : rows_per_rank;
-      for (int it = et; it < ni * (RP / 8); it += 32 * C::kEpiWarps) {
+      const int L = S > 8 ? 4 : 1, l4 = et & (L - 1);
+      const unsigned gmask = 0xFu << (lane & 28u);
+      for (int it = et / L; it < ni * (RP / 8); it += 32 * C::kEpiWarps / L) {
         const int i = i0 + it / (RP / 8), gg = it % (RP / 8);
         const int row = mt * C::kBM + i;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (okx && gg < R / 8 && row < M) {
-          v = slices_to_bf16x8(args.part + size_t(row) * RP + gg * 8, size_t(M) * RP, S);
-          if (i / rows_per_rank == rank) *reinterpret_cast<uint4*>(args.u + size_t(row) * R + gg * 8) = v;
+          const float* pr = args.part + size_t(row) * RP + gg * 8;
+          v = L == 4 ? slices_to_bf16x8_4lanes(pr, size_t(M) * RP, S, l4, gmask) : slices_to_bf16x8(pr, size_t(M) * RP, S);
+          if (l4 == 0 && i / rows_per_rank == rank) *reinterpret_cast<uint4*>(args.u + size_t(row) * R + gg * 8) = v;
         }
-        if constexpr (UP) *reinterpret_cast<uint4*>(utile + utile_offset<RP>(i, gg)) = v;
+        if constexpr (UP)
+          if (l4 == 0) *reinterpret_cast<uint4*>(utile + utile_offset<RP>(i, gg)) = v;
       }
       fence_proxy_async();     // generic writes of the U tile before the tensor core reads it
       named_bar(1, 32 * C::kEpiWarps);

@@ -185,6 +185,10 @@ struct BcArgs {
   __nv_bfloat16* du;                // [M][R]
   int M, K, N, R, S, n_ch, n_kt;    // S, n_ch, n_kt: set by the launcher
   float alpha;
+  // Rows per unit (phase_c false only; 256 with phase C): 256, a chunk, or 128, one row tile, whose
+  // dB tree is then the unit's partial -- db_part holds ceil(M / unit_rows) partials, and the
+  // combine's canonical tree over them first adds the two tiles of each chunk.
+  int unit_rows;
 };
 // phase_c = false: phase A and the dU rows only (the dX, dA and combine launches follow; the x, a
 // and dx maps are then unused).

@@ -268,7 +268,9 @@ lora_status lora_delta_set_profile_events(void *const *events, int count);
  *     single-site backward of R <= 16 as cluster reductions where its 256-row
  *     chunks give at least three quarters of the SMs a CTA (on a GB300, M of
  *     about 7300 rows and more with clusters of 4), else as separate launches --
- *     the faster choice at every shape measured.
+ *     the faster choice at every shape measured. (Under
+ *     LORA_SCHEDULE_CLUSTER_REDUCE, batches with too few chunks for that take
+ *     128-row units.)
  * The cluster schedules cover the single-site forward of R <= 32 and the
  * single-site backward of R <= 16 whose per-CTA share of a tile is at most
  * 32 MiB of input; other calls (grouped calls included) run the separate

@@ -232,10 +232,11 @@ def test_launch_plan():
     schedule keeps the forward's separate launches and takes the backward's cluster reductions
     where its 256-row chunks give at least three quarters of the SMs a CTA."""
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
-    big = (256 * ((3 * nsm + 15) // 16) + 256)   # enough chunks for clusters of 4
+    big = 256 * ((3 * nsm + 15) // 16) + 256     # enough 256-row chunks for clusters of 4
     assert ld.lora_delta_plan(False, 8192, 4096, 4096, 16) == (SEP, 3)
     assert ld.lora_delta_plan(True, big, 4096, 4096, 16) == (RED, 4)
     assert ld.lora_delta_plan(True, 256, 4096, 4096, 16) == (SEP, 5)
+    assert ld.lora_delta_plan(True, 4096, 5120, 17408, 16) == (SEP, 5)     # too few 256-row chunks
     assert ld.lora_delta_plan(True, big, 4096, 4096, 32) == (SEP, 6)       # rank above 16: separate
     assert ld.lora_delta_plan(False, 0, 4096, 4096, 16) == (SEP, 0)
     with schedule(ONE, 4):
