@@ -95,7 +95,11 @@ __device__ __forceinline__ void bc_leaves4(uint32_t taddr, bool ok, float (&o)[8
 
 // PC = false: phase A and the dU rows only (each CTA forms and stores its share of the chunk's
 // rows); dX and the dA partials then run as the separate up-projection and weight-gradient launches.
-template <bool PC>
+// UR: rows of a unit, a 256-row chunk or (PC = false only) one 128-row tile, whose dB tree is then
+// the unit's partial (the combine's first level adds the two tiles of each chunk). L: lanes that
+// share one value of the dU rows step (4 where there are more than 8 slices, else 1). Both are
+// compile-time so that the common case carries no registers for the others.
+template <bool PC, int UR, int L>
 __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
     bwd_cluster_kernel(const __grid_constant__ BcArgs args, uint32_t* status) {
   using C = BcCfg<PC>;
@@ -121,9 +125,7 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
   const int CL = int(cluster_size()), rank = int(cluster_rank());
   const int cid = int(cluster_index()), ncl = int(cluster_count());
   const int M = args.M, K = args.K, N = args.N, S = args.S, n_ch = args.n_ch;
-  // rows of a unit: a 256-row chunk, or (cluster reductions only) one 128-row tile, whose dB tree is
-  // then the unit's partial (the combine's first level adds the two tiles of each chunk)
-  const int UR = PC ? kDyChunk : args.unit_rows;
+  static_assert((UR == kDyChunk || (!PC && UR == C::kBM)) && (L == 1 || L == 4), "unit shapes");
   const int n_kt = PC ? args.n_kt : 0;   // phase C column tiles (none without phase C)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSlots; ++s) {
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
       // More than 8 slices: four consecutive lanes per value (the rows kernel's four-lane tree, the
       // same bits), all four active together (the conditions below are the same for the four).
       const int i0 = PC ? 0 : rank * rows_per_rank, ni = PC ? UR : rows_per_rank;
-      const int L = S > 8 ? 4 : 1, l4 = et & (L - 1);
+      const int l4 = et & (L - 1);
       const unsigned gmask = 0xFu << (lane & 28u);
       for (int it = et / L; it < ni * (RP / 8); it += 32 * C::kEpiWarps / L) {
         const int i = i0 + it / (RP / 8), gg = it % (RP / 8);
@@ -567,14 +569,28 @@ static cudaLaunchConfig_t bc_config(int cl, int ncl, cudaStream_t st, cudaLaunch
   return cfg;
 }
 
+template <bool PC, int UR, int L>
+static cudaError_t bc_launch(BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = bc_config<PC>(cl, ncl, st, attr, 2);
+  return cudaLaunchKernelEx(&cfg, bwd_cluster_kernel<PC, UR, L>, a, status);
+}
+
+template <bool PC, int UR, int L>
+static cudaError_t bc_prepare() {
+  return cudaFuncSetAttribute(bwd_cluster_kernel<PC, UR, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(BcCfg<PC>::kSmem));
+}
+
+// every instance has the same threads, shared memory and one CTA per SM: one stands for all
 cudaError_t bwd_cluster_max_clusters(bool phase_c, int cl, int* n) {
   cudaLaunchAttribute attr[2];
   if (phase_c) {
     cudaLaunchConfig_t cfg = bc_config<true>(cl, 1, nullptr, attr, 1);
-    return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel<true>, &cfg);
+    return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel<true, kDyChunk, 1>, &cfg);
   }
   cudaLaunchConfig_t cfg = bc_config<false>(cl, 1, nullptr, attr, 1);
-  return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel<false>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, bwd_cluster_kernel<false, kDyChunk, 1>, &cfg);
 }
 
 cudaError_t launch_bwd_cluster(bool phase_c, BcArgs& a, uint32_t* status, int cl, int ncl, cudaStream_t st) {
@@ -584,21 +600,22 @@ cudaError_t launch_bwd_cluster(bool phase_c, BcArgs& a, uint32_t* status, int cl
   a.n_ch = int(ceil_div(a.M, a.unit_rows));
   a.n_kt = int(ceil_div(a.K, 128));
   if (cl < 1 || cl > 8 || (256 % cl) != 0 || ncl < 1) return cudaErrorInvalidValue;
-  cudaLaunchAttribute attr[2];
-  if (phase_c) {
-    cudaLaunchConfig_t cfg = bc_config<true>(cl, ncl, st, attr, 2);
-    return cudaLaunchKernelEx(&cfg, bwd_cluster_kernel<true>, a, status);
-  }
-  cudaLaunchConfig_t cfg = bc_config<false>(cl, ncl, st, attr, 2);
-  return cudaLaunchKernelEx(&cfg, bwd_cluster_kernel<false>, a, status);
+  const bool many = a.S > 8;   // four lanes per value in the dU rows step
+  if (phase_c)
+    return many ? bc_launch<true, kDyChunk, 4>(a, status, cl, ncl, st) : bc_launch<true, kDyChunk, 1>(a, status, cl, ncl, st);
+  if (a.unit_rows == kDyChunk)
+    return many ? bc_launch<false, kDyChunk, 4>(a, status, cl, ncl, st) : bc_launch<false, kDyChunk, 1>(a, status, cl, ncl, st);
+  return many ? bc_launch<false, 128, 4>(a, status, cl, ncl, st) : bc_launch<false, 128, 1>(a, status, cl, ncl, st);
 }
 
 cudaError_t prepare_bwd_cluster() {
-  const cudaError_t e = cudaFuncSetAttribute(bwd_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(BcCfg<true>::kSmem));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(bwd_cluster_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(BcCfg<false>::kSmem));
+  cudaError_t e;
+  if ((e = bc_prepare<true, kDyChunk, 1>()) != cudaSuccess) return e;
+  if ((e = bc_prepare<true, kDyChunk, 4>()) != cudaSuccess) return e;
+  if ((e = bc_prepare<false, kDyChunk, 1>()) != cudaSuccess) return e;
+  if ((e = bc_prepare<false, kDyChunk, 4>()) != cudaSuccess) return e;
+  if ((e = bc_prepare<false, 128, 1>()) != cudaSuccess) return e;
+  return bc_prepare<false, 128, 4>();
 }
 
 }  // namespace lora
