@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "LoRA delta fwd+bwd ms & HBM GB/s (%roofline) at M=8192 K=N=4096 R=16"
 # kernels of one step: the forward's three launches, the backward's five (R <= 16)
 KERNELS_FWD = ["down U", "rows U", "up dY_lora"]
-KERNELS_BWD = ["dy dU+dB", "rows dU+dB", "up dX", "wgrad dA", "combine dA"]
+KERNELS_BWD = ["dy dU+dB", "rows dU+dB", "dX+dA", "combine dA"]   # rank <= 16: dX and dA in one launch
 KERNELS = KERNELS_FWD + KERNELS_BWD
 N_FWD = len(KERNELS_FWD)
 FUSED_FWD = "fwd down+rows+up"   # lora_delta_fwd_fused: the same three steps in one launch
@@ -69,8 +69,8 @@ def algorithmic_bytes(M, K, N, R):
         "dy dU+dB": M * N * bf + N * R * bf + M * R * bf            # dY (read once), B, U -> dU, dB partials
                     + N * R * f4,                                   # (dB written by the combine)
         "rows dU+dB": M * R * bf,                                   # -> dU (and dB from its chunk partials)
-        "up dX": M * R * bf + R * K * bf + M * K * f4,              # dU, A -> dX
-        "wgrad dA": M * K * bf + M * R * bf + R * K * f4,           # X, dU -> dA partials (dA written by the combine)
+        "dX+dA": M * K * bf + M * R * bf + R * K * bf               # X, dU, A (read once for both)
+                 + M * K * f4 + R * K * f4,                         # -> dX, dA partials
         "combine dA": 0,
     }
 
@@ -95,13 +95,12 @@ def measured_peaks():
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
 NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
-    "down U": {"bytes": 72_015_104, "src_hash": "cd87db2509e13a82"},
-    "rows U": {"bytes": 45_824, "src_hash": "cd87db2509e13a82"},
-    "up dY_lora": {"bytes": 123_836_160, "src_hash": "cd87db2509e13a82"},
-    "dy dU+dB+rows dU (cluster)": {"bytes": 79_399_680, "src_hash": "cd87db2509e13a82"},
-    "up dX": {"bytes": 126_049_280, "src_hash": "cd87db2509e13a82"},
-    "wgrad dA": {"bytes": 74_881_536, "src_hash": "cd87db2509e13a82"},
-    "combine dA+dB": {"bytes": 817_408, "src_hash": "cd87db2509e13a82"},
+    "down U": {"bytes": 72_533_760, "src_hash": "73d76538dbbb08b5"},
+    "rows U": {"bytes": 85_504, "src_hash": "73d76538dbbb08b5"},
+    "up dY_lora": {"bytes": 126_194_176, "src_hash": "73d76538dbbb08b5"},
+    "dy dU+dB+rows dU (cluster)": {"bytes": 80_356_864, "src_hash": "73d76538dbbb08b5"},
+    "dX+dA": {"bytes": 198_473_472, "src_hash": "73d76538dbbb08b5"},
+    "combine dA+dB": {"bytes": 4_179_968, "src_hash": "73d76538dbbb08b5"},
 }
 
 
@@ -349,7 +348,7 @@ def fwd_variants(ld, Xs, A, B, alpha, M, K, N, R, dev, peak, steps=40, reps=25):
 SCHEDULES = [
     ("separate", 0, 0, KERNELS_FWD, KERNELS_BWD),
     ("cluster_reduce_cl4", 1, 4, ["down+rows U (cluster)", "up dY_lora"],
-     ["dy dU+dB+rows dU (cluster)", "up dX", "wgrad dA", "combine dA+dB"]),
+     ["dy dU+dB+rows dU (cluster)", "dX+dA", "combine dA+dB"]),
     ("cluster_single_cl2", 2, 2, ["fwd (cluster)"], ["bwd (cluster)", "combine dA+dB"]),
     ("cluster_single_cl4", 2, 4, ["fwd (cluster)"], ["bwd (cluster)", "combine dA+dB"]),
 ]
@@ -364,7 +363,7 @@ def schedule_kernels(fwd_schedule, bwd_schedule, M, K, N, R):
     kb.update({"down+rows U (cluster)": alg["down U"] + alg["rows U"],
                "dy dU+dB+rows dU (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"], "combine dA+dB": 0,
                "fwd (cluster)": alg["down U"] + alg["rows U"] + alg["up dY_lora"],
-               "bwd (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"] + alg["up dX"] + alg["wgrad dA"]})
+               "bwd (cluster)": alg["dy dU+dB"] + alg["rows dU+dB"] + alg["dX+dA"]})
     by = {sched: (kf, kbw) for _, sched, _, kf, kbw in SCHEDULES}
     return by[fwd_schedule][0], by[bwd_schedule][1], kb
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "liblora_delta.so")
 BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
-SOURCES = ["api.cu", "down.cu", "up.cu", "fwd_fused.cu", "fwd_cluster.cu", "bwd_cluster.cu", "wgrad.cu", "dy.cu", "rows.cu", "combine.cu", "noalloc.cu",
+SOURCES = ["api.cu", "down.cu", "up.cu", "fwd_fused.cu", "fwd_cluster.cu", "bwd_cluster.cu", "dxda.cu", "wgrad.cu", "dy.cu", "rows.cu", "combine.cu", "noalloc.cu",
            "dvf32.cu", "exact.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", *GENCODE]

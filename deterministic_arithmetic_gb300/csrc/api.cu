@@ -127,7 +127,7 @@ lora_status device_ready(int* num_sms) {
     if (d.usable) {
       if (prepare_down() != cudaSuccess || prepare_up() != cudaSuccess || prepare_wgrad() != cudaSuccess ||
           prepare_dy() != cudaSuccess || prepare_exact() != cudaSuccess || prepare_fwd_fused() != cudaSuccess ||
-          prepare_fwd_cluster() != cudaSuccess || prepare_bwd_cluster() != cudaSuccess) {
+          prepare_fwd_cluster() != cudaSuccess || prepare_bwd_cluster() != cudaSuccess || prepare_dxda() != cudaSuccess) {
         d.probed = false;
         return LORA_ERR_CUDA;
       }
@@ -449,14 +449,15 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   DownArgs dargs{};
   WgArgs bargs{}, aargs{};
   UpArgs uargs{};
+  XaArgs xargs{};
   RowsArgs rargs{};
   CombineJobs da_jobs{}, db_jobs{};
-  yargs.n = dargs.n = bargs.n = aargs.n = uargs.n = rargs.n = m;
+  yargs.n = dargs.n = bargs.n = aargs.n = uargs.n = xargs.n = rargs.n = m;
   uargs.R = rargs.R = int(R);
   rargs.RP = RP;
   da_jobs.n = db_jobs.n = m;
   size_t off = kControlBytes;
-  int64_t n_dy = 0, n_du = 0, n_db = 0, n_up = 0, n_da = 0;
+  int64_t n_dy = 0, n_du = 0, n_db = 0, n_up = 0, n_da = 0, n_xa = 0;
   for (int j = 0; j < m; ++j) {
     const BwdIn& p = in[active[j]];
     const BwdLayout L = bwd_layout(p.M, p.K, p.N, R);
@@ -513,14 +514,30 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     wa.M = M;
     wa.Cw = K;
     wa.alpha = 1.0f;
+    xargs.s[j] = XaSite{wa.in, q.b, q.a, q.out, dapart, M, K, 0, 0, 0};
     da_jobs.j[j] = CombineJob{dapart, p.da, C, K, int(R), RP, 0};
     db_jobs.j[j] = CombineJob{dbpart, p.db, C, N, int(R), RP, 1};
     n_up += up_units(M, K, RP);
     n_da += wgrad_units(M, K, RP);
+    n_xa += dxda_units(M, K);
   }
   if (off > workspace_bytes) return LORA_ERR_WORKSPACE;   // every region inside the workspace
   Recorder rec(st);
   rec.mark();
+  // dX and the dA chunk partials: one pass over x for padded rank 16, else the up-projection
+  // and weight-gradient launches
+  auto dx_da = [&]() -> bool {
+    if (RP == 16) {
+      if (launch_dxda(xargs, status, grid_for(n_xa, nsm), st) != cudaSuccess) return false;
+      rec.mark();
+      return true;
+    }
+    if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return false;
+    rec.mark();
+    if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return false;
+    rec.mark();
+    return true;
+  };
   const int bcl = cluster_of_setting();
   const int sched = bwd_schedule(m, RP, in[active[0]].M, in[active[0]].N, nsm);
   if (sched != LORA_SCHEDULE_SEPARATE) {
@@ -554,12 +571,7 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
     const int ncl = int(std::min<int64_t>(mc, n_units));
     if (launch_bwd_cluster(single, ba, status, bcl, ncl, st) != cudaSuccess) return LORA_ERR_CUDA;
     rec.mark();
-    if (!single) {
-      if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
-      rec.mark();
-      if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
-      rec.mark();
-    }
+    if (!single && !dx_da()) return LORA_ERR_CUDA;
     CombineJobs jobs{};
     jobs.n = 2;
     jobs.j[0] = da_jobs.j[0];
@@ -585,10 +597,7 @@ lora_status bwd_group(const BwdIn* in, int n, int64_t R, void* workspace, size_t
   // canonical tree over the chunk partials just written (still in L2)
   if (launch_rows(rargs, &db_jobs, nsm, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
-  if (launch_up(RP, true, false, uargs, status, grid_for(n_up, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
-  rec.mark();
-  if (launch_wgrad(RP, false, aargs, status, grid_for(n_da, nsm), st) != cudaSuccess) return LORA_ERR_CUDA;
-  rec.mark();
+  if (!dx_da()) return LORA_ERR_CUDA;
   // dA: canonical tree over the chunk partials
   if (launch_combine(da_jobs, st) != cudaSuccess) return LORA_ERR_CUDA;
   rec.mark();
@@ -864,7 +873,9 @@ lora_status lora_delta_plan(int backward, int64_t M, int64_t K, int64_t N, int64
   } else {
     const int sc = bwd_schedule(1, RP, M, N, nsm);
     *schedule = sc;
-    *launches = sc == LORA_SCHEDULE_CLUSTER_SINGLE ? 2 : (sc == LORA_SCHEDULE_CLUSTER_REDUCE ? 4 : (RP == 16 ? 5 : 6));
+    // padded rank 16: dX and dA in one launch (cluster reductions: dy + rows, dX + dA, combine;
+    // separate: dy, rows, dX + dA, combine); above: dU, dB, rows, dX, dA, combine
+    *launches = sc == LORA_SCHEDULE_CLUSTER_SINGLE ? 2 : (sc == LORA_SCHEDULE_CLUSTER_REDUCE ? 3 : (RP == 16 ? 4 : 6));
   }
   return LORA_OK;
 }

@@ -91,6 +91,15 @@ struct WgSite {
 };
 using WgArgs = Sites<WgSite, kMaxSites>;
 
+// dX and the dA chunk partials from the finished du rows in one pass (padded rank 16).
+struct XaSite {
+  CUtensorMap x, a, du, dx;   // x 64 x 64 and a RP x 64 boxes (128-byte swizzle); du 128 x RP (row span);
+                              // dx 32 x 32 FP32 (128-byte swizzle)
+  float* da_part;             // [n_ch][RP][K]
+  int M, K, n_kt, n_ch, u0;
+};
+using XaArgs = Sites<XaSite, kMaxSites>;
+
 // Launch with programmatic stream serialization (the kernel calls
 // grid_dependency_wait() before its first global-memory access).
 template <typename... KArgs, typename... Args>
@@ -126,6 +135,11 @@ cudaError_t launch_up(int RP, bool dx, bool y_bf16, UpArgs& args, uint32_t* stat
 cudaError_t launch_dy(DyArgs& args, uint32_t* status, int grid, cudaStream_t st);
 // args: sites filled in except n_ct, n_ch, u0 and total (set here)
 cudaError_t launch_wgrad(int RP, bool dv, WgArgs& args, uint32_t* status, int grid, cudaStream_t st);
+
+// du: complete when the launch starts (written by the preceding kernel). args: sites filled in
+// except n_kt, n_ch, u0 and total (set here).
+cudaError_t launch_dxda(XaArgs& args, uint32_t* status, int grid, cudaStream_t st);
+inline int64_t dxda_units(int64_t M, int64_t K) { return ceil_div(M, kWgradChunk) * ceil_div(K, 128); }
 
 // The BF16 rows of U (or dU) from the slice partials of the down (or dy) kernel: for every row
 // and every group of 8 columns, the canonical pairwise tree over the S slice partials, rounded
@@ -245,5 +259,6 @@ cudaError_t prepare_down();
 cudaError_t prepare_up();
 cudaError_t prepare_wgrad();
 cudaError_t prepare_dy();
+cudaError_t prepare_dxda();
 
 }  // namespace lora

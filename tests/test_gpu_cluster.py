@@ -234,9 +234,9 @@ def test_launch_plan():
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     big = 256 * ((3 * nsm + 15) // 16) + 256     # enough 256-row chunks for clusters of 4
     assert ld.lora_delta_plan(False, 8192, 4096, 4096, 16) == (SEP, 3)
-    assert ld.lora_delta_plan(True, big, 4096, 4096, 16) == (RED, 4)
-    assert ld.lora_delta_plan(True, 256, 4096, 4096, 16) == (SEP, 5)
-    assert ld.lora_delta_plan(True, 4096, 5120, 17408, 16) == (SEP, 5)     # too few 256-row chunks
+    assert ld.lora_delta_plan(True, big, 4096, 4096, 16) == (RED, 3)
+    assert ld.lora_delta_plan(True, 256, 4096, 4096, 16) == (SEP, 4)
+    assert ld.lora_delta_plan(True, 4096, 5120, 17408, 16) == (SEP, 4)     # too few 256-row chunks
     assert ld.lora_delta_plan(True, big, 4096, 4096, 32) == (SEP, 6)       # rank above 16: separate
     assert ld.lora_delta_plan(False, 0, 4096, 4096, 16) == (SEP, 0)
     with schedule(ONE, 4):
@@ -245,7 +245,7 @@ def test_launch_plan():
         assert ld.lora_delta_plan(True, 300, 1032, 520, 16) == (ONE, 2)
     with schedule(RED, 2):
         assert ld.lora_delta_plan(False, 8192, 4096, 4096, 16) == (RED, 2)
-        assert ld.lora_delta_plan(True, 8192, 4096, 4096, 16) == (RED, 4)
-        assert ld.lora_delta_plan(True, 8192, 4096, 1 << 20, 16) == (SEP, 5)   # a CTA's share too large
+        assert ld.lora_delta_plan(True, 8192, 4096, 4096, 16) == (RED, 3)
+        assert ld.lora_delta_plan(True, 8192, 4096, 1 << 20, 16) == (SEP, 4)   # a CTA's share too large
     with pytest.raises(ld.LoraDeltaError):
         ld.lora_delta_plan(True, 8192, 4095, 4096, 16)                      # K not a multiple of 8
