@@ -95,12 +95,12 @@ def measured_peaks():
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
 NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
-    "down U": {"bytes": 72_533_760, "src_hash": "73d76538dbbb08b5"},
-    "rows U": {"bytes": 85_504, "src_hash": "73d76538dbbb08b5"},
-    "up dY_lora": {"bytes": 126_194_176, "src_hash": "73d76538dbbb08b5"},
-    "dy dU+dB+rows dU (cluster)": {"bytes": 80_356_864, "src_hash": "73d76538dbbb08b5"},
-    "dX+dA": {"bytes": 198_473_472, "src_hash": "73d76538dbbb08b5"},
-    "combine dA+dB": {"bytes": 4_179_968, "src_hash": "73d76538dbbb08b5"},
+    "down U": {"bytes": 72_628_224, "src_hash": "7a64c8623babe949"},
+    "rows U": {"bytes": 118_016, "src_hash": "7a64c8623babe949"},
+    "up dY_lora": {"bytes": 126_273_792, "src_hash": "7a64c8623babe949"},
+    "dy dU+dB+rows dU (cluster)": {"bytes": 80_580_352, "src_hash": "7a64c8623babe949"},
+    "dX+dA": {"bytes": 198_195_456, "src_hash": "7a64c8623babe949"},
+    "combine dA+dB": {"bytes": 4_429_568, "src_hash": "7a64c8623babe949"},
 }
 
 
@@ -487,7 +487,7 @@ def bwd_variants(ld, Xs, DYs, A, B, alpha, M, K, N, R, dev, steps=40, reps=25):
         nbytes = M * N * dsz + N * R * bf + M * R * bf + M * K * bf + R * K * bf + M * K * f4 + 2 * M * R * bf \
             + R * K * f4 + N * R * f4
         out[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                     "launches_per_step": 5 if dsz == bf else 6}
+                     "launches_per_step": ld.lora_delta_plan(True, M, K, N, R)[1] + (0 if dsz == bf else 1)}
         assert ld.lora_delta_device_status(wb) == 0
     return out
 
@@ -672,7 +672,11 @@ def grouped_variants(ld, dev, peak, steps=10, reps=20):
 
     out = {}
     nbytes = sum(step_bytes(M, s["x"].shape[1], s["b"].shape[0], R) for s in sites)
-    for name, fn, launches in (("mlp_fc1_fc2_separate", separate, 2 * (3 + 5)), ("mlp_fc1_fc2_grouped", grouped, 3 + 5)):
+    # single-site calls: each call's launch plan; a grouped call takes the separate launches once
+    # for all sites (R <= 16: down, rows, up; dy, rows, dX + dA, combine)
+    n_sep = sum(ld.lora_delta_plan(False, M, s["x"].shape[1], s["b"].shape[0], R)[1]
+                + ld.lora_delta_plan(True, M, s["x"].shape[1], s["b"].shape[0], R)[1] for s in sites)
+    for name, fn, launches in (("mlp_fc1_fc2_separate", separate, n_sep), ("mlp_fc1_fc2_grouped", grouped, 3 + 4)):
         for _ in range(3):
             fn(torch.cuda.current_stream(dev))
         torch.cuda.synchronize()

@@ -45,7 +45,7 @@ struct XaCfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kCPT = RP / 2;                      // dA columns of R per epilogue thread
-  static constexpr int kStg = 2, kStgBytes = 32 * 32 * 4;  // dX staging boxes per epilogue warp
+  static constexpr int kStg = 1, kStgBytes = 32 * 32 * 4;  // dX staging boxes per epilogue warp (two measured slower)
   static constexpr size_t kStgOff = size_t(kSlots) * kSlotBytes;
   static constexpr size_t kArea = kStgOff + size_t(kEpiWarps) * kStg * kStgBytes;
   // mbarriers: slots (full, empty), TMEM (full, empty), drain, never
