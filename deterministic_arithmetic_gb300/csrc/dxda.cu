@@ -124,15 +124,6 @@ __global__ void __launch_bounds__(XaCfg::kThreads, 1)
       prefetch_map(&args.s[i].du);
       prefetch_map(&args.s[i].dx);
     }
-    if (int(blockIdx.x) < total) {
-      // the first x tile of this CTA, into L2 while the predecessor drains (x is no output of it)
-      const int u = int(blockIdx.x);
-      const XaSite& P = site(u);
-      const int kt = (u - P.u0) % P.n_kt, ch = (u - P.u0) / P.n_kt;
-      for (int hh = 0; hh < halves(P, ch); ++hh)
-        for (int h2 = 0; h2 < 2; ++h2)
-          for (int q = 0; q < 2; ++q) tma_prefetch_l2(&P.x, kt * C::kBK + 64 * q, ch * kWgradChunk + hh * C::kBM + 64 * h2);
-    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -142,6 +133,34 @@ __global__ void __launch_bounds__(XaCfg::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+  // the x tile [128 rows][128 columns] (two 64-row halves: columns 0..63, then 64..127) and the
+  // a columns of one step into slot st
+  auto copy_xa = [&](uint32_t st, uint32_t bar, const XaSite& P, int k0, int m0) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      tma_load(st + h2 * 16384u, &P.x, bar, k0, m0 + 64 * h2, pol_stream);
+      tma_load(st + h2 * 16384u + 8192u, &P.x, bar, k0 + 64, m0 + 64 * h2, pol_stream);
+    }
+    tma_load(st + C::kXBytes, &P.a, bar, k0, 0, pol_keep);                 // a[0..RP)[k0 .. +63]
+    tma_load(st + C::kXBytes + RP * 128, &P.a, bar, k0 + 64, 0, pol_keep); // a[0..RP)[k0+64 .. +127]
+  };
+  // x and a are inputs of the call and no output of the launches before this one, whose CTAs
+  // start their dependents only after their own dependency wait, so every earlier writer of x
+  // and a has completed when this kernel starts: the first ring slots get their x and a copies
+  // before the dependency wait (while the predecessor's last CTAs finish), their du rows (the
+  // predecessor's output) after it. Not with a test hook set: the stall comes first.
+  int pre = 0;
+  if (warp == 0 && lane == 0 && !stall_requested(status, kKindWgrad) && !stall_requested(status, kKindUp)) {
+    for (int u = blockIdx.x; u < total && pre < C::kSlots; u += gridDim.x) {
+      const XaSite& P = site(u);
+      const int kt = (u - P.u0) % P.n_kt, ch = (u - P.u0) / P.n_kt;
+      for (int hh = 0; hh < halves(P, ch) && pre < C::kSlots; ++hh, ++pre) {
+        mbar_expect_tx(full(pre), uint32_t(C::kSlotBytes));   // fresh slots: free, phase 0
+        copy_xa(base + pre * C::kSlotBytes, full(pre), P, kt * C::kBK, ch * kWgradChunk + hh * C::kBM);
+      }
+    }
+  }
   grid_dependency_wait();      // predecessor done: the du rows are complete
   grid_dependents_launch();
   const Abort ab = make_abort(abort_flag, status);
@@ -151,28 +170,25 @@ __global__ void __launch_bounds__(XaCfg::kThreads, 1)
     if (lane == 0) {
       if (stall_requested(status, kKindWgrad)) stall_wait(never, ab, 29);   // test hooks: a wait that runs out
       if (stall_requested(status, kKindUp)) stall_wait(never, ab, 10);
-      const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
       Ring r;
       uint32_t issued = 0, parities = 0;
+      int i = 0;   // step index of this CTA
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const XaSite& P = site(u);
         const int kt = (u - P.u0) % P.n_kt, ch = (u - P.u0) / P.n_kt;
         const int k0 = kt * C::kBK;
-        for (int hh = 0; hh < halves(P, ch); ++hh) {
+        for (int hh = 0; hh < halves(P, ch); ++hh, ++i) {
           const int s = int(r.idx);
-          if (wait(empty(s), r.phase ^ 1u, ab, 81)) {
+          const uint32_t st = base + s * C::kSlotBytes;
+          const int m0 = ch * kWgradChunk + hh * C::kBM;
+          if (i < pre) {   // slot i, phase 0: its x and a copies are in flight
+            issued |= 1u << s;
+            tma_load(st + C::kXBytes + C::kABytes, &P.du, full(s), 0, m0, pol_keep);   // du rows m0 .. +127
+          } else if (wait(empty(s), r.phase ^ 1u, ab, 81)) {
             mbar_expect_tx(full(s), uint32_t(C::kSlotBytes));
             issued |= 1u << s;
             parities = (parities & ~(1u << s)) | (r.phase << s);
-            const uint32_t st = base + s * C::kSlotBytes;
-            const int m0 = ch * kWgradChunk + hh * C::kBM;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {   // 64-row halves: columns 0..63, then 64..127
-              tma_load(st + h2 * 16384u, &P.x, full(s), k0, m0 + 64 * h2, pol_stream);
-              tma_load(st + h2 * 16384u + 8192u, &P.x, full(s), k0 + 64, m0 + 64 * h2, pol_stream);
-            }
-            tma_load(st + C::kXBytes, &P.a, full(s), k0, 0, pol_keep);                 // a[0..RP)[k0 .. +63]
-            tma_load(st + C::kXBytes + RP * 128, &P.a, full(s), k0 + 64, 0, pol_keep); // a[0..RP)[k0+64 .. +127]
+            copy_xa(st, full(s), P, k0, m0);
             tma_load(st + C::kXBytes + C::kABytes, &P.du, full(s), 0, m0, pol_keep);   // du rows m0 .. +127
           }
           r.next<C::kSlots>();
