@@ -95,12 +95,12 @@ def measured_peaks():
 # the counters were taken on (every file under csrc/); after any change to the
 # sources the line reports null until the counters are taken again.
 NCU_TRAFFIC = {   # warm second step of `ncu --cache-control none` (profiles/train_step_M8192_K4096_N4096_R16.md)
-    "down U": {"bytes": 72_628_224, "src_hash": "7a64c8623babe949"},
-    "rows U": {"bytes": 118_016, "src_hash": "7a64c8623babe949"},
-    "up dY_lora": {"bytes": 126_273_792, "src_hash": "7a64c8623babe949"},
-    "dy dU+dB+rows dU (cluster)": {"bytes": 80_580_352, "src_hash": "7a64c8623babe949"},
-    "dX+dA": {"bytes": 198_195_456, "src_hash": "7a64c8623babe949"},
-    "combine dA+dB": {"bytes": 4_429_568, "src_hash": "7a64c8623babe949"},
+    "down U": {"bytes": 72_551_936, "src_hash": "adc8988410d035d4"},
+    "rows U": {"bytes": 124_416, "src_hash": "adc8988410d035d4"},
+    "up dY_lora": {"bytes": 125_898_496, "src_hash": "adc8988410d035d4"},
+    "dy dU+dB+rows dU (cluster)": {"bytes": 80_691_712, "src_hash": "adc8988410d035d4"},
+    "dX+dA": {"bytes": 197_936_896, "src_hash": "adc8988410d035d4"},
+    "combine dA+dB": {"bytes": 4_846_080, "src_hash": "adc8988410d035d4"},
 }
 
 
