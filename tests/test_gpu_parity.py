@@ -47,6 +47,36 @@ def test_integer_inputs_are_bitwise_equal_to_the_oracle(oracle, M, K, N, R):
         G.assert_bitwise(k, out[k], g[k])
 
 
+def _fuzz_shapes(n, seed=20261202):
+    """Seeded random ragged shapes: M in [1, 900], K and N multiples of 8 up to 1600, ranks 8
+    and 16 (dX and dA in one launch) and 24 / 32 (separate launches), alpha 2, 0.5 or 1 (the
+    dV pass-through)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(rng.integers(1, 901))
+        K, N = (8 * int(v) for v in rng.integers(1, 201, size=2))
+        R = (8, 16, 16, 24, 32)[i % 5]
+        out.append((M, K, N, R, (2.0, 0.5, 1.0)[i % 3]))
+    return out
+
+
+@pytest.mark.parametrize("M,K,N,R,alpha", _fuzz_shapes(15))
+def test_random_ragged_shapes_bitwise_on_integer_inputs(oracle, M, K, N, R, alpha):
+    """Small-integer inputs at random ragged shapes (every partial sum exact): every output of
+    the forward and the backward equals the oracle bit for bit, whatever the shape's tails,
+    unit counts against the SM count, ring-slot counts and launch schedule."""
+    w = S.integers(M, K, N, R, alpha, bound=2)
+    d = w.generate(7)
+    out = G.run(d, alpha)
+    f = oracle.fwd(d["x"], d["a"], d["b"], alpha)
+    g = oracle.bwd(d["dy"], d["x"], d["a"], d["b"], f["u"], alpha)
+    for k in ("u", "delta_y"):
+        G.assert_bitwise(k, out[k], f[k])
+    for k in ("du", "db", "dx", "da"):
+        G.assert_bitwise(k, out[k], g[k])
+
+
 EDGE = [  # (M, K, N, R, alpha): ragged M / K / N tails, every padded rank, single rows, one-tile and many-tile cases
     (1, 64, 64, 8, 2.0), (7, 136, 96, 16, 0.5), (100, 200, 104, 24, 1.0), (129, 512, 264, 32, 2.0),
     (300, 1032, 520, 40, 0.75), (257, 256, 128, 48, 1.5), (65, 8, 8, 56, 2.0), (600, 2056, 300 - 4, 64, 1.0),
