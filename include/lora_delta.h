@@ -57,7 +57,9 @@
  *       word 2  test hook, 0 for normal use: a kernel kind (1 down-projection,
  *               2 up-projection / dX, 3 fused dU + dB pass, 4 weight gradients)
  *               whose producer warp first waits on a barrier that nothing
- *               completes, so that the wait runs out (failure-path tests).
+ *               completes, so that the wait runs out (failure-path tests; the
+ *               launch that writes dX and the dA partials for R <= 16 answers
+ *               to kinds 2 and 4).
  *       word 3  test hook, 0 for normal use: the wait limit in microseconds.
  *     The library never writes words 2 and 3. A workspace must not be shared
  *     by calls that may run concurrently.
@@ -252,14 +254,15 @@ lora_status lora_delta_set_profile_events(void *const *events, int count);
  * result bit -- every schedule runs the same leaves, trees and rounding
  * points). The operator's steps can be grouped into launches three ways:
  *   LORA_SCHEDULE_SEPARATE: forward down-projection, rows, up-projection;
- *     backward dU + dB pass, rows (with the dB tree), dX, dA, combine.
+ *     backward dU + dB pass, rows (with the dB tree), dX and the dA partials
+ *     (one launch for R <= 16, two above), combine.
  *   LORA_SCHEDULE_CLUSTER_REDUCE: the reductions that feed a BF16 row on
  *     thread-block clusters -- a cluster of `cluster_size` CTAs shares each
  *     128-row tile (forward: U partials and the U rows) or 256-row chunk
  *     (backward, R <= 16: the dU + dB pass and the dU rows), the CTAs meeting
  *     at mbarriers in each other's shared memory instead of at a launch
- *     boundary -- then the expansions and dA as separate launches and one
- *     combine launch for dA and dB.
+ *     boundary -- then the expansion (forward) or the dX and dA launch
+ *     (backward) and one combine launch for dA and dB.
  *   LORA_SCHEDULE_CLUSTER_SINGLE: the forward in one cluster launch (each CTA
  *     also expands its share of the tile's columns of delta_y); the backward
  *     (R <= 16) in one cluster launch (each CTA also writes its share of dX and
