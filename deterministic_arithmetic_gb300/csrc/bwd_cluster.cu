@@ -53,7 +53,7 @@ struct BcCfg {
   static constexpr int kXBytes = 128 * 128 * 2;            // 32 KB
   static constexpr int kABytes = RP * 128 * 2;             // 4 KB
   static constexpr int kSlotBytes = kTileBytes + 2 * kWBytes;   // 40 KB (phase C uses 36 KB)
-  static constexpr int kSlots = PC ? 4 : 5;
+  static constexpr int kSlots = 4;                         // five measured slower without phase C
   static constexpr int kLeaves = 8;                        // 16-term leaves per 128 of the reduction
   static constexpr int kTCols = 256, kTSlots = 2;          // TMEM ring
   static constexpr int kSliceTiles = kDySlice / 128;       // column tiles per dU slice
