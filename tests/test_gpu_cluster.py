@@ -196,6 +196,9 @@ BWD_SHAPES = [  # (M, K, N, R, alpha): R 8 and 16, ragged M / K / N, one row, ch
     (1, 64, 64, 8, 2.0), (7, 136, 96, 16, 0.5), (300, 1032, 520, 16, 0.75), (129, 512, 264, 8, 2.0),
     (257, 4104, 136, 16, 1.5), (1000, 96, 2048, 16, 3.0), (2048, 5120, 1024, 16, 1.0),
     (640, 1024, 17408, 16, 0.5), (12000, 1032, 1024, 16, 2.0),
+    # more than 8 dU slices with 256-row units (four lanes per value in the rows step; clusters
+    # of 4 and 8, and the automatic schedule, take 256-row units here, clusters of 2 128-row ones)
+    (7500, 256, 4616, 16, 2.0),
 ]
 
 
