@@ -74,25 +74,6 @@ struct BcCfg {
   static_assert(kSmem < 227 * 1024, "one CTA per SM");
 };
 
-// tree over 4 leaves (8 columns each) starting at TMEM column `taddr`, 16 columns apart
-__device__ __forceinline__ void bc_leaves4(uint32_t taddr, bool ok, float (&o)[8]) {
-  uint32_t v[4][8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[j][e] = 0u;
-  if (ok) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tmem_ld8(taddr + j * 16, v[j]);
-    tmem_ld_wait();
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    o[c] = tree4(__uint_as_float(v[0][c]), __uint_as_float(v[1][c]), __uint_as_float(v[2][c]), __uint_as_float(v[3][c]));
-}
-
 // PC = false: phase A and the dU rows only (each CTA forms and stores its share of the chunk's
 // rows); dX and the dA partials then run as the separate up-projection and weight-gradient launches.
 // UR: rows of a unit, a 256-row chunk or (PC = false only) one 128-row tile, whose dB tree is then
@@ -346,12 +327,12 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
               tc_fence_after();
               const uint32_t ta = tq + t.idx * C::kTCols + h * C::kCPT;
               float x0[8], x1[8];
-              bc_leaves4(ta, ok, x0);                               // dU leaves 0..3
-              bc_leaves4(ta + 4 * RP, ok, x1);                      // dU leaves 4..7
+              leaves4_tree(ta, ok, x0);                             // dU leaves 0..3
+              leaves4_tree(ta + 4 * RP, ok, x1);                    // dU leaves 4..7
 #pragma unroll
               for (int c = 0; c < C::kCPT; ++c) dun[c] = __fadd_rn(x0[c], x1[c]);
-              bc_leaves4(ta + C::kLeaves * RP, ok, x0);             // dB leaves 0..3
-              bc_leaves4(ta + C::kLeaves * RP + 4 * RP, ok, x1);    // dB leaves 4..7
+              leaves4_tree(ta + C::kLeaves * RP, ok, x0);           // dB leaves 0..3
+              leaves4_tree(ta + C::kLeaves * RP + 4 * RP, ok, x1);  // dB leaves 4..7
 #pragma unroll
               for (int c = 0; c < C::kCPT; ++c) dbn[c] = __fadd_rn(x0[c], x1[c]);
               tc_fence_before();
@@ -446,8 +427,8 @@ __global__ void __launch_bounds__(BcCfg<PC>::kThreads, 1)
             tc_fence_after();
             const uint32_t ta = tq + t.idx * C::kTCols;
             float x0[8], x1[8];
-            bc_leaves4(ta + h * C::kCPT, ok, x0);              // dA leaves 0..3 (rows 0..63 of the half)
-            bc_leaves4(ta + h * C::kCPT + 4 * RP, ok, x1);     // dA leaves 4..7
+            leaves4_tree(ta + h * C::kCPT, ok, x0);           // dA leaves 0..3 (rows 0..63 of the half)
+            leaves4_tree(ta + h * C::kCPT + 4 * RP, ok, x1);  // dA leaves 4..7
 #pragma unroll
             for (int c = 0; c < C::kCPT; ++c) dan[c] = __fadd_rn(x0[c], x1[c]);
             // dX rows hh * 128 + q * 32 + lane, columns kt * 128 + h * 64 .. + 63: two 32-column boxes

@@ -415,6 +415,27 @@ __device__ __forceinline__ float tree4(float l0, float l1, float l2, float l3) {
   return __fadd_rn(__fadd_rn(l0, l1), __fadd_rn(l2, l3));
 }
 
+// The canonical tree over 4 consecutive leaves of 8 columns each, read from TMEM starting at
+// column `taddr`, leaves 16 columns apart (this warp's lane quarter): o[c] = tree4 of column c
+// of the four leaves. !ok: no TMEM access, o = 0 (an aborting CTA).
+__device__ __forceinline__ void leaves4_tree(uint32_t taddr, bool ok, float (&o)[8]) {
+  uint32_t v[4][8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[j][e] = 0u;
+  if (ok) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tmem_ld8(taddr + j * 16, v[j]);
+    tmem_ld_wait();
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) reg_fence(v[j]);
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    o[c] = tree4(__uint_as_float(v[0][c]), __uint_as_float(v[1][c]), __uint_as_float(v[2][c]), __uint_as_float(v[3][c]));
+}
+
 // ------------------------------------------------ slice partials -> BF16 tile
 // Canonical pairwise tree over the first n (<= NB, NB a power of two) of NB
 // slices, for G groups of 8 consecutive FP32 values: group g of slice i is

@@ -56,25 +56,6 @@ struct XaCfg {
   static_assert(kSmem <= 227 * 1024, "one CTA per SM");
 };
 
-// tree over 4 dA leaves (8 columns each) starting at TMEM column `taddr`, 16 columns apart
-__device__ __forceinline__ void xa_leaves4(uint32_t taddr, bool ok, float (&o)[8]) {
-  uint32_t v[4][8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[j][e] = 0u;
-  if (ok) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tmem_ld8(taddr + j * 16, v[j]);
-    tmem_ld_wait();
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    o[c] = tree4(__uint_as_float(v[0][c]), __uint_as_float(v[1][c]), __uint_as_float(v[2][c]), __uint_as_float(v[3][c]));
-}
-
 // GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
 template <bool GR>
 __global__ void __launch_bounds__(XaCfg::kThreads, 1)
@@ -269,8 +250,8 @@ __global__ void __launch_bounds__(XaCfg::kThreads, 1)
           tc_fence_after();
           const uint32_t ta = tq + t.idx * C::kTCols;
           float x0[8], x1[8];
-          xa_leaves4(ta + h * C::kCPT, ok, x0);              // dA leaves 0..3 (rows 0..63 of the half)
-          xa_leaves4(ta + h * C::kCPT + 4 * RP, ok, x1);     // dA leaves 4..7
+          leaves4_tree(ta + h * C::kCPT, ok, x0);           // dA leaves 0..3 (rows 0..63 of the half)
+          leaves4_tree(ta + h * C::kCPT + 4 * RP, ok, x1);  // dA leaves 4..7
 #pragma unroll
           for (int c = 0; c < C::kCPT; ++c) dan[c] = __fadd_rn(x0[c], x1[c]);
           // dX rows hh * 128 + q * 32 + lane, columns kt * 128 + h * 64 .. + 63: two 32-column boxes

@@ -54,25 +54,6 @@ struct DyCfg {
   static_assert(kSmem < 256 * 1024, "descriptor start addresses must fit their 14-bit field");
 };
 
-// tree over 4 leaves (8 columns each) starting at TMEM column `col`, 16 columns apart
-__device__ __forceinline__ void leaves4(uint32_t taddr, bool ok, float (&o)[8]) {
-  uint32_t v[4][8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[j][e] = 0u;
-  if (ok) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tmem_ld8(taddr + j * 16, v[j]);
-    tmem_ld_wait();
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) reg_fence(v[j]);
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    o[c] = tree4(__uint_as_float(v[0][c]), __uint_as_float(v[1][c]), __uint_as_float(v[2][c]), __uint_as_float(v[3][c]));
-}
-
 // GR: a grouped launch (several sites); otherwise the table holds one site, read at fixed offsets
 template <bool GR>
 __global__ void __launch_bounds__(DyCfg::kThreads, 1)
@@ -259,12 +240,12 @@ __global__ void __launch_bounds__(DyCfg::kThreads, 1)
             tc_fence_after();
             const uint32_t ta = tq + g.idx * C::kGroupCols;
             float x0[8], x1[8];
-            leaves4(ta, ok, x0);                               // dU leaves 0..3
-            leaves4(ta + 4 * RP, ok, x1);                      // dU leaves 4..7
+            leaves4_tree(ta, ok, x0);                             // dU leaves 0..3
+            leaves4_tree(ta + 4 * RP, ok, x1);                    // dU leaves 4..7
 #pragma unroll
             for (int c = 0; c < C::kCPT; ++c) dun[c] = __fadd_rn(x0[c], x1[c]);
-            leaves4(ta + C::kLeaves * RP, ok, x0);             // dB leaves 0..3
-            leaves4(ta + C::kLeaves * RP + 4 * RP, ok, x1);    // dB leaves 4..7
+            leaves4_tree(ta + C::kLeaves * RP, ok, x0);           // dB leaves 0..3
+            leaves4_tree(ta + C::kLeaves * RP + 4 * RP, ok, x1);  // dB leaves 4..7
 #pragma unroll
             for (int c = 0; c < C::kCPT; ++c) dbn[c] = __fadd_rn(x0[c], x1[c]);
             tc_fence_before();
